@@ -1,0 +1,574 @@
+#!/usr/bin/env python
+"""Benchmark of the FP4 weight-only (W4A16) decode GEMM on synthetic weights.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the hot path over one batch of each
+size M of the workload: for every M, every projection of the workload is called once (the
+decode MLP of the default workload: fused gate_up then down), each call on its own copy of
+the weights so that the bytes streamed per step exceed the L2 cache.  `value` is algorithmic
+HBM bytes per second (packed codes + scales + global + bf16 activations), whole job.
+
+N > 1 runs independent replicas (one process per GPU, launched by torchrun): the layer does
+not exchange data between GPUs, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from dataclasses import dataclass, field
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+METRIC = "FP4 W4A16 decode GEMM: HBM GB/s (% of GB300 peak) and µs/call at M=1–8"
+NVFP4, MXFP4 = 0, 1
+GROUP = {NVFP4: 16, MXFP4: 32}
+L2_BYTES = 129 * 10 ** 6
+ROLE_W, ROLE_A, ROLE_GATE, ROLE_UP = 1, 2, 11, 12
+
+
+def _tid(workload: int, layer: int, role: int, extra: int = 0) -> int:
+    # same id scheme as synth.tensor_id (kept local so the GPU leg imports no test module)
+    return (workload << 40) | (layer << 24) | (role << 8) | extra
+
+
+@dataclass
+class Proj:
+    name: str
+    K: int
+    N: int = 0
+    I: int = 0          # fused gate_up: N = 2 * I
+    wid: int = 0
+    layer: int = 0
+    role: int = ROLE_W
+
+    def __post_init__(self):
+        if self.I:
+            self.N = 2 * self.I
+
+    @property
+    def fused(self) -> bool:
+        return self.I > 0
+
+    def tid(self, role: int, extra: int = 0) -> int:
+        return _tid(self.wid, self.layer, role if role != ROLE_W else self.role, extra)
+
+
+@dataclass
+class Workload:
+    name: str
+    wid: int
+    fmt: int
+    Ms: list
+    projs: list
+    layers: int = 1
+    note: str = ""
+    extra: dict = field(default_factory=dict)
+
+
+def _algo_bytes(fmt, N, K, M):
+    return N * K // 2 + N * K // GROUP[fmt] + (4 if fmt == NVFP4 else 0) + 2 * M * K
+
+
+WORKLOADS = {
+    "nvfp4_gemm_2048x1024": Workload(
+        "nvfp4_gemm_2048x1024", 1, NVFP4, [1], [Proj("gemm", 1024, N=2048, wid=1)],
+        note="NVFP4 W4A16 single GEMM M=1, N=2048, K=1024"),
+    "mxfp4_mlp_12288x4096": Workload(
+        "mxfp4_mlp_12288x4096", 2, MXFP4, [1, 2, 4, 8],
+        [Proj("gate_up", 4096, I=12288, wid=2, role=ROLE_GATE),
+         Proj("down", 12288, N=4096, wid=2, role=13)],
+        note="MXFP4 W4A16 dense MLP decode: fused gate_up N=2x12288 K=4096, down N=4096 "
+             "K=12288, M in {1,2,4,8}"),
+    "nvfp4_lm_head_248320x2560": Workload(
+        "nvfp4_lm_head_248320x2560", 3, NVFP4, [1, 2, 4, 8],
+        [Proj("lm_head", 2560, N=248320, wid=3)],
+        note="NVFP4 packed lm_head N=248320, K=2560, M in {1,2,4,8}"),
+    "nvfp4_lm_head_248320x5120": Workload(
+        "nvfp4_lm_head_248320x5120", 6, NVFP4, [1, 2, 4, 8],
+        [Proj("lm_head", 5120, N=248320, wid=6)],
+        note="NVFP4 packed lm_head N=248320, K=5120 (0.666 GiB packed), M in {1,2,4,8}"),
+    "nvfp4_layer_sweep_5120": Workload(
+        "nvfp4_layer_sweep_5120", 4, NVFP4, [1, 2, 4, 8, 16],
+        [Proj("gate_up", 5120, I=17408, wid=4, role=ROLE_GATE),
+         Proj("down", 17408, N=5120, wid=4, role=13),
+         Proj("o_proj", 6144, N=5120, wid=4, role=14)],
+        layers=16,
+        note="NVFP4 decode layer sweep, 16 layers of distinct weights: gate_up N=2x17408 "
+             "K=5120, down N=5120 K=17408, o_proj N=5120 K=6144, M in {1,2,4,8,16}"),
+}
+DEFAULT_WORKLOAD = "mxfp4_mlp_12288x4096"
+
+
+def _layer_projs(w: Workload, layer: int):
+    out = []
+    for p in w.projs:
+        q = Proj(p.name, p.K, N=0 if p.I else p.N, I=p.I, wid=p.wid, layer=layer, role=p.role)
+        out.append(q)
+    return out
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# -------------------------------------------------------------------- GPU leg
+def _build_weights(w: Workload, copies: int, dev):
+    """GPU-side synthetic weights: bf16 N(0, 0.02) from a seeded torch generator, quantised
+    by the library's quantiser, prepacked.  Returns list over copies/layers of lists of
+    PackedWeight (one per projection)."""
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    sets = []
+    for c in range(copies):
+        layer_sets = []
+        for layer in range(w.layers):
+            ws = []
+            for p in _layer_projs(w, layer):
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(p.tid(ROLE_W, c) & 0x7FFFFFFFFFFF)
+                if p.fused:
+                    halves = []
+                    for h in range(2):
+                        Wb = (torch.randn((p.I, p.K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+                        c_, s_, g_ = vt.quantize(Wb, w.fmt)
+                        halves.append((c_, s_, float(g_.item())))
+                        del Wb
+                    ws.append(vt.PackedWeight.gate_up(halves[0], halves[1], w.fmt, p.I, p.K))
+                else:
+                    Wb = (torch.randn((p.N, p.K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+                    c_, s_, g_ = vt.quantize(Wb, w.fmt)
+                    del Wb
+                    ws.append(vt.PackedWeight.from_codes(c_, s_, float(g_.item()), w.fmt, p.N, p.K))
+            layer_sets.append(ws)
+        sets.append(layer_sets)
+    torch.cuda.synchronize()
+    return sets
+
+
+def _copies_needed(w: Workload) -> int:
+    per_copy = sum(_algo_bytes(w.fmt, p.N, p.K, 0) for p in w.projs) * w.layers
+    need = 1
+    # every M of a step uses its own copy when one copy does not exceed the L2 twice over
+    if per_copy < 2 * L2_BYTES:
+        need = max(len(w.Ms), int(np.ceil(2 * L2_BYTES / per_copy)))
+    return min(need, 512)
+
+
+def _calls(w: Workload, sets):
+    """The ordered calls of one step: (copy, layer, proj index, M)."""
+    copies = len(sets)
+    calls = []
+    step_copy = 0
+    for mi, M in enumerate(w.Ms):
+        for layer in range(w.layers):
+            for pi in range(len(w.projs)):
+                calls.append((step_copy % copies, layer, pi, M))
+                if copies > len(w.Ms):
+                    step_copy += 1
+        if copies <= len(w.Ms):
+            step_copy += 1
+    return calls
+
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    from fp4_weight_only_nvfp4_gb300 import build as vtbuild
+    vtbuild.build()
+
+    w = WORKLOADS[args.workload]
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    copies = _copies_needed(w)
+    sets = _build_weights(w, copies, dev)
+    calls = _calls(w, sets)
+    Mmax = max(w.Ms)
+    wsz = max(Wt.workspace_bytes(Mmax) for layer_sets in sets for ws in layer_sets for Wt in ws)
+    ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(12345 + rank)
+    Kmax = max(p.K for p in w.projs)
+    A = {(M, p.K): torch.randn((M, p.K), generator=gen, device=dev).to(torch.bfloat16)
+         for M in w.Ms for p in w.projs}
+    C = {(M, p.N): torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+         for M in w.Ms for p in w.projs}
+    stream = torch.cuda.Stream(device=dev)
+    step_bytes = sum(_algo_bytes(w.fmt, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
+    n_calls = len(calls)
+
+    def issue(timing_events=None):
+        for i, (c, layer, pi, M) in enumerate(calls):
+            p = w.projs[pi]
+            if timing_events is not None:
+                timing_events[i][0].record(stream)
+            vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
+                          stream=stream)
+            if timing_events is not None:
+                timing_events[i][1].record(stream)
+
+    # warm-up (also sets function attributes outside capture)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            issue()
+    stream.synchronize()
+    launches_per_call = sets[0][0][0].stats()["launches"]
+
+    # capture the step, with per-call event records (external event nodes) when available
+    try:
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_calls)]
+    except TypeError:
+        ev = None
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                issue(ev)
+    except Exception:  # event record nodes not supported here: time calls outside the graph
+        ev = None
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                issue(None)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    stream.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+
+    # per-call durations from the event nodes of the last replay
+    per_call = []
+    if ev is not None:
+        durs = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n_calls)]
+    else:
+        durs = []
+        for i in range(n_calls):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c, layer, pi, M = calls[i]
+            p = w.projs[pi]
+            e0.record(stream)
+            vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            durs.append(e0.elapsed_time(e1))
+    agg = {}
+    for i, (c, layer, pi, M) in enumerate(calls):
+        p = w.projs[pi]
+        key = (p.name, M)
+        b = _algo_bytes(w.fmt, p.N, p.K, M)
+        a = agg.setdefault(key, [0.0, 0, 0])
+        a[0] += durs[i]
+        a[1] += 1
+        a[2] += b
+    for (name, M), (ms, n, b) in agg.items():
+        us = ms * 1e3 / n
+        per_call.append({"proj": name, "M": M, "us_per_call": round(us, 3),
+                         "GBps": round(b / n / (us * 1e-6) / 1e9, 1)})
+    kernel_ms = sum(durs)
+    achieved = step_bytes / (kernel_ms * 1e-3) / 1e9
+
+    # end to end: pinned host activations in, host logits out, every call
+    e2e = run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist)
+    ws_status = vt.workspace_status(ws, stream)
+    return {
+        "value": value, "ms_per_step": ms_step, "step_bytes": step_bytes, "clocks": clocks,
+        "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
+        "gpu_launches": launches_per_call * n_calls * args.steps, "copies": copies,
+        "calls_per_step": n_calls, "ws_status": ws_status,
+    }
+
+
+def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    hA, dA, hC, dC = {}, {}, {}, {}
+    for M in w.Ms:
+        for p in w.projs:
+            hA[(M, p.K)] = torch.randn((M, p.K)).to(torch.bfloat16).pin_memory()
+            dA[(M, p.K)] = torch.empty((M, p.K), dtype=torch.bfloat16, device=dev)
+            hC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16).pin_memory()
+            dC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+    h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls)
+    d2h = sum(M * w.projs[pi].N * 2 for _, _, pi, M in calls)
+
+    def issue():
+        for c, layer, pi, M in calls:
+            p = w.projs[pi]
+            dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
+            vt.w4a16_gemm(dA[(M, p.K)], sets[c][layer][pi], out=dC[(M, p.N)], workspace=ws,
+                          stream=stream)
+            hC[(M, p.N)].copy_(dC[(M, p.N)], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            issue()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            issue()
+    for _ in range(3):
+        graph.replay()
+    stream.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    stream.synchronize()
+    ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+    return {"value": round(step_bytes * world / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------- CPU (oracle) leg
+def run_oracle_sample(w: Workload, target_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the workload: every (projection, M)
+    call of a step, restricted to a fixed fraction of the output columns.  Returns
+    (GB/s of algorithmic bytes, seconds, threads, description)."""
+    import oracle
+    import synth
+
+    def sample_calls(frac):
+        jobs = []
+        for M in w.Ms:
+            for p in w.projs:
+                n = max(8, int(p.N * frac))
+                jobs.append((p, M, n))
+        return jobs
+
+    prepared = {}
+
+    def prep(p, n):
+        key = (p.name, n)
+        if key not in prepared:
+            rows = np.arange(n, dtype=np.int64)
+            Wb = synth.normal_bf16_rows(0, p.tid(ROLE_W), 0.02, p.K, rows)
+            prepared[key] = oracle.quantize(w.fmt, Wb)
+        return prepared[key]
+
+    def run(frac):
+        jobs = sample_calls(frac)
+        inputs = []
+        for p, M, n in jobs:
+            c, s, G = prep(p, n)
+            Ab = synth.normal_bf16(0, p.tid(ROLE_A, M), 1.0, M, p.K)
+            inputs.append((p, M, n, Ab, c, s, G))
+        t = time.perf_counter()
+        nbytes = 0
+        for p, M, n, Ab, c, s, G in inputs:
+            oracle.gemm(w.fmt, Ab, c, s, G, n)
+            nbytes += _algo_bytes(w.fmt, n, p.K, M)
+        return nbytes, time.perf_counter() - t
+
+    frac = 1.0 / 1024
+    nbytes, dt = run(frac)
+    frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))
+    nbytes, dt = run(frac)
+    desc = (f"every (projection, M) call of one step of {w.name} on the first "
+            f"{frac * 100:.3g}% of each projection's output columns")
+    return nbytes / dt / 1e9, dt, oracle.threads(), desc
+
+
+# ------------------------------------------------------------------------ main
+def _peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _profiled_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if one
+    matches this workload (None otherwise)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get(workload)
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="vtfp4", choices=["vtfp4", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    config = {"workload": w.name, "description": w.note,
+              "format": "nvfp4" if w.fmt == NVFP4 else "mxfp4", "Ms": w.Ms,
+              "shapes": [{"proj": p.name, "N": p.N, "K": p.K} for p in w.projs],
+              "layers": w.layers}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbps, dt, threads, desc = 0.0, 0.0, 0, ""
+        per_step = []
+        for _ in range(args.warmup):
+            run_oracle_sample(w, target_s=0.5)
+        for _ in range(args.steps):
+            gbps, dt, threads, desc = run_oracle_sample(w, target_s=2.0)
+            per_step.append((gbps, dt))
+        value = statistics.median(g for g, _ in per_step)
+        ms = statistics.median(d for _, d in per_step) * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": dict(config, l2="CPU oracle; no GPU"),
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = _peak()
+    traffic = _profiled_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": round(r["value"], 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16-mma-f32-acc", "data": "synthetic",
+        "config": dict(config, parallelism=f"replicas{world}",
+                       l2=f"inputs larger than L2: {r['copies']} weight copies rotate, "
+                          f"{r['step_bytes'] / 1e6:.1f} MB streamed per step",
+                       calls_per_step=r["calls_per_step"]),
+        "roofline": {"bound": "hbm", "kernel": "k_decode (+ k_prep_a, one GEMM call)",
+                     "achieved": round(r["achieved"], 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(r["achieved"] / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic},
+        "per_call": r["per_call"],
+        "e2e": r["e2e"],
+        "gpu_launches": r["gpu_launches"],
+        "clocks": r["clocks"],
+        "workspace_status": r["ws_status"],
+    }
+    if not args.no_cpu_baseline:
+        gbps, dt, threads, desc = run_oracle_sample(w)
+        line["cpu_baseline"] = {"value": round(gbps, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

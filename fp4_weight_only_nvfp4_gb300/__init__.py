@@ -1,0 +1,181 @@
+"""GB300-native FP4 weight-only (W4A16) linear layers: NVFP4 and MXFP4 weights against bf16
+activations, for LLM decode (M <= 16) and prefill.
+
+This module is a thin binding over the C ABI of ``libvtfp4.so`` (``include/vt_fp4.h``):
+PyTorch supplies device memory and streams, every step of the computation runs in the
+library's CUDA kernels.  If the library is missing the calls raise; nothing falls back to
+PyTorch or the CPU.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import GemmOpts, LaunchInfo, VtError, check, lib
+
+NVFP4, MXFP4 = 0, 1
+GROUP = {NVFP4: 16, MXFP4: 32}
+
+__all__ = ["NVFP4", "MXFP4", "GROUP", "PackedWeight", "w4a16_gemm", "quantize", "prepack_bytes",
+           "workspace_status", "VtError", "algorithmic_bytes"]
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def algorithmic_bytes(fmt: int, N: int, K: int, M: int) -> int:
+    """Bytes a W4A16 call must move at minimum: packed codes N*K/2, one scale byte per group,
+    the 4-byte NVFP4 global and the bf16 activations 2*M*K (output bytes not included)."""
+    return N * K // 2 + N * K // GROUP[fmt] + (4 if fmt == NVFP4 else 0) + 2 * M * K
+
+
+def prepack_bytes(fmt: int, N: int, K: int) -> int:
+    out = ctypes.c_size_t(0)
+    check(lib().vt_fp4_prepack_bytes(fmt, N, K, ctypes.byref(out)), "vt_fp4_prepack_bytes")
+    return out.value
+
+
+class PackedWeight:
+    """A weight prepacked into the kernels' tile layout.  Owns its packed device buffer (a
+    torch uint8 tensor) and the library handle."""
+
+    def __init__(self, handle: ctypes.c_void_p, packed: torch.Tensor, fmt: int, N: int, K: int):
+        self._h = handle
+        self.packed = packed
+        self.fmt, self.N, self.K = fmt, N, K
+
+    @classmethod
+    def from_codes(cls, codes: torch.Tensor, scales: torch.Tensor, global_scale: float, fmt: int,
+                   N: int, K: int, stream=None) -> "PackedWeight":
+        """codes u8 [N, K/2] (low nibble = even k), scales u8 [N, K/g], both on the GPU."""
+        _check_src(codes, scales, N, K, fmt)
+        nbytes = prepack_bytes(fmt, N, K)
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=codes.device)
+        h = ctypes.c_void_p(0)
+        check(lib().vt_fp4_prepack(_ptr(codes), _ptr(scales), float(global_scale), fmt, N, K,
+                                   _ptr(packed), nbytes, _stream(stream), ctypes.byref(h)),
+              "vt_fp4_prepack")
+        return cls(h, packed, fmt, N, K)
+
+    @classmethod
+    def gate_up(cls, gate: tuple, up: tuple, fmt: int, I: int, K: int, stream=None) -> "PackedWeight":
+        """Fused gate_up: ``gate``/``up`` are (codes, scales, global); N = 2*I."""
+        (gc, gs, gg), (uc, us, ug) = gate, up
+        _check_src(gc, gs, I, K, fmt)
+        _check_src(uc, us, I, K, fmt)
+        nbytes = prepack_bytes(fmt, 2 * I, K)
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=gc.device)
+        h = ctypes.c_void_p(0)
+        check(lib().vt_fp4_prepack_gate_up(_ptr(gc), _ptr(gs), float(gg), _ptr(uc), _ptr(us),
+                                           float(ug), fmt, I, K, _ptr(packed), nbytes,
+                                           _stream(stream), ctypes.byref(h)),
+              "vt_fp4_prepack_gate_up")
+        return cls(h, packed, fmt, 2 * I, K)
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise ValueError("PackedWeight has been closed")
+        return self._h
+
+    def workspace_bytes(self, M_max: int) -> int:
+        out = ctypes.c_size_t(0)
+        check(lib().vt_fp4_workspace_bytes(self.handle, M_max, ctypes.byref(out)),
+              "vt_fp4_workspace_bytes")
+        return out.value
+
+    def new_workspace(self, M_max: int) -> torch.Tensor:
+        """A zeroed workspace for calls with M <= M_max (zero once; it self-resets)."""
+        return torch.zeros(self.workspace_bytes(M_max), dtype=torch.uint8,
+                           device=self.packed.device)
+
+    def dequant(self, stream=None) -> torch.Tensor:
+        out = torch.empty((self.N, self.K), dtype=torch.float32, device=self.packed.device)
+        check(lib().vt_fp4_dequant(self.handle, _ptr(out), _stream(stream)), "vt_fp4_dequant")
+        return out
+
+    def unpack(self, stream=None):
+        dev = self.packed.device
+        codes = torch.empty((self.N, self.K // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((self.N, self.K // GROUP[self.fmt]), dtype=torch.uint8, device=dev)
+        check(lib().vt_fp4_unpack(self.handle, _ptr(codes), _ptr(scales), _stream(stream)),
+              "vt_fp4_unpack")
+        return codes, scales
+
+    def stats(self) -> dict:
+        info = LaunchInfo()
+        check(lib().vt_fp4_stats(self.handle, ctypes.byref(info)), "vt_fp4_stats")
+        return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+    def close(self) -> None:
+        if self._h:
+            lib().vt_fp4_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _check_src(codes, scales, N, K, fmt):
+    if codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
+        raise TypeError("codes and scales must be uint8 tensors")
+    if not (codes.is_cuda and scales.is_cuda and codes.is_contiguous() and scales.is_contiguous()):
+        raise ValueError("codes and scales must be contiguous CUDA tensors")
+    if codes.numel() != N * K // 2 or scales.numel() != N * K // GROUP[fmt]:
+        raise ValueError("codes/scales sizes do not match N and K")
+
+
+def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, stream=None,
+               opts: dict | None = None) -> torch.Tensor:
+    """out[M, N] (bf16) = A[M, K] (bf16) . W^T, fp32 accumulation, on the library's kernels."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = W.new_workspace(M)
+    o = None
+    if opts:
+        o = GemmOpts(int(opts.get("grid", 0)), int(opts.get("warps", 0)),
+                     int(opts.get("stages", 0)), int(opts.get("force_path", 0)))
+    check(lib().vt_fp4_w4a16_gemm_ex(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
+                                     out.stride(0), _ptr(workspace), workspace.numel(),
+                                     _stream(stream), ctypes.byref(o) if o else None),
+          "vt_fp4_w4a16_gemm")
+    return out
+
+
+def workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    st = ctypes.c_int(0)
+    check(lib().vt_fp4_workspace_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
+          "vt_fp4_workspace_status")
+    return st.value
+
+
+def quantize(W: torch.Tensor, fmt: int, stream=None):
+    """Quantise a bf16 [N, K] CUDA tensor: returns (codes u8 [N, K/2], scales u8 [N, K/g],
+    global fp32 tensor [1] (1.0 for MXFP4))."""
+    if W.dtype != torch.bfloat16 or W.dim() != 2 or not W.is_contiguous() or not W.is_cuda:
+        raise ValueError("W must be a contiguous bf16 CUDA [N, K] tensor")
+    N, K = W.shape
+    dev = W.device
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, K // GROUP[fmt]), dtype=torch.uint8, device=dev)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    scratch = torch.empty(16, dtype=torch.uint8, device=dev)
+    check(lib().vt_fp4_quantize(_ptr(W), N, K, fmt, _ptr(codes), _ptr(scales), _ptr(g),
+                                _ptr(scratch), _stream(stream)), "vt_fp4_quantize")
+    return codes, scales, g

@@ -1,0 +1,378 @@
+// C ABI of libvtfp4 (declared in include/vt_fp4.h): argument checks, handle state, launch
+// shape selection and kernel launches.  Every check that needs no GPU runs before any
+// CUDA call, so bad arguments are rejected the same way on a host without a device.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "../../include/vt_fp4.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace vt;
+
+struct vt_fp4_weight_s {
+  int fmt;
+  int64_t N, K, RT, KT;
+  int64_t seg_split;
+  const void* packed;
+  size_t packed_bytes;
+  vt_fp4_launch_info info;
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+vt_status fail(vt_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+vt_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(VT_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+inline int group_of(int fmt) { return fmt == VT_FP4_NVFP4 ? 16 : 32; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+vt_status check_shape(vt_fp4_format fmt, int64_t N, int64_t K) {
+  if (fmt != VT_FP4_NVFP4 && fmt != VT_FP4_MXFP4)
+    return fail(VT_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+  if (N <= 0 || K <= 0) return fail(VT_ERR_INVALID_ARG, "N and K must be > 0 (N=%lld K=%lld)",
+                                    (long long)N, (long long)K);
+  if (K % group_of(fmt))
+    return fail(VT_ERR_INVALID_ARG, "K=%lld is not a multiple of the group size %d",
+                (long long)K, group_of(fmt));
+  if (N > (int64_t)1 << 31 || K > (int64_t)1 << 24)
+    return fail(VT_ERR_UNSUPPORTED, "N or K too large (N=%lld K=%lld)", (long long)N,
+                (long long)K);
+  return VT_OK;
+}
+
+size_t packed_size(int fmt, int64_t N, int64_t K) {
+  return (size_t)kHeaderBytes +
+         (size_t)cdiv(N, kTileRows) * cdiv(K, kTileK) * tile_bytes(fmt);
+}
+
+// Workspace layout shared by vt_fp4_workspace_bytes and the GEMM.
+struct WsLayout {
+  size_t status, counters, rowscale, ap, partials, total;
+};
+
+WsLayout ws_layout(const vt_fp4_weight_s* W, int64_t M) {
+  WsLayout L;
+  const int64_t Kp = W->KT * kTileK;
+  const int64_t mrows = M <= 16 ? 16 : cdiv(M, 128) * 128;
+  L.status = 0;
+  L.counters = 256;
+  L.rowscale = up256(L.counters + (size_t)W->RT * 4);
+  L.ap = up256(L.rowscale + (size_t)mrows * 4);
+  L.partials = up256(L.ap + (size_t)mrows * Kp * 2);
+  const size_t part = M <= 16 ? (size_t)kMaxDecodeGrid * 2 * 16 * 128 * 4 : 0;
+  L.total = up256(L.partials + part);
+  return L;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+vt_status do_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
+                     const float globals[2], int nsrc, vt_fp4_format fmt, int64_t I, int64_t K,
+                     void* dst, size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out) {
+  if (!out) return fail(VT_ERR_INVALID_ARG, "out handle pointer is NULL");
+  *out = nullptr;
+  const int64_t N = I * nsrc;
+  vt_status st = check_shape(fmt, N, K);
+  if (st) return st;
+  for (int i = 0; i < nsrc; ++i) {
+    if (!codes[i] || !scales[i]) return fail(VT_ERR_INVALID_ARG, "codes/scales pointer is NULL");
+    if (fmt == VT_FP4_NVFP4) {
+      if (!(isfinite(globals[i]) && globals[i] > 0.0f))
+        return fail(VT_ERR_INVALID_ARG, "NVFP4 global scale must be finite and > 0 (got %g)",
+                    (double)globals[i]);
+    } else if (globals[i] != 1.0f) {
+      return fail(VT_ERR_INVALID_ARG, "MXFP4 has no global scale: pass 1.0 (got %g)",
+                  (double)globals[i]);
+    }
+  }
+  if (!dst) return fail(VT_ERR_INVALID_ARG, "packed_dst is NULL");
+  if (!aligned(dst, 16)) return fail(VT_ERR_MISALIGNED, "packed_dst must be 16-byte aligned");
+  const size_t need = packed_size(fmt, N, K);
+  if (dst_bytes < need)
+    return fail(VT_ERR_INVALID_ARG, "packed_dst holds %zu bytes, %zu needed", dst_bytes, need);
+
+  vt_fp4_weight_s* h = new (std::nothrow) vt_fp4_weight_s();
+  if (!h) return fail(VT_ERR_INVALID_ARG, "out of host memory");
+  h->fmt = fmt;
+  h->N = N;
+  h->K = K;
+  h->RT = cdiv(N, kTileRows);
+  h->KT = cdiv(K, kTileK);
+  h->seg_split = nsrc == 2 ? I : N;
+  h->packed = dst;
+  h->packed_bytes = need;
+  memset(&h->info, 0, sizeof(h->info));
+  const uint8_t* c2[2] = {codes[0], nsrc == 2 ? codes[1] : codes[0]};
+  const uint8_t* s2[2] = {scales[0], nsrc == 2 ? scales[1] : scales[0]};
+  const float f1 = nsrc == 2 ? globals[1] : globals[0];
+  cudaError_t e = launch_prepack(c2, s2, h->seg_split, globals[0], f1, fmt, N, K, h->RT, h->KT,
+                                 dst, (cudaStream_t)s);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "prepack launch");
+  }
+  *out = h;
+  return VT_OK;
+}
+
+vt_status check_handle(vt_fp4_handle W) {
+  if (!W) return fail(VT_ERR_INVALID_ARG, "weight handle is NULL");
+  return VT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vt_fp4_last_error(void) { return g_err; }
+
+vt_status vt_fp4_prepack_bytes(vt_fp4_format fmt, int64_t N, int64_t K, size_t* packed_bytes) {
+  if (!packed_bytes) return fail(VT_ERR_INVALID_ARG, "packed_bytes is NULL");
+  vt_status st = check_shape(fmt, N, K);
+  if (st) return st;
+  *packed_bytes = packed_size(fmt, N, K);
+  return VT_OK;
+}
+
+vt_status vt_fp4_prepack(const uint8_t* codes, const uint8_t* scales, float global_scale,
+                         vt_fp4_format fmt, int64_t N, int64_t K, void* packed_dst,
+                         size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out) {
+  const uint8_t* c[2] = {codes, codes};
+  const uint8_t* sc[2] = {scales, scales};
+  const float g[2] = {global_scale, global_scale};
+  return do_prepack(c, sc, g, 1, fmt, N, K, packed_dst, dst_bytes, s, out);
+}
+
+vt_status vt_fp4_prepack_gate_up(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                 float gate_global, const uint8_t* up_codes,
+                                 const uint8_t* up_scales, float up_global, vt_fp4_format fmt,
+                                 int64_t I, int64_t K, void* packed_dst, size_t dst_bytes,
+                                 vt_stream_t s, vt_fp4_handle* out) {
+  const uint8_t* c[2] = {gate_codes, up_codes};
+  const uint8_t* sc[2] = {gate_scales, up_scales};
+  const float g[2] = {gate_global, up_global};
+  return do_prepack(c, sc, g, 2, fmt, I, K, packed_dst, dst_bytes, s, out);
+}
+
+vt_status vt_fp4_destroy(vt_fp4_handle W) {
+  delete W;
+  return VT_OK;
+}
+
+vt_status vt_fp4_shape(vt_fp4_handle W, vt_fp4_format* fmt, int64_t* N, int64_t* K) {
+  if (vt_status st = check_handle(W)) return st;
+  if (fmt) *fmt = (vt_fp4_format)W->fmt;
+  if (N) *N = W->N;
+  if (K) *K = W->K;
+  return VT_OK;
+}
+
+vt_status vt_fp4_workspace_bytes(vt_fp4_handle W, int64_t M_max, size_t* bytes) {
+  if (vt_status st = check_handle(W)) return st;
+  if (!bytes) return fail(VT_ERR_INVALID_ARG, "bytes is NULL");
+  if (M_max < 0) return fail(VT_ERR_INVALID_ARG, "M_max must be >= 0");
+  WsLayout a = ws_layout(W, M_max < 1 ? 1 : M_max);
+  size_t tot = a.total;
+  if (M_max > 16) {  // a workspace sized for M_max also serves every smaller M
+    WsLayout d = ws_layout(W, 16);
+    if (d.total > tot) tot = d.total;
+  }
+  *bytes = tot;
+  return VT_OK;
+}
+
+vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
+                               int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
+                               const vt_fp4_gemm_opts* opts) {
+  if (vt_status st = check_handle(W)) return st;
+  if (M < 0) return fail(VT_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
+  if (M == 0) return VT_OK;
+  if (!A || !C || !workspace) return fail(VT_ERR_INVALID_ARG, "A, C and workspace must be set");
+  if (lda < W->K || ldc < W->N)
+    return fail(VT_ERR_INVALID_ARG, "lda (%lld) must be >= K and ldc (%lld) >= N",
+                (long long)lda, (long long)ldc);
+  if (!aligned(A, 16) || lda % 8)
+    return fail(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda %% 8 == 0");
+  if (!aligned(C, 4) || ldc % 2) return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
+  if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  const int force = opts ? opts->force_path : 0;
+  const bool decode = force ? force == 1 : M <= 16;
+  if (force == 1 && M > 16) return fail(VT_ERR_INVALID_ARG, "decode path needs M <= 16");
+  if (W->K > 110000) return fail(VT_ERR_UNSUPPORTED, "K > 110000 is not supported");
+  WsLayout L = ws_layout(W, decode ? (M < 16 ? M : 16) : M);
+  if (ws_bytes < L.total)
+    return fail(VT_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, L.total);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+
+  if (decode) {
+    DecodeLaunch D;
+    D.packed = W->packed;
+    D.fmt = W->fmt;
+    D.N = W->N;
+    D.K = W->K;
+    D.RT = W->RT;
+    D.KT = W->KT;
+    D.seg_split = W->seg_split;
+    D.A = A;
+    D.lda = lda;
+    D.M = (int)M;
+    D.C = C;
+    D.ldc = ldc;
+    D.status = reinterpret_cast<int*>(ws + L.status);
+    D.counters = reinterpret_cast<int*>(ws + L.counters);
+    D.rowscale = reinterpret_cast<float*>(ws + L.rowscale);
+    D.Ap = ws + L.ap;
+    D.partials = reinterpret_cast<float*>(ws + L.partials);
+    const int64_t items = W->RT * W->KT;
+    int warps = (opts && opts->warps) ? opts->warps : 8;
+    if (warps != 4 && warps != 8) return fail(VT_ERR_INVALID_ARG, "warps must be 4 or 8");
+    const int mt = decode_mt((int)M);
+    int stages = (opts && opts->stages) ? opts->stages : (mt == 8 ? 4 : 3);
+    if (stages < 2 || stages > 6) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 6]");
+    if (decode_smem_bytes(W->fmt, mt, warps, stages) > 227 * 1024)
+      return fail(VT_ERR_INVALID_ARG, "warps x stages exceed shared memory");
+    int64_t grid = (opts && opts->grid) ? opts->grid : sm_count();
+    if (!(opts && opts->grid)) grid = grid < cdiv(items, warps) ? grid : cdiv(items, warps);
+    if (grid > items) grid = items;
+    if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
+    if (grid < 1) grid = 1;
+    D.grid = (int)grid;
+    D.warps = warps;
+    D.stages = stages;
+    int launches = 0;
+    cudaError_t e = launch_decode(D, (cudaStream_t)s, &launches);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    W->info.path = 1;
+    W->info.grid = D.grid;
+    W->info.warps_per_cta = warps;
+    W->info.m_tile = mt;
+    W->info.items = items;
+    W->info.launches = launches;
+    W->info.calls += 1;
+    return VT_OK;
+  }
+  PrefillLaunch P;
+  P.packed = W->packed;
+  P.fmt = W->fmt;
+  P.N = W->N;
+  P.K = W->K;
+  P.RT = W->RT;
+  P.KT = W->KT;
+  P.seg_split = W->seg_split;
+  P.A = A;
+  P.lda = lda;
+  P.M = M;
+  P.C = C;
+  P.ldc = ldc;
+  P.status = reinterpret_cast<int*>(ws + L.status);
+  P.rowscale = reinterpret_cast<float*>(ws + L.rowscale);
+  P.Ap = ws + L.ap;
+  P.grid = (opts && opts->grid) ? opts->grid : sm_count();
+  int launches = 0, grid = 0;
+  int64_t tiles = 0;
+  cudaError_t e = launch_prefill(P, (cudaStream_t)s, &launches, &grid, &tiles);
+  if (e == cudaErrorNotSupported)
+    return fail(VT_ERR_UNSUPPORTED, "the prefill tile path is not available in this build");
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  W->info.path = 2;
+  W->info.grid = grid;
+  W->info.warps_per_cta = 0;
+  W->info.m_tile = 128;
+  W->info.items = tiles;
+  W->info.launches = launches;
+  W->info.calls += 1;
+  return VT_OK;
+}
+
+vt_status vt_fp4_w4a16_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
+                            int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s) {
+  return vt_fp4_w4a16_gemm_ex(A, M, lda, W, C, ldc, workspace, ws_bytes, s, nullptr);
+}
+
+vt_status vt_fp4_workspace_status(void* workspace, vt_stream_t s, int* status) {
+  if (!workspace || !status) return fail(VT_ERR_INVALID_ARG, "workspace and status must be set");
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
+  *status = v;
+  if (v) {
+    const int zero = 0;
+    e = cudaMemcpyAsync(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice, (cudaStream_t)s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
+  }
+  return VT_OK;
+}
+
+vt_status vt_fp4_stats(vt_fp4_handle W, vt_fp4_launch_info* info) {
+  if (vt_status st = check_handle(W)) return st;
+  if (!info) return fail(VT_ERR_INVALID_ARG, "info is NULL");
+  *info = W->info;
+  return VT_OK;
+}
+
+vt_status vt_fp4_dequant(vt_fp4_handle W, float* out, vt_stream_t s) {
+  if (vt_status st = check_handle(W)) return st;
+  if (!out) return fail(VT_ERR_INVALID_ARG, "out is NULL");
+  cudaError_t e = launch_dequant(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split, out,
+                                 (cudaStream_t)s);
+  return e == cudaSuccess ? VT_OK : cuda_fail(e, "dequant launch");
+}
+
+vt_status vt_fp4_unpack(vt_fp4_handle W, uint8_t* codes, uint8_t* scales, vt_stream_t s) {
+  if (vt_status st = check_handle(W)) return st;
+  if (!codes || !scales) return fail(VT_ERR_INVALID_ARG, "codes and scales must be set");
+  cudaError_t e = launch_unpack(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split, codes,
+                                scales, (cudaStream_t)s);
+  return e == cudaSuccess ? VT_OK : cuda_fail(e, "unpack launch");
+}
+
+vt_status vt_fp4_quantize(const void* Wt, int64_t N, int64_t K, vt_fp4_format fmt,
+                          uint8_t* codes, uint8_t* scales, float* global_out, void* scratch,
+                          vt_stream_t s) {
+  vt_status st = check_shape(fmt, N, K);
+  if (st) return st;
+  if (!Wt || !codes || !scales || !scratch)
+    return fail(VT_ERR_INVALID_ARG, "W, codes, scales and scratch must be set");
+  if (fmt == VT_FP4_NVFP4 && !global_out)
+    return fail(VT_ERR_INVALID_ARG, "NVFP4 needs global_out");
+  if (!aligned(Wt, 16) || !aligned(scratch, 16) || !aligned(codes, 16))
+    return fail(VT_ERR_MISALIGNED, "W, codes and scratch must be 16-byte aligned");
+  cudaError_t e = launch_quantize(Wt, N, K, fmt, codes, scales, global_out, scratch,
+                                  (cudaStream_t)s);
+  return e == cudaSuccess ? VT_OK : cuda_fail(e, "quantize launch");
+}
+
+}  // extern "C"

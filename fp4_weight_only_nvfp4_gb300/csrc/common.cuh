@@ -1,0 +1,204 @@
+// Shared device-side definitions of libvtfp4: the prepacked tile layout and small PTX
+// wrappers (TMA bulk copies, mbarriers, FP4/FP8 conversions, mma.sync).
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vt {
+
+// ------------------------------------------------------------------ packed layout
+// A weight W[N][K] is stored as a 256-byte header followed by tiles of 128 rows x 64 k,
+// tile (rt, kt) at byte 256 + (rt * KT + kt) * tile_bytes, rows padded to 128 and k to 64
+// with zero bytes.  Inside a tile:
+//   codes  [8 row blocks j][32 lanes][16 B]  (4096 B).  Lane l = 4g + t, byte 4q + b:
+//          b=0: row 16j+g,   source byte kt*32 + 8t + 2q       (k = 64kt+16t+4q+{0,1})
+//          b=1: row 16j+g+8, same byte
+//          b=2: row 16j+g,   source byte kt*32 + 8t + 2q + 1   (k = 64kt+16t+4q+{2,3})
+//          b=3: row 16j+g+8, same byte
+//          i.e. word q of lane l is the f16 A-operand fragment of an m16n8k16 MMA for k
+//          step q, with the MMA's logical k columns {2t,2t+1,2t+8,2t+9} mapped onto the
+//          four consecutive physical k = 64kt+16t+4q+{0..3}.  Lane t therefore covers
+//          physical k in [16t, 16t+16) of the tile over the four steps.
+//   scales NVFP4 [32 lanes][8 j][2 B] (512 B): E4M3 bytes of rows 16j+g and 16j+g+8 for
+//          group 4kt+t (the 16 k lane t covers).
+//   scales MXFP4 [8 g][2 h][8 j][2 B] (256 B): rows 16j+g, 16j+g+8, group 2kt+h; the
+//          bytes are re-encoded as the high byte of an f16 power of two (see prepack).
+constexpr int kHeaderBytes = 256;
+constexpr int kTileRows = 128;
+constexpr int kTileK = 64;
+constexpr int kCodeBytes = 4096;
+constexpr int kScaleBytesNV = 512;
+constexpr int kScaleBytesMX = 256;
+constexpr int kTileBytesNV = kCodeBytes + kScaleBytesNV;  // 4608
+constexpr int kTileBytesMX = kCodeBytes + kScaleBytesMX;  // 4352
+
+enum { FMT_NV = 0, FMT_MX = 1 };
+
+__host__ __device__ constexpr int tile_bytes(int fmt) {
+  return fmt == FMT_NV ? kTileBytesNV : kTileBytesMX;
+}
+
+// Header written by the prepack kernels and read by the GEMM epilogue.
+struct PackedHeader {
+  uint32_t magic;      // 'VTF4'
+  uint32_t fmt;
+  int64_t N, K;
+  int64_t seg_split;   // rows [0, seg_split) use factor[0], the rest factor[1]
+  float factor[2];     // epilogue multiplier per segment (NVFP4 global, MXFP4 2^(emax-140))
+  int32_t emax[2];     // MXFP4: largest finite E8M0 byte per segment
+  uint32_t pad[52];
+};
+static_assert(sizeof(PackedHeader) == kHeaderBytes, "header size");
+constexpr uint32_t kMagic = 0x34465456u;  // "VTF4"
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D TMA bulk copy global -> shared, completion signalled on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after `limit_ns` of wall time and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Two E2M1 codes (one byte, low nibble -> low half) to f16x2, exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 lo;\n .reg .b16 h;\n cvt.u16.u32 h, %1;\n cvt.u8.u16 lo, h;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, lo;\n}"
+      : "=r"(r)
+      : "r"(byte));
+  return r;
+}
+
+// Four codes bytes of a word -> four f16x2.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t& r0, uint32_t& r1,
+                                                uint32_t& r2, uint32_t& r3) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) to f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  uint16_t h = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
+}
+
+// Two re-encoded MXFP4 scale bytes -> f16x2 (each byte is the high byte of its f16).
+__device__ __forceinline__ uint32_t mxenc2_to_f16x2(uint32_t two_bytes) {
+  return __byte_perm(two_bytes, 0u, 0x1404);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Broadcast the low / high f16 of a pair to both halves.
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t x) { return __byte_perm(x, 0u, 0x1010); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t x) { return __byte_perm(x, 0u, 0x3232); }
+
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ int4 ld_shared_v4(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ int4 ld_global_nc_v4(const void* p) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+}  // namespace vt

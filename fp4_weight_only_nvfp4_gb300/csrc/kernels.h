@@ -1,0 +1,66 @@
+// Host-side launchers implemented by the .cu files of libvtfp4 (internal header).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vt {
+
+cudaError_t launch_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
+                           int64_t split, float f0, float f1, int fmt, int64_t N, int64_t K,
+                           int64_t RT, int64_t KT, void* dst, cudaStream_t s);
+cudaError_t launch_unpack(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
+                          int64_t KT, int64_t split, uint8_t* codes, uint8_t* scales,
+                          cudaStream_t s);
+cudaError_t launch_dequant(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
+                           int64_t KT, int64_t split, float* out, cudaStream_t s);
+
+// Decode GEMM (M <= 16).
+struct DecodeLaunch {
+  const void* packed;     // header + tiles
+  int fmt;
+  int64_t N, K, RT, KT;
+  int64_t seg_split;
+  const void* A;          // bf16 [M][lda]
+  int64_t lda;
+  int M;
+  void* C;                // bf16 [M][ldc]
+  int64_t ldc;
+  // workspace pieces
+  int* status;
+  int* counters;          // [RT]
+  float* rowscale;        // [16]
+  void* Ap;               // f16 [KT][MT][64]
+  float* partials;        // [grid*2][MT][128]
+  // launch shape
+  int grid, warps, stages;
+};
+int decode_mt(int M);  // 8 or 16
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
+size_t decode_smem_bytes(int fmt, int mt, int warps, int stages);
+
+// Prefill tile GEMM (tensor cores), any M.
+struct PrefillLaunch {
+  const void* packed;
+  int fmt;
+  int64_t N, K, RT, KT;
+  int64_t seg_split;
+  const void* A;
+  int64_t lda;
+  int64_t M;
+  void* C;
+  int64_t ldc;
+  int* status;
+  float* rowscale;        // [Mp]
+  void* Ap;               // f16 [Mp][Kp]
+  int grid;
+};
+cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches, int* grid_out,
+                           int64_t* tiles_out);
+
+// Quantiser.
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, int fmt, uint8_t* codes,
+                            uint8_t* scales, float* global_out, void* scratch, cudaStream_t s);
+
+constexpr int kMaxDecodeGrid = 512;
+
+}  // namespace vt

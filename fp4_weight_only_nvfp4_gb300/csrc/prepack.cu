@@ -1,0 +1,314 @@
+// Prepack (source layout -> tile layout), its inverse, and the dequantisation used by the
+// bit-exact tests.  Source for the packed-resident design: "keep the ModelOpt NVFP4
+// lm_head packed" (vllm.cpp PR #263), "Why this row matters" -- the weight is kept packed
+// and its kernel-ready form is built once at load.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace vt {
+
+// Source description of one or two stacked weights (fused gate_up uses two).
+struct SrcPair {
+  const uint8_t* codes[2];
+  const uint8_t* scales[2];
+  int64_t split;  // rows [0, split) come from source 0, the rest from source 1
+};
+
+__device__ __forceinline__ void src_row(const SrcPair& s, int64_t row, int& which,
+                                        int64_t& r) {
+  which = row < s.split ? 0 : 1;
+  r = which ? row - s.split : row;
+}
+
+__global__ void k_header(PackedHeader* h, int fmt, int64_t N, int64_t K, int64_t split,
+                         float f0, float f1) {
+  if (threadIdx.x == 0) {
+    h->magic = kMagic;
+    h->fmt = static_cast<uint32_t>(fmt);
+    h->N = N;
+    h->K = K;
+    h->seg_split = split;
+    h->factor[0] = f0;
+    h->factor[1] = f1;
+    h->emax[0] = -1;
+    h->emax[1] = -1;
+  }
+}
+
+// MXFP4: largest finite E8M0 byte of each segment.
+__global__ void k_mx_emax(SrcPair s, int64_t N, int64_t K, PackedHeader* h) {
+  const int64_t gpr = K / 32;
+  const int64_t total = N * gpr;
+  int local[2] = {-1, -1};
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t row = i / gpr, grp = i % gpr;
+    int which;
+    int64_t r;
+    src_row(s, row, which, r);
+    int e = s.scales[which][r * gpr + grp];
+    if (e != 0xFF) local[which] = max(local[which], e);
+  }
+  for (int w = 0; w < 2; ++w) {
+    int v = local[w];
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0 && v >= 0) atomicMax(&h->emax[w], v);
+  }
+}
+
+// MXFP4: fix the per-segment epilogue factor 2^(emax - 140) once emax is known.
+__global__ void k_mx_factor(PackedHeader* h) {
+  if (threadIdx.x < 2) {
+    int e = h->emax[threadIdx.x];
+    if (e < 0) e = 127;  // no finite scale: any offset works
+    h->emax[threadIdx.x] = e;
+    h->factor[threadIdx.x] = ldexpf(1.0f, e - 140);
+  }
+}
+
+// E8M0 byte -> high byte of the f16 2^x, x = e - emax + 13, so that the largest scale of
+// the segment maps to 2^13 (codes up to 6 stay below the f16 limit) and scales down to
+// 2^-16 stay exact; smaller ones flush to 0; 0xFF (NaN) maps to an f16 NaN.
+__device__ __forceinline__ uint8_t mx_encode(int e, int emax) {
+  if (e == 0xFF) return 0x7E;
+  int x = e - emax + 13;
+  if (x >= -14) return static_cast<uint8_t>((x + 15) << 2);
+  if (x == -15) return 0x02;
+  if (x == -16) return 0x01;
+  return 0;
+}
+
+// One block per tile; 256 threads.  Thread i < 256 writes the 16 code bytes of
+// (row block j = i/32, lane = i%32); the first 32 (NVFP4) / 16 (MXFP4) threads also
+// write the scale bytes.
+__global__ void __launch_bounds__(256) k_pack(SrcPair s, int fmt, int64_t N, int64_t K,
+                                              int64_t KT, uint8_t* tiles,
+                                              const PackedHeader* h) {
+  const int64_t tile = blockIdx.x;
+  const int64_t rt = tile / KT, kt = tile % KT;
+  const int tb = tile_bytes(fmt);
+  uint8_t* out = tiles + tile * tb;
+  const int i = threadIdx.x;
+  const int j = i >> 5, lane = i & 31, g = lane >> 2, t = lane & 3;
+  const int64_t kb = K / 2;  // code bytes per row
+  uint32_t words[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      int64_t row = rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0);
+      int64_t col = kt * 32 + 8 * t + 2 * q + (b >> 1);
+      uint32_t v = 0;
+      if (row < N && col < kb) {
+        int which;
+        int64_t r;
+        src_row(s, row, which, r);
+        v = s.codes[which][r * kb + col];
+      }
+      w |= v << (8 * b);
+    }
+    words[q] = w;
+  }
+  *reinterpret_cast<uint4*>(out + j * 512 + lane * 16) =
+      make_uint4(words[0], words[1], words[2], words[3]);
+
+  if (fmt == FMT_NV) {
+    if (i < 32) {
+      const int64_t gpr = K / 16;
+      const int64_t grp = kt * 4 + t;
+      uint32_t w4[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          int64_t row = rt * kTileRows + jj * 16 + g + half * 8;
+          uint32_t v = 0;
+          if (row < N && grp < gpr) {
+            int which;
+            int64_t r;
+            src_row(s, row, which, r);
+            v = s.scales[which][r * gpr + grp];
+          }
+          int byte = jj * 2 + half;
+          w4[byte >> 2] |= v << (8 * (byte & 3));
+        }
+      }
+      *reinterpret_cast<uint4*>(out + kCodeBytes + lane * 16) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+  } else {
+    if (i < 16) {
+      const int gg = i >> 1, hh = i & 1;
+      const int64_t gpr = K / 32;
+      const int64_t grp = kt * 2 + hh;
+      uint32_t w4[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          int64_t row = rt * kTileRows + jj * 16 + gg + half * 8;
+          uint32_t v = 0;
+          if (row < N && grp < gpr) {
+            int which;
+            int64_t r;
+            src_row(s, row, which, r);
+            v = mx_encode(s.scales[which][r * gpr + grp], h->emax[which]);
+          }
+          int byte = jj * 2 + half;
+          w4[byte >> 2] |= v << (8 * (byte & 3));
+        }
+      }
+      *reinterpret_cast<uint4*>(out + kCodeBytes + (gg * 2 + hh) * 16) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+  }
+}
+
+// Inverse of k_pack for the codes and (NVFP4) scale bytes.  MXFP4 scale bytes are
+// recovered from the re-encoding and the segment's emax.
+__device__ __forceinline__ int mx_decode(uint8_t enc, int emax) {
+  if (enc == 0x7E) return 0xFF;
+  int x;
+  if (enc >= 0x04) x = (enc >> 2) - 15;
+  else if (enc == 0x02) x = -15;
+  else if (enc == 0x01) x = -16;
+  else return -1;  // flushed: not recoverable
+  return x + emax - 13;
+}
+
+__global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, int64_t N,
+                                                int64_t K, int64_t KT, int64_t split,
+                                                const PackedHeader* h, uint8_t* codes,
+                                                uint8_t* scales) {
+  const int64_t tile = blockIdx.x;
+  const int64_t rt = tile / KT, kt = tile % KT;
+  const uint8_t* in = tiles + tile * tile_bytes(fmt);
+  const int i = threadIdx.x;
+  const int j = i >> 5, lane = i & 31, g = lane >> 2, t = lane & 3;
+  const int64_t kb = K / 2;
+  uint4 v = *reinterpret_cast<const uint4*>(in + j * 512 + lane * 16);
+  uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      int64_t row = rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0);
+      int64_t col = kt * 32 + 8 * t + 2 * q + (b >> 1);
+      if (row < N && col < kb) codes[row * kb + col] = (words[q] >> (8 * b)) & 0xFF;
+    }
+  if (fmt == FMT_NV) {
+    if (i < 32) {
+      const int64_t gpr = K / 16, grp = kt * 4 + t;
+      uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + lane * 16);
+      uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
+      for (int jj = 0; jj < 8; ++jj)
+        for (int half = 0; half < 2; ++half) {
+          int64_t row = rt * kTileRows + jj * 16 + g + half * 8;
+          int byte = jj * 2 + half;
+          if (row < N && grp < gpr) scales[row * gpr + grp] = (w4[byte >> 2] >> (8 * (byte & 3))) & 0xFF;
+        }
+    }
+  } else {
+    if (i < 16) {
+      const int gg = i >> 1, hh = i & 1;
+      const int64_t gpr = K / 32, grp = kt * 2 + hh;
+      uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + (gg * 2 + hh) * 16);
+      uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
+      for (int jj = 0; jj < 8; ++jj)
+        for (int half = 0; half < 2; ++half) {
+          int64_t row = rt * kTileRows + jj * 16 + gg + half * 8;
+          int byte = jj * 2 + half;
+          if (row < N && grp < gpr) {
+            uint8_t enc = (w4[byte >> 2] >> (8 * (byte & 3))) & 0xFF;
+            int e = mx_decode(enc, h->emax[row < split ? 0 : 1]);
+            scales[row * gpr + grp] = static_cast<uint8_t>(e < 0 ? 0 : e);
+          }
+        }
+    }
+  }
+}
+
+// Dequantise through the same conversions the GEMM uses: E2M1 pair -> f16x2, scale ->
+// f16x2, one f16 multiply (exact), then fp32 multiply by the segment factor.
+__global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, int64_t N,
+                                                 int64_t K, int64_t KT, int64_t split,
+                                                 const PackedHeader* h, float* out) {
+  const int64_t tile = blockIdx.x;
+  const int64_t rt = tile / KT, kt = tile % KT;
+  const uint8_t* in = tiles + tile * tile_bytes(fmt);
+  const int i = threadIdx.x;
+  const int j = i >> 5, lane = i & 31, g = lane >> 2, t = lane & 3;
+  uint4 v = *reinterpret_cast<const uint4*>(in + j * 512 + lane * 16);
+  uint32_t words[4] = {v.x, v.y, v.z, v.w};
+  uint32_t sc2;
+  if (fmt == FMT_NV) {
+    uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + lane * 16);
+    uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
+    uint32_t two = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
+    sc2 = e4m3x2_to_f16x2(two);
+  } else {
+    uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + (g * 2 + (t >> 1)) * 16);
+    uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
+    uint32_t two = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
+    sc2 = mxenc2_to_f16x2(two);
+  }
+  const uint32_t s_g = bcast_lo(sc2), s_g8 = bcast_hi(sc2);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t r[4];
+    e2m1x8_to_f16x8(words[q], r[0], r[1], r[2], r[3]);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t p = hmul2_u32(r[b], (b & 1) ? s_g8 : s_g);
+      __half2 hp = *reinterpret_cast<__half2*>(&p);
+      int64_t row = rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0);
+      int64_t k0 = kt * kTileK + 16 * t + 4 * q + ((b >> 1) ? 2 : 0);
+      if (row < N && k0 < K) {
+        float f = h->factor[row < split ? 0 : 1];
+        out[row * K + k0] = __low2float(hp) * f;
+        out[row * K + k0 + 1] = __high2float(hp) * f;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host launchers
+cudaError_t launch_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
+                           int64_t split, float f0, float f1, int fmt, int64_t N, int64_t K,
+                           int64_t RT, int64_t KT, void* dst, cudaStream_t s) {
+  PackedHeader* h = reinterpret_cast<PackedHeader*>(dst);
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(dst) + kHeaderBytes;
+  SrcPair sp{{codes[0], codes[1]}, {scales[0], scales[1]}, split};
+  k_header<<<1, 32, 0, s>>>(h, fmt, N, K, split, f0, f1);
+  if (fmt == FMT_MX) {
+    int64_t total = N * (K / 32);
+    int64_t nb = (total + 255) / 256;
+    int blocks = static_cast<int>(nb < 4096 ? nb : 4096);
+    k_mx_emax<<<blocks, 256, 0, s>>>(sp, N, K, h);
+    k_mx_factor<<<1, 32, 0, s>>>(h);
+  }
+  k_pack<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(sp, fmt, N, K, KT, tiles, h);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
+                          int64_t KT, int64_t split, uint8_t* codes, uint8_t* scales,
+                          cudaStream_t s) {
+  const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
+  const uint8_t* tiles = reinterpret_cast<const uint8_t*>(packed) + kHeaderBytes;
+  k_unpack<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(tiles, fmt, N, K, KT, split, h,
+                                                          codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
+                           int64_t KT, int64_t split, float* out, cudaStream_t s) {
+  const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
+  const uint8_t* tiles = reinterpret_cast<const uint8_t*>(packed) + kHeaderBytes;
+  k_dequant<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(tiles, fmt, N, K, KT, split, h,
+                                                           out);
+  return cudaGetLastError();
+}
+
+}  // namespace vt

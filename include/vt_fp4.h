@@ -1,0 +1,180 @@
+/*
+ * vt_fp4.h -- C ABI of libvtfp4: FP4 weight-only (W4A16) linear layers on GB300 (sm_103a).
+ *
+ * The layer:  C[m][n] = bf16( sum_k A[m][k] * w[n][k] ),  A bf16 [M][K], w dequantised
+ * from FP4:
+ *   NVFP4  w = e2m1(code) * e4m3(scale[n][k/16]) * global      (global: fp32 multiplier)
+ *   MXFP4  w = e2m1(code) * 2^(e8m0(scale[n][k/32]) - 127)     (no global)
+ * Sources (vllm.cpp pull-request pages):
+ *   "keep the ModelOpt NVFP4 lm_head packed" (PR #263), "Why this row matters": the
+ *     packed NVFP4 head is U8 codes (two per byte) + FP8 scales + FP32 second scale, and
+ *     it runs as a W4A16 GEMM instead of being expanded to bf16;
+ *   "re-verify 27B NVFP4 on the nvidia ModelOpt checkpoint" (PR #178), "Layer 3": the
+ *     ModelOpt weight_scale_2 is a direct multiplier; "W4A16 is the default": activation
+ *     scales (input_scale) are not consumed;
+ *   "native MXFP4 keep-quant + Qwen e2e" (PR #38), commit "W2": MXFP4 is E2M1 with one
+ *     E8M0 scale per 32 weights, U8 [N, K/32], and no global scale;
+ *   "MXFP4 decode-graph + gate_up FUSION default-ON" (PR #54), "Step 2": gate and up are
+ *     merged into one GEMM of N = 2*I.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are CUDA device pointers owned by the caller; (host) are
+ *     host pointers.  The library never allocates device memory and keeps no global
+ *     cache keyed by address: all state of a prepacked weight lives in its handle and in
+ *     the caller's packed buffer.
+ *   - Work is enqueued on the caller's stream `s` and is asynchronous; no entry point
+ *     synchronises the device except vt_fp4_workspace_status.
+ *   - Every entry returns a vt_status and never aborts.  On failure nothing is enqueued
+ *     and vt_fp4_last_error() returns a message for the calling thread.
+ *   - Built for sm_103a only; on another device the launches fail with VT_ERR_CUDA.
+ */
+#ifndef VT_FP4_H
+#define VT_FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vt_stream_t; /* same object as cudaStream_t; NULL = default */
+
+typedef enum { VT_FP4_NVFP4 = 0, VT_FP4_MXFP4 = 1 } vt_fp4_format;
+
+typedef enum {
+  VT_OK = 0,
+  VT_ERR_INVALID_ARG = 1, /* bad size, null pointer, bad scale, format mismatch */
+  VT_ERR_UNSUPPORTED = 2, /* a shape or option this build does not implement */
+  VT_ERR_MISALIGNED = 3,  /* a pointer or leading dimension breaks the alignment rule */
+  VT_ERR_CUDA = 4,        /* a CUDA runtime call failed (message has the CUDA error) */
+  VT_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see workspace status) */
+} vt_status;
+
+typedef struct vt_fp4_weight_s* vt_fp4_handle;
+
+/* What the last vt_fp4_w4a16_gemm on a handle launched (host-side record). */
+typedef struct {
+  int path;           /* 0 none yet, 1 decode (M <= 16), 2 prefill tile path */
+  int grid;           /* CTAs of the main kernel */
+  int warps_per_cta;  /* warps per CTA of the main kernel */
+  int m_tile;         /* decode: tokens per MMA column block (8 or 16); prefill: 128 */
+  int64_t items;      /* decode: (row tile, k tile) work items; prefill: output tiles */
+  int64_t launches;   /* kernels enqueued by that call */
+  int64_t calls;      /* GEMM calls made on this handle so far */
+} vt_fp4_launch_info;
+
+/* Optional tuning overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
+typedef struct {
+  int grid;      /* decode: number of CTAs (clamped to [1, 1024]) */
+  int warps;     /* decode: warps per CTA, one of 4, 8, 12, 16 */
+  int stages;    /* decode: TMA ring depth per warp, 2..6 */
+  int force_path;/* 1 decode (requires M <= 16), 2 prefill */
+} vt_fp4_gemm_opts;
+
+/* ---------------------------------------------------------------------- sizes */
+
+/* Exact size in bytes of the prepacked buffer for an N x K weight of format `fmt`:
+ * a 256-byte header plus ceil(N/128)*ceil(K/64) tiles of 4608 (NVFP4) or 4352 (MXFP4)
+ * bytes.  Requires N > 0, K > 0, K % 16 == 0 (NVFP4) or K % 32 == 0 (MXFP4). */
+vt_status vt_fp4_prepack_bytes(vt_fp4_format fmt, int64_t N, int64_t K, size_t* packed_bytes);
+
+/* ------------------------------------------------------------------- prepack */
+
+/* Reorders one weight into the kernels' tile layout (a bijection of the code and scale
+ * bytes plus zero padding) and returns a handle.  Source: "keep the ModelOpt NVFP4
+ * lm_head packed" (PR #263): the weight stays packed and its resident form is built once
+ * at load, "paid once, instead of rebuilding ... every decode step".
+ *   codes        (device) u8 [N][K/2], row-major; the low nibble holds the even k.
+ *   scales       (device) u8 [N][K/g], row-major; g = 16 (E4M3) or 32 (E8M0).
+ *   global_scale NVFP4: the fp32 multiplier (ModelOpt weight_scale_2), finite and > 0;
+ *                MXFP4: must be 1.0f (the format has no global scale).
+ *   packed_dst   (device) caller-owned, 16-byte aligned, >= vt_fp4_prepack_bytes bytes;
+ *                it must outlive the handle and must not be written by the caller.
+ * codes/scales are read by kernels enqueued on `s`; they may be freed once those have
+ * run.  *out receives a new handle (free it with vt_fp4_destroy). */
+vt_status vt_fp4_prepack(const uint8_t* codes, const uint8_t* scales, float global_scale,
+                         vt_fp4_format fmt, int64_t N, int64_t K, void* packed_dst,
+                         size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out);
+
+/* Fused gate_up: one handle holding gate (rows [0, I)) and up (rows [I, 2I)), each with
+ * its own codes, scales and global, so that one GEMM call writes C[M][2I] with gate in
+ * columns [0, I) and up in [I, 2I).  Source: "MXFP4 decode-graph + gate_up FUSION
+ * default-ON" (PR #54), "Step 2".  Sizes as vt_fp4_prepack with N = 2*I. */
+vt_status vt_fp4_prepack_gate_up(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                 float gate_global, const uint8_t* up_codes,
+                                 const uint8_t* up_scales, float up_global, vt_fp4_format fmt,
+                                 int64_t I, int64_t K, void* packed_dst, size_t dst_bytes,
+                                 vt_stream_t s, vt_fp4_handle* out);
+
+/* Frees the host-side handle (never device memory). NULL is a no-op. */
+vt_status vt_fp4_destroy(vt_fp4_handle W);
+
+/* Shape and format of a handle. */
+vt_status vt_fp4_shape(vt_fp4_handle W, vt_fp4_format* fmt, int64_t* N, int64_t* K);
+
+/* ----------------------------------------------------------------- the GEMM */
+
+/* Bytes of workspace a GEMM on W with M <= M_max needs.  The workspace holds the
+ * activations converted for the tensor cores, split-K partial sums, per-tile arrival
+ * counters and a status word.  The caller zeroes it ONCE after allocation; the library
+ * leaves the counters at zero after every call (self-resetting), so it can be reused by
+ * later calls in stream order.  A workspace must not be used by two calls that may run
+ * at the same time. */
+vt_status vt_fp4_workspace_bytes(vt_fp4_handle W, int64_t M_max, size_t* bytes);
+
+/* C = A . W^T in bf16 with fp32 accumulation.
+ *   A  (device) bf16 [M][lda], 16-byte aligned, lda >= K, lda % 8 == 0.
+ *   C  (device) bf16 [M][ldc], 4-byte aligned, ldc >= N, ldc % 2 == 0.
+ *   M  tokens; M == 0 is a no-op.  M <= 16 runs the decode kernel, larger M the
+ *      tensor-core tile kernel.
+ *   workspace (device) >= vt_fp4_workspace_bytes(W, M), 256-byte aligned, zeroed once.
+ * Deterministic: the same inputs and launch configuration give the same bits.
+ * Asynchronous on `s`, no host synchronisation, capturable in a CUDA graph.
+ * Source: "keep the ModelOpt NVFP4 lm_head packed" (PR #263), "Why this row matters":
+ * the logits GEMM runs on the packed weight (W4A16), never on a bf16 expansion. */
+vt_status vt_fp4_w4a16_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
+                            int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s);
+
+/* As vt_fp4_w4a16_gemm with tuning overrides (NULL opts = defaults). */
+vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                               void* C, int64_t ldc, void* workspace, size_t ws_bytes,
+                               vt_stream_t s, const vt_fp4_gemm_opts* opts);
+
+/* Reads the workspace status word (synchronises `s`): *status = VT_OK, or VT_ERR_TIMEOUT
+ * if a bounded device-side wait gave up during an earlier call; the word is then cleared. */
+vt_status vt_fp4_workspace_status(void* workspace, vt_stream_t s, int* status);
+
+/* Host-side record of the last GEMM launched on W. */
+vt_status vt_fp4_stats(vt_fp4_handle W, vt_fp4_launch_info* info);
+
+/* ------------------------------------------------------------ debug / tests */
+
+/* out (device) fp32 [N][K]: the dequantised weight as the kernels see it,
+ * NVFP4 fl32(e2m1*e4m3*global) (e2m1*e4m3 is exact), MXFP4 e2m1*2^(e-127) (exact). */
+vt_status vt_fp4_dequant(vt_fp4_handle W, float* out, vt_stream_t s);
+
+/* Inverse of the prepack: codes (device) u8 [N][K/2] and scales (device) u8 [N][K/g] in
+ * the input layout, recovered from the packed buffer. */
+vt_status vt_fp4_unpack(vt_fp4_handle W, uint8_t* codes, uint8_t* scales, vt_stream_t s);
+
+/* ------------------------------------------------------------- quantiser */
+
+/* Quantises a bf16 weight [N][K] (device, row-major, 16-byte aligned, K % g == 0) into
+ * codes [N][K/2] and scales [N][K/g] (device) with the synthetic-weight recipe:
+ *   NVFP4: G = fl32(amax/(6*448)); s = E4M3_RNE_sat(amax_g/(6G)); code = E2M1_RNE(w/(s G))
+ *   MXFP4: e = min{e : 2^e >= amax_g/6}; code = E2M1_RNE(w / 2^e)
+ * (quotients in fp64, ties to even, saturating).  NVFP4 writes G to *global_out
+ * (device, 4 bytes; MXFP4 ignores it).  `scratch` (device, >= 16 bytes, 16-aligned) is
+ * overwritten. */
+vt_status vt_fp4_quantize(const void* W, int64_t N, int64_t K, vt_fp4_format fmt,
+                          uint8_t* codes, uint8_t* scales, float* global_out, void* scratch,
+                          vt_stream_t s);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* vt_fp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VT_FP4_H */
