@@ -274,26 +274,14 @@ def run_gpu(args, rank: int, world: int):
     stream.synchronize()
     launches_per_call = sets[0][0][0].stats()["launches"]
 
-    # capture the step, with per-call event records (external event nodes) when available
-    try:
-        ev = [(torch.cuda.Event(enable_timing=True, external=True),
-               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_calls)]
-    except TypeError:
-        ev = None
+    # the timed step: one CUDA graph of all the step's calls, back to back (consecutive
+    # calls overlap through programmatic dependent launch)
     graph = torch.cuda.CUDAGraph()
-    try:
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream):
-                issue(ev)
-    except Exception:  # event record nodes not supported here: time calls outside the graph
-        ev = None
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream):
-                issue(None)
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            issue(None)
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
     stream.synchronize()
 
     dist = None
@@ -302,16 +290,16 @@ def run_gpu(args, rank: int, world: int):
         dist.barrier()
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    t0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    t1.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     if dist:
@@ -325,21 +313,34 @@ def run_gpu(args, rank: int, world: int):
     ms_step = ms_total / args.steps
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
 
-    # per-call durations from the event nodes of the last replay
-    per_call = []
-    if ev is not None:
+    # per-call durations: a second graph with an event record node around every call (the
+    # event nodes break the overlap between calls, so these durations are slightly larger
+    # than the calls' share of the timed step)
+    try:
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_calls)]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g2, stream=stream):
+                issue(ev)
+            for _ in range(3):
+                g2.replay()
+        stream.synchronize()
         durs = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n_calls)]
-    else:
+    except (TypeError, RuntimeError):
+        torch.cuda.synchronize()
         durs = []
         for i in range(n_calls):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             c, layer, pi, M = calls[i]
             p = w.projs[pi]
             e0.record(stream)
-            vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws, stream=stream)
+            vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
+                          stream=stream)
             e1.record(stream)
             stream.synchronize()
             durs.append(e0.elapsed_time(e1))
+    per_call = []
     agg = {}
     for i, (c, layer, pi, M) in enumerate(calls):
         p = w.projs[pi]
@@ -354,7 +355,8 @@ def run_gpu(args, rank: int, world: int):
         per_call.append({"proj": name, "M": M, "us_per_call": round(us, 3),
                          "GBps": round(b / n / (us * 1e-6) / 1e9, 1)})
     kernel_ms = sum(durs)
-    achieved = step_bytes / (kernel_ms * 1e-3) / 1e9
+    # the step runs nothing but GEMM calls: their average throughput over the timed region
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9
 
     # end to end: pinned host activations in, host logits out, every call
     e2e = run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist)
@@ -396,17 +398,19 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
             issue()
-    for _ in range(3):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
     stream.synchronize()
     if dist:
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    t1.record(stream)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
     stream.synchronize()
     ms = t0.elapsed_time(t1)
     if dist:

@@ -9,7 +9,7 @@
 #include <mutex>
 #include <new>
 
-#include "../../include/vt_fp4.h"
+#include "vt_fp4.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -75,8 +75,10 @@ WsLayout ws_layout(const vt_fp4_weight_s* W, int64_t M) {
   const int64_t mrows = M <= 16 ? 16 : cdiv(M, 128) * 128;
   L.status = 0;
   L.counters = 256;
+  // activation scales: decode [KT][16] floats; prefill one per token row
   L.rowscale = up256(L.counters + (size_t)W->RT * 4);
-  L.ap = up256(L.rowscale + (size_t)mrows * 4);
+  const size_t nscale = M <= 16 ? (size_t)W->KT * 16 : (size_t)mrows;
+  L.ap = up256(L.rowscale + nscale * 4);
   L.partials = up256(L.ap + (size_t)mrows * Kp * 2);
   const size_t part = M <= 16 ? (size_t)kMaxDecodeGrid * 2 * 16 * 128 * 4 : 0;
   L.total = up256(L.partials + part);
@@ -250,31 +252,39 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
     D.ldc = ldc;
     D.status = reinterpret_cast<int*>(ws + L.status);
     D.counters = reinterpret_cast<int*>(ws + L.counters);
-    D.rowscale = reinterpret_cast<float*>(ws + L.rowscale);
+    D.ascale = reinterpret_cast<float*>(ws + L.rowscale);
     D.Ap = ws + L.ap;
     D.partials = reinterpret_cast<float*>(ws + L.partials);
     const int64_t items = W->RT * W->KT;
-    int warps = (opts && opts->warps) ? opts->warps : 8;
-    if (warps != 4 && warps != 8) return fail(VT_ERR_INVALID_ARG, "warps must be 4 or 8");
+    // k tiles per pipeline stage (8: up to 37 KB of weights per TMA copy) and ring depth
+    int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
+    if (ks != 4 && ks != 8) return fail(VT_ERR_INVALID_ARG, "stage width must be 4 or 8 k tiles");
     const int mt = decode_mt((int)M);
-    int stages = (opts && opts->stages) ? opts->stages : (mt == 8 ? 4 : 3);
-    if (stages < 2 || stages > 6) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 6]");
-    if (decode_smem_bytes(W->fmt, mt, warps, stages) > 227 * 1024)
-      return fail(VT_ERR_INVALID_ARG, "warps x stages exceed shared memory");
+    int stages = (opts && opts->stages) ? opts->stages : 0;
+    if (!stages) {  // as deep as shared memory allows, at most 6
+      stages = 6;
+      while (stages > 2 && decode_smem_bytes(W->fmt, (int)M, ks, stages) > 226 * 1024) --stages;
+    }
+    if (stages < 2 || stages > 16) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 16]");
+    if (decode_smem_bytes(W->fmt, (int)M, ks, stages) > 226 * 1024)
+      return fail(VT_ERR_INVALID_ARG, "stage width x stages exceed shared memory");
     int64_t grid = (opts && opts->grid) ? opts->grid : sm_count();
-    if (!(opts && opts->grid)) grid = grid < cdiv(items, warps) ? grid : cdiv(items, warps);
+    if (!(opts && opts->grid)) {
+      const int64_t per_cta = 2 * ks;  // at least two stages of work per CTA
+      grid = grid < cdiv(items, per_cta) ? grid : cdiv(items, per_cta);
+    }
     if (grid > items) grid = items;
     if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
     if (grid < 1) grid = 1;
     D.grid = (int)grid;
-    D.warps = warps;
+    D.ks = ks;
     D.stages = stages;
     int launches = 0;
     cudaError_t e = launch_decode(D, (cudaStream_t)s, &launches);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     W->info.path = 1;
     W->info.grid = D.grid;
-    W->info.warps_per_cta = warps;
+    W->info.warps_per_cta = 17;  // 16 consumer warps + the TMA producer warp
     W->info.m_tile = mt;
     W->info.items = items;
     W->info.launches = launches;

@@ -20,10 +20,11 @@ namespace vt {
 //          step q, with the MMA's logical k columns {2t,2t+1,2t+8,2t+9} mapped onto the
 //          four consecutive physical k = 64kt+16t+4q+{0..3}.  Lane t therefore covers
 //          physical k in [16t, 16t+16) of the tile over the four steps.
-//   scales NVFP4 [32 lanes][8 j][2 B] (512 B): E4M3 bytes of rows 16j+g and 16j+g+8 for
-//          group 4kt+t (the 16 k lane t covers).
-//   scales MXFP4 [8 g][2 h][8 j][2 B] (256 B): rows 16j+g, 16j+g+8, group 2kt+h; the
-//          bytes are re-encoded as the high byte of an f16 power of two (see prepack).
+//   scales NVFP4 [4 row-block pairs jp][32 lanes][2 j][2 B] (512 B): E4M3 bytes of rows
+//          16j+g and 16j+g+8 (j = 2jp + j&1) for group 4kt+t (the 16 k lane t covers).
+//   scales MXFP4 [4 jp][8 g][2 h][2 j][2 B] (256 B): rows 16j+g, 16j+g+8, group 2kt+h;
+//          the bytes are re-encoded as the high byte of an f16 power of two (see prepack).
+//   so the four scale bytes lane (g, t) needs for a row-block pair form one 32-bit word.
 constexpr int kHeaderBytes = 256;
 constexpr int kTileRows = 128;
 constexpr int kTileK = 64;
@@ -37,6 +38,13 @@ enum { FMT_NV = 0, FMT_MX = 1 };
 
 __host__ __device__ constexpr int tile_bytes(int fmt) {
   return fmt == FMT_NV ? kTileBytesNV : kTileBytesMX;
+}
+
+// Byte offset, inside a tile, of the two scale bytes (rows g, g+8) lane (g, t) of row
+// block j needs.
+__host__ __device__ constexpr int scale_offset(int fmt, int j, int g, int t) {
+  return fmt == FMT_NV ? kCodeBytes + (j >> 1) * 128 + (4 * g + t) * 4 + (j & 1) * 2
+                       : kCodeBytes + (j >> 1) * 64 + (g * 2 + (t >> 1)) * 4 + (j & 1) * 2;
 }
 
 // Header written by the prepack kernels and read by the GEMM epilogue.
@@ -71,6 +79,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {

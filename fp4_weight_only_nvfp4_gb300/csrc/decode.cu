@@ -2,20 +2,20 @@
 // tile layout.  Sources: "keep the ModelOpt NVFP4 lm_head packed" (vllm.cpp PR #263),
 // "Why this row matters" (W4A16 decode is pure weight traffic); "re-verify 27B NVFP4"
 // (PR #178), "Attribution" (the FP4 MLP GEMM at ~68% of the bandwidth roof is the lever);
-// "MXFP4 decode-graph + gate_up FUSION" (PR #54), "Step 3" (CTA count per SM decides the
+// "MXFP4 decode-graph + gate_up FUSION" (PR #54), "Step 3" (the CTA count per SM decides the
 // residual; a regrouped fp32 reduce moves bf16 ULPs, so reductions here have a fixed
 // order); "re-verify 27B NVFP4" (PR #178): a split-K workspace whose spin-locks were not
 // zeroed hung the GPU, so this kernel has no spin-locks (the last CTA to arrive reduces).
 //
-// Design (GB300): one persistent CTA per SM, W warps.  Work items are (128-row tile,
-// 64-k tile) pairs in row-tile-major order; CTA c owns items [c*I/G, (c+1)*I/G).  Each
-// warp streams its items (every W-th item of the CTA's range) through its own ring of D
-// shared-memory stages filled by 1-D TMA bulk copies (weights + the matching slice of the
-// converted activations), dequantises in registers (E2M1 -> f16 by cvt, times the group
-// scale in f16, both exact) and accumulates with m16n8k16 MMAs in fp32.  At the end of
-// each row-tile segment the warps' partial sums are added in warp order through shared
-// memory; a row tile shared by several CTAs is finished by the last CTA to arrive, which
-// adds the CTAs' partials in CTA order.
+// Design (GB300): one persistent CTA per SM with 16 consumer warps and one producer warp.
+// Work items are (128-row tile, 64-k tile) pairs in row-tile-major order; CTA c owns items
+// [c*I/G, (c+1)*I/G).  The producer thread streams the CTA's items through a ring of
+// shared-memory stages with 1-D TMA bulk copies (up to KS consecutive k tiles of weights
+// per copy, plus the matching activation slices and scales).  Consumers dequantise in
+// registers (E2M1 -> f16 by cvt, times the group scale in f16, both exact) and accumulate
+// with m16n8k16 MMAs in fp32.  At the end of each row-tile segment the warps' partial sums
+// are added in a fixed order through shared memory; a row tile shared by several CTAs is
+// finished by the last CTA to arrive, which adds the CTAs' partials in CTA order.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -23,73 +23,75 @@
 
 namespace vt {
 
-constexpr int kSlotPad = 132;  // floats per token row of a warp's reduction slot
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+constexpr int kAScaleStride = 16;   // floats per k tile in the activation-scale array
+constexpr int kConsumerWarps = 16;
+constexpr int kSlotPad = 36;        // floats per token row of a warp's reduction slot
 
 int decode_mt(int M) { return M <= 8 ? 8 : 16; }
 
-size_t decode_smem_bytes(int fmt, int mt, int warps, int stages) {
-  size_t stage = tile_bytes(fmt) + (size_t)mt * 128;
-  return (size_t)warps * stages * stage + (size_t)warps * mt * kSlotPad * 4 +
-         (size_t)warps * stages * 8 + 64;
+// Dynamic shared memory of the decode kernel: `stages` stages of `ks` k tiles (weights, M
+// activation rows and the activation scales each), the consumer warps' reduction slots and
+// the barriers.
+size_t decode_smem_bytes(int fmt, int M, int ks, int stages) {
+  const size_t mt = (size_t)decode_mt(M);
+  const size_t stage = (size_t)ks * (tile_bytes(fmt) + (size_t)M * 128 + kAScaleStride * 4);
+  return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 + (size_t)stages * 16 + 64;
 }
 
 // ------------------------------------------------------------- activation pre-pass
-// One block per token row m: A'[kt][m][64] (f16) = A[m][k] * 2^-p[m], rowscale[m] = 2^p[m],
-// with p chosen from the row's largest magnitude so that every value lands below 2^15
-// (no f16 overflow) and values down to 2^-31 of the maximum stay exact.  The 16-byte
-// granules of each 128-byte row are stored XOR-swizzled by (m & 7) so that the MMA
-// fragment reads from shared memory are free of bank conflicts.
-__global__ void __launch_bounds__(256) k_prep_a(const __nv_bfloat16* __restrict__ A,
-                                                int64_t lda, int64_t K, int64_t KT, int mt,
-                                                __half* __restrict__ Ap,
-                                                float* __restrict__ rowscale) {
+// A[m][k] (bf16) -> A'[kt][m][64] (f16) with one power-of-two scale per (token m, 64-wide
+// k tile kt): A' = A * 2^-p, ascale[kt][m] = 2^p, p chosen from the tile's largest
+// magnitude so that every value lands below 2^15 (no f16 overflow) and values down to
+// 2^-31 of that maximum stay exact.  The GEMM multiplies each k tile's partial sums by
+// its ascale.  The 16-byte granules of each 128-byte row are stored XOR-swizzled by
+// (m & 7) so that the MMA fragment reads from shared memory are free of bank conflicts.
+// Grid (M, ceil(KT / 8)); 64 threads = 8 k tiles x 8 granules, one granule each.
+constexpr int kPrepThreads = 64;
+constexpr int kPrepTiles = 8;
+
+__global__ void __launch_bounds__(kPrepThreads) k_prep_a(const __nv_bfloat16* __restrict__ A,
+                                                         int64_t lda, int64_t K, int64_t KT,
+                                                         int rows, __half* __restrict__ Ap,
+                                                         float* __restrict__ ascale) {
+  // Let the GEMM kernel launch (it starts streaming weights), then wait for whatever
+  // produced A (and for the previous GEMM, which may still read the workspace).
   pdl_launch_dependents();
-  extern __shared__ __align__(16) uint8_t sm_row[];
-  __shared__ int red[8];
+  pdl_wait();
   const int m = blockIdx.x;
-  const uint4* src = reinterpret_cast<const uint4*>(A + m * lda);
-  uint4* row = reinterpret_cast<uint4*>(sm_row);
+  const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + (threadIdx.x >> 3);
+  const int gi = threadIdx.x & 7;
+  const int64_t k0 = kt * 64 + gi * 8;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   int mx = 0;
-  for (int64_t v = threadIdx.x; v < K / 8; v += blockDim.x) {
-    uint4 x = src[v];
-    row[v] = x;
-    uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      mx = max(mx, (int)(w[i] & 0x7FFFu));
-      mx = max(mx, (int)((w[i] >> 16) & 0x7FFFu));
-    }
+  for (int q = 0; q < 4; ++q) {
+    mx = max(mx, (int)(w[q] & 0x7FFFu));
+    mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
   }
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  mx = 0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mx = max(mx, red[i]);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (kt >= KT) return;
   int p = 0;
   if (mx > 0 && mx <= 0x7F80) {
-    int e = (mx >> 7) - 127;  // exponent of the largest magnitude (subnormals: -127)
+    const int e = (mx >> 7) - 127;  // exponent of the largest magnitude (subnormals: -127)
     p = e - 14;
     p = p < -120 ? -120 : (p > 113 ? 113 : p);
   }
   const float down = ldexpf(1.0f, -p);
-  const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(sm_row);
-  for (int64_t c = threadIdx.x; c < KT * 8; c += blockDim.x) {
-    const int64_t kt = c >> 3;
-    const int gi = (int)(c & 7);
-    const int64_t k0 = kt * 64 + gi * 8;
-    uint32_t o[4];
+  uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float lo = (k0 + 2 * i < K) ? __bfloat162float(rb[k0 + 2 * i]) * down : 0.0f;
-      float hi = (k0 + 2 * i + 1 < K) ? __bfloat162float(rb[k0 + 2 * i + 1]) * down : 0.0f;
-      __half2 h = __floats2half2_rn(lo, hi);
-      o[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(Ap + ((kt * mt + m) * 64 + ((gi ^ (m & 7)) * 8)));
-    *dst = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int q = 0; q < 4; ++q) {
+    const float lo = __uint_as_float(w[q] << 16) * down;
+    const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
+    __half2 h = __floats2half2_rn(lo, hi);
+    o[q] = *reinterpret_cast<uint32_t*>(&h);
   }
-  if (threadIdx.x == 0) rowscale[m] = ldexpf(1.0f, p);
+  uint4* dst = reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8)));
+  *dst = make_uint4(o[0], o[1], o[2], o[3]);
+  if (gi == 0) ascale[kt * kAScaleStride + m] = ldexpf(1.0f, p);
 }
 
 // ------------------------------------------------------------------- main kernel
@@ -99,7 +101,7 @@ struct DecodeParams {
   int64_t N, KT, items, seg_split, ldc;
   int M, stages;
   const __half* Ap;
-  const float* rowscale;
+  const float* ascale;  // [KT][16]
   __nv_bfloat16* C;
   float* partials;
   int* counters;
@@ -110,187 +112,270 @@ __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t I, int64_t G) {
   return ((i + 1) * G - 1) / I;  // the CTA c with c*I/G <= i < (c+1)*I/G
 }
 
-template <int FMT, int MT>
-__global__ void __launch_bounds__(256, 1) k_decode(const DecodeParams p) {
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// CTA layout: 16 consumer warps and one producer warp.  A stage holds up to KS consecutive
+// k tiles of one 128-row tile (one TMA bulk copy of the weights, one of the matching
+// activation slices, one of their scales); consumer warp w owns the row-block pair w % 4
+// (32 rows) and the stage's k tiles w / 4, w / 4 + 4, ... .  The producer is one thread.
+template <int FMT, int MT, int KS>
+__global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const DecodeParams p) {
   constexpr int TB = tile_bytes(FMT);
-  constexpr int AB = MT * 128;  // activation bytes of one k tile (all MT rows)
-  constexpr int NJ = MT / 8;    // n8 MMA column blocks
+  constexpr int NJ = MT / 8;           // n8 MMA column blocks
+  constexpr int CW = kConsumerWarps;
+  constexpr int CT = CW * 32;          // consumer threads
+  constexpr int SLOT = MT * kSlotPad;  // floats per warp reduction slot (32 rows + pad)
+  constexpr int WBYTES = KS * TB;      // weight bytes of a full stage
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_flag;
+  // The next kernel in the stream may launch now: it only waits (griddepcontrol.wait)
+  // for this grid to finish before it touches anything this grid reads or writes.
+  pdl_launch_dependents();
 
-  const int W = blockDim.x >> 5;
-  const int D = p.stages;
+  const int S = p.stages;
+  const int M = p.M;
+  // stage: weights | activation slices (M rows of 128 B per k tile) | activation scales
+  const int SCALES_OFF = WBYTES + KS * M * 128;
+  const int STAGE = SCALES_OFF + KS * kAScaleStride * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t G = gridDim.x, c = blockIdx.x, I = p.items, KT = p.KT;
   const int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
-  const int STAGE = TB + AB;
 
-  uint8_t* ring = smem + (size_t)warp * D * STAGE;
-  float* slots = reinterpret_cast<float*>(smem + (size_t)W * D * STAGE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)W * D * STAGE +
-                                               (size_t)W * MT * kSlotPad * 4) +
-                   warp * D;
-  const uint32_t ring_u = smem_u32(ring);
-  const uint32_t bar_u = smem_u32(bars);
-  const int abytes = p.M * 128;  // only the valid token rows are copied
-  const uint32_t tx = TB + abytes;
+  float* slots = reinterpret_cast<float*>(smem + (size_t)S * STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE + (size_t)CW * SLOT * 4);
+  uint64_t* empty = full + S;
+  const uint32_t ring_u = smem_u32(smem), full_u = smem_u32(full), empty_u = smem_u32(empty);
 
-  const int64_t span = i1 - i0;
-  const int64_t n_my = span > warp ? (span - warp + W - 1) / W : 0;
+  // Stages walk the CTA's items in order; all loop state advances incrementally.
+  const int kt_first = (int)(i0 % KT);
+  const int KTi = (int)KT;
+  auto stage_len = [&](int64_t pos, int kt) -> int {
+    int n = KS;
+    if (n > KTi - kt) n = KTi - kt;
+    if ((int64_t)n > i1 - pos) n = (int)(i1 - pos);
+    return n;
+  };
 
-  if (lane == 0)
-    for (int d = 0; d < D; ++d) mbar_init(bar_u + 8 * d, 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_u + 8 * s, 1);
+      mbar_init(empty_u + 8 * s, CW);
+    }
+  }
   fence_mbar_init();
   __syncthreads();
 
-  const uint64_t pol = l2_evict_first_policy();   // weights: streamed once
-  const uint64_t pol_a = l2_evict_last_policy();  // activations: re-read by every CTA
-  // Weights do not depend on the activation pre-pass: start streaming them first.
-  if (lane == 0) {
-    for (int64_t n = 0; n < n_my && n < D; ++n) {
-      const int64_t item = i0 + warp + W * n;
-      const uint32_t bar = bar_u + 8 * (uint32_t)n;
-      mbar_expect_tx(bar, tx);  // one arrival for the stage: weights + activations
-      bulk_g2s(ring_u + (uint32_t)n * STAGE, p.tiles + item * TB, TB, bar, pol);
-    }
-  }
-  pdl_wait();  // the converted activations are ready past this point
-  if (lane == 0) {
-    fence_proxy_async_all();
-    for (int64_t n = 0; n < n_my && n < D; ++n) {
-      const int64_t item = i0 + warp + W * n;
-      const int64_t kt = item % KT;
-      const uint32_t bar = bar_u + 8 * (uint32_t)n;
-      bulk_g2s(ring_u + (uint32_t)n * STAGE + TB, p.Ap + kt * MT * 64, abytes, bar, pol_a);
-    }
-  }
-
-  const float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
-  bool ok = true;
-  int64_t n = 0;  // this warp's item counter
-  int64_t issued = n_my < D ? n_my : D;
-  const int64_t rt_first = i0 / KT, rt_last = (i1 - 1) / KT;
-
-  for (int64_t rt = rt_first; rt <= rt_last; ++rt) {
-    const int64_t seg_hi = min(i1, (rt + 1) * KT);
-    float acc[8][NJ][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int u = 0; u < NJ; ++u)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[j][u][r] = 0.0f;
-
-    while (n < n_my) {
-      const int64_t item = i0 + warp + W * n;
-      if (item >= seg_hi) break;
-      const int slot = (int)(n % D);
-      const uint32_t parity = (uint32_t)((n / D) & 1);
-      if (ok) ok = mbar_wait_bounded(bar_u + 8 * slot, parity, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        const uint32_t sbase = ring_u + (uint32_t)slot * STAGE;
-        // activation fragments (B operand): token rows g and g+8, physical k 16t..16t+15
-        uint32_t bfr[NJ][4][2];
-#pragma unroll
-        for (int u = 0; u < NJ; ++u) {
-          const int m = g + 8 * u;
-          if (m < p.M) {
-            const uint32_t rowa = sbase + TB + m * 128;
-            const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (m & 7)) << 4));
-            const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (m & 7)) << 4));
-            bfr[u][0][0] = v0.x; bfr[u][0][1] = v0.y;
-            bfr[u][1][0] = v0.z; bfr[u][1][1] = v0.w;
-            bfr[u][2][0] = v1.x; bfr[u][2][1] = v1.y;
-            bfr[u][3][0] = v1.z; bfr[u][3][1] = v1.w;
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) bfr[u][q][0] = bfr[u][q][1] = 0u;
-          }
+  if (warp == CW) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();   // weights: streamed once
+      const uint64_t pol_a = l2_evict_last_policy();  // activations: re-read by every CTA
+      const uint32_t per_tile = (uint32_t)(TB + M * 128 + kAScaleStride * 4);
+      // the weights do not depend on the activation pre-pass: start them first
+      int64_t pos = i0;
+      int kt = kt_first, s = 0;
+      for (; s < S && pos < i1; ++s) {
+        const int n = stage_len(pos, kt);
+        mbar_expect_tx(full_u + 8 * s, n * per_tile);
+        bulk_g2s(ring_u + s * STAGE, p.tiles + pos * TB, (uint32_t)(n * TB), full_u + 8 * s, pol);
+        pos += n;
+        kt += n;
+        if (kt == KTi) kt = 0;
+      }
+      pdl_wait();
+      fence_proxy_async_all();
+      pos = i0;
+      kt = kt_first;
+      for (int s2 = 0; s2 < s; ++s2) {
+        const int n = stage_len(pos, kt);
+        bulk_g2s(ring_u + s2 * STAGE + WBYTES, p.Ap + (int64_t)kt * M * 64,
+                 (uint32_t)(n * M * 128), full_u + 8 * s2, pol_a);
+        bulk_g2s(ring_u + s2 * STAGE + SCALES_OFF, p.ascale + (int64_t)kt * kAScaleStride,
+                 (uint32_t)(n * kAScaleStride * 4), full_u + 8 * s2, pol_a);
+        pos += n;
+        kt += n;
+        if (kt == KTi) kt = 0;
+      }
+      int slot = s == S ? 0 : s;
+      uint32_t par = 0;  // phase parity of the empty barrier of `slot` to wait for
+      while (pos < i1) {
+        if (!mbar_wait_bounded(empty_u + 8 * slot, par, kWaitLimitNs)) {
+          atomicExch(p.status, 5);
+          break;
         }
-        const int soff = (FMT == FMT_NV) ? lane * 16 : ((g * 2 + (t >> 1)) * 16);
-        const int4 sv = ld_shared_v4(sbase + kCodeBytes + soff);
-        const uint32_t sw[4] = {(uint32_t)sv.x, (uint32_t)sv.y, (uint32_t)sv.z, (uint32_t)sv.w};
+        const int n = stage_len(pos, kt);
+        const uint32_t dst = ring_u + slot * STAGE;
+        mbar_expect_tx(full_u + 8 * slot, n * per_tile);
+        bulk_g2s(dst, p.tiles + pos * TB, (uint32_t)(n * TB), full_u + 8 * slot, pol);
+        bulk_g2s(dst + WBYTES, p.Ap + (int64_t)kt * M * 64, (uint32_t)(n * M * 128),
+                 full_u + 8 * slot, pol_a);
+        bulk_g2s(dst + SCALES_OFF, p.ascale + (int64_t)kt * kAScaleStride,
+                 (uint32_t)(n * kAScaleStride * 4), full_u + 8 * slot, pol_a);
+        pos += n;
+        kt += n;
+        if (kt == KTi) kt = 0;
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  pdl_wait();
+  const int jp = warp & 3, kq = warp >> 2;  // row blocks 2jp, 2jp+1; k tiles kq, kq+4
+  const float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
+  const int soff = scale_offset(FMT, 2 * jp, g, t);
+  float acc[2][NJ][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int4 wv = ld_shared_v4(sbase + j * 512 + lane * 16);
-          const uint32_t two = (sw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-          const uint32_t sc = (FMT == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
-          const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc);
-          const __half2 sg = __low2half2(sc2), sg8 = __high2half2(sc2);
-          const uint32_t words[4] = {(uint32_t)wv.x, (uint32_t)wv.y, (uint32_t)wv.z,
-                                     (uint32_t)wv.w};
+  for (int b = 0; b < 2; ++b)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t r0, r1, r2, r3;
-            e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
-            __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&r0), sg);
-            __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&r1), sg8);
-            __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&r2), sg);
-            __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&r3), sg8);
-            const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0);
-            const uint32_t a1 = *reinterpret_cast<uint32_t*>(&h1);
-            const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2);
-            const uint32_t a3 = *reinterpret_cast<uint32_t*>(&h3);
+    for (int u = 0; u < NJ; ++u)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[b][u][r] = 0.0f;
+
+  bool ok = true;
+  int64_t pos = i0;
+  int kt = kt_first, slot = 0;
+  uint32_t par = 0;
+  while (pos < i1) {
+    const int n = stage_len(pos, kt);
+    if (ok) ok = mbar_wait_bounded(full_u + 8 * slot, par, kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const uint32_t sbase = ring_u + slot * STAGE;
+#pragma unroll
+      for (int kh = kq; kh < KS; kh += 4) {
+        if (kh < n) {
+          const uint32_t tb = sbase + kh * TB;
+          const uint32_t ab = sbase + WBYTES + kh * M * 128;
+          // activation fragments (B operand): token rows g (+8), physical k 16t .. 16t+15
+          uint32_t bfr[NJ][4][2];
+#pragma unroll
+          for (int u = 0; u < NJ; ++u) {
+            const int m = g + 8 * u;
+            if (m < M) {
+              const uint32_t rowa = ab + m * 128;
+              const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (m & 7)) << 4));
+              const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (m & 7)) << 4));
+              bfr[u][0][0] = v0.x; bfr[u][0][1] = v0.y;
+              bfr[u][1][0] = v0.z; bfr[u][1][1] = v0.w;
+              bfr[u][2][0] = v1.x; bfr[u][2][1] = v1.y;
+              bfr[u][3][0] = v1.z; bfr[u][3][1] = v1.w;
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) bfr[u][q][0] = bfr[u][q][1] = 0u;
+            }
+          }
+          // activation scales of this k tile for the tokens of this lane's accumulators
+          float as[NJ][2];
+#pragma unroll
+          for (int u = 0; u < NJ; ++u) {
+            const uint32_t sa =
+                sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(as[u][0]), "=f"(as[u][1])
+                         : "r"(sa));
+          }
+          uint32_t sc4;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc4) : "r"(tb + soff));
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int j = 2 * jp + b;
+            const int4 wv = ld_shared_v4(tb + j * 512 + lane * 16);
+            const uint32_t two = b ? (sc4 >> 16) : (sc4 & 0xFFFFu);
+            const uint32_t sc = (FMT == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
+            const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc);
+            const __half2 sg = __low2half2(sc2), sg8 = __high2half2(sc2);
+            const uint32_t words[4] = {(uint32_t)wv.x, (uint32_t)wv.y, (uint32_t)wv.z,
+                                       (uint32_t)wv.w};
+            float tmp[NJ][4];
 #pragma unroll
             for (int u = 0; u < NJ; ++u)
-              mma_f16_16816(acc[j][u], a0, a1, a2, a3, bfr[u][q][0], bfr[u][q][1]);
+#pragma unroll
+              for (int r = 0; r < 4; ++r) tmp[u][r] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t r0, r1, r2, r3;
+              e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
+              __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&r0), sg);
+              __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&r1), sg8);
+              __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&r2), sg);
+              __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&r3), sg8);
+              const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0);
+              const uint32_t a1 = *reinterpret_cast<uint32_t*>(&h1);
+              const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2);
+              const uint32_t a3 = *reinterpret_cast<uint32_t*>(&h3);
+#pragma unroll
+              for (int u = 0; u < NJ; ++u)
+                mma_f16_16816(tmp[u], a0, a1, a2, a3, bfr[u][q][0], bfr[u][q][1]);
+            }
+            // this k tile's sums back to the activations' true scale
+#pragma unroll
+            for (int u = 0; u < NJ; ++u) {
+              acc[b][u][0] = fmaf(tmp[u][0], as[u][0], acc[b][u][0]);
+              acc[b][u][1] = fmaf(tmp[u][1], as[u][1], acc[b][u][1]);
+              acc[b][u][2] = fmaf(tmp[u][2], as[u][0], acc[b][u][2]);
+              acc[b][u][3] = fmaf(tmp[u][3], as[u][1], acc[b][u][3]);
+            }
           }
         }
       }
-      __syncwarp();
-      // refill this slot with the item D ahead
-      if (lane == 0 && ok && issued < n_my) {
-        fence_proxy_async_smem();
-        const int64_t nitem = i0 + warp + W * issued;
-        const uint32_t bar = bar_u + 8 * slot;
-        const uint32_t dst = ring_u + (uint32_t)slot * STAGE;
-        mbar_expect_tx(bar, tx);
-        bulk_g2s(dst, p.tiles + nitem * TB, TB, bar, pol);
-        bulk_g2s(dst + TB, p.Ap + (nitem % KT) * MT * 64, abytes, bar, pol_a);
-      }
-      issued = (ok && issued < n_my) ? issued + 1 : issued;
-      ++n;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_u + 8 * slot);
+    pos += n;
+    kt += n;
+    if (++slot == S) {
+      slot = 0;
+      par ^= 1u;
+    }
+    if (kt == KTi) kt = 0;
+    if (pos != i1 && kt != 0) continue;
 
-    // ---- segment flush: warp partials -> slots -> fixed-order sum
-    float* my = slots + (size_t)warp * MT * kSlotPad;
+    // ---- end of a row-tile segment: warp partials -> slots -> fixed-order sums
+    const int64_t rt = (pos - 1) / KT;
+    float* my = slots + warp * SLOT;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int b = 0; b < 2; ++b)
 #pragma unroll
       for (int u = 0; u < NJ; ++u) {
         const int m0 = 2 * t + 8 * u;
-        const int r0 = j * 16 + g;
-        my[m0 * kSlotPad + r0] = acc[j][u][0];
-        my[(m0 + 1) * kSlotPad + r0] = acc[j][u][1];
-        my[m0 * kSlotPad + r0 + 8] = acc[j][u][2];
-        my[(m0 + 1) * kSlotPad + r0 + 8] = acc[j][u][3];
+        const int r0 = b * 16 + g;
+        my[m0 * kSlotPad + r0] = acc[b][u][0];
+        my[(m0 + 1) * kSlotPad + r0] = acc[b][u][1];
+        my[m0 * kSlotPad + r0 + 8] = acc[b][u][2];
+        my[(m0 + 1) * kSlotPad + r0 + 8] = acc[b][u][3];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[b][u][r] = 0.0f;
       }
-    __syncthreads();
-
-    const int64_t seg_lo = max(i0, rt * KT);
+    consumer_sync(CT);
     const int64_t c_lo = owner_of(rt * KT, I, G), c_hi = owner_of(rt * KT + KT - 1, I, G);
     const bool complete = (c_lo == c_hi);
-    (void)seg_lo;
-    const int sel = (rt == rt_first) ? 0 : 1;
-    const int nout = p.M * 128;
-    for (int idx = threadIdx.x; idx < nout; idx += blockDim.x) {
-      const int m = idx >> 7, row = idx & 127;
-      float s = 0.0f;
-      for (int w = 0; w < W; ++w) s += slots[((size_t)w * MT + m) * kSlotPad + row];
+    const int sel = (rt == i0 / KT) ? 0 : 1;
+    const int nout = M * 128;
+    for (int idx = threadIdx.x; idx < nout; idx += CT) {
+      const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
+      float sum = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
       const int64_t rowg = rt * kTileRows + row;
       if (complete) {
         if (rowg < p.N) {
           const float f = rowg < p.seg_split ? f0 : f1;
-          p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(s * f * p.rowscale[m]);
+          p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(sum * f);
         }
       } else {
-        p.partials[(((size_t)c * 2 + sel) * MT + m) * 128 + row] = s;
+        p.partials[(((size_t)c * 2 + sel) * MT + m) * 128 + row] = sum;
       }
     }
     if (!complete) {
       __threadfence();
-      __syncthreads();
+      consumer_sync(CT);
       if (threadIdx.x == 0) {
         const int prev = atomicAdd(&p.counters[rt], 1);
         const int last = (prev == (int)(c_hi - c_lo));
@@ -300,36 +385,46 @@ __global__ void __launch_bounds__(256, 1) k_decode(const DecodeParams p) {
         }
         s_flag = last;
       }
-      __syncthreads();
+      consumer_sync(CT);
       if (s_flag) {
-        for (int idx = threadIdx.x; idx < nout; idx += blockDim.x) {
+        // Contributor cc > c_lo starts inside this row tile (its slot 0); c_lo's slot is 0
+        // only if its range starts exactly at the tile.  Loads are issued in batches of 8
+        // and added in contributor order.
+        const int sel_lo = ((c_lo * I / G) == rt * KT) ? 0 : 1;
+        const int ncon = (int)(c_hi - c_lo + 1);
+        for (int idx = threadIdx.x; idx < nout; idx += CT) {
           const int m = idx >> 7, row = idx & 127;
-          float s = 0.0f;
-          for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
-            const int selc = (rt == (cc * I / G) / KT) ? 0 : 1;
-            s += __ldcg(&p.partials[(((size_t)cc * 2 + selc) * MT + m) * 128 + row]);
+          const size_t off = (size_t)m * 128 + row;
+          float sum = 0.0f;
+          for (int b0 = 0; b0 < ncon; b0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int64_t cc = c_lo + b0 + q;
+              const int selc = (b0 + q == 0) ? sel_lo : 0;
+              v[q] = (b0 + q < ncon)
+                         ? __ldcg(&p.partials[((size_t)cc * 2 + selc) * MT * 128 + off])
+                         : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (b0 + q < ncon) sum += v[q];
           }
           const int64_t rowg = rt * kTileRows + row;
           if (rowg < p.N) {
             const float f = rowg < p.seg_split ? f0 : f1;
-            p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(s * f * p.rowscale[m]);
+            p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(sum * f);
           }
         }
       }
     }
-    __syncthreads();  // slots are rewritten by the next segment
+    consumer_sync(CT);  // slots are rewritten by the next segment
   }
-
-  if (!ok) {
-    if (lane == 0) atomicExch(p.status, 5);
-    // wait (bounded) for this warp's copies still in flight before leaving
-    for (int64_t x = n; x < issued; ++x)
-      mbar_wait_bounded(bar_u + 8 * (int)(x % D), (uint32_t)((x / D) & 1), 100000000ull);
-  }
+  if (!ok && lane == 0) atomicExch(p.status, 5);
 }
 
-// Raises a kernel's dynamic shared memory limit once per device (never during a capture:
-// the first call on a device, made before any capture, does it).
+// Raises a kernel's dynamic shared memory limit once per device (the first call on a
+// device, made before any graph capture, does it).
 template <typename Kern>
 static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
   int dev = 0;
@@ -342,11 +437,11 @@ static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
   return e;
 }
 
-template <int FMT, int MT>
+template <int FMT, int MT, int KS>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   static int done[64] = {0};
-  const size_t smem = decode_smem_bytes(FMT, MT, L.warps, L.stages);
-  cudaError_t e = allow_smem(k_decode<FMT, MT>, 227 * 1024, done);
+  const size_t smem = decode_smem_bytes(FMT, L.M, KS, L.stages);
+  cudaError_t e = allow_smem(k_decode<FMT, MT, KS>, (int)smem, done);
   if (e != cudaSuccess) return e;
   DecodeParams p;
   p.tiles = reinterpret_cast<const uint8_t*>(L.packed) + kHeaderBytes;
@@ -359,7 +454,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.M = L.M;
   p.stages = L.stages;
   p.Ap = reinterpret_cast<const __half*>(L.Ap);
-  p.rowscale = L.rowscale;
+  p.ascale = L.ascale;
   p.C = reinterpret_cast<__nv_bfloat16*>(L.C);
   p.partials = L.partials;
   p.counters = L.counters;
@@ -367,7 +462,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
-  cfg.blockDim = dim3((unsigned)(L.warps * 32));
+  cfg.blockDim = dim3((unsigned)(kConsumerWarps * 32 + 32));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -375,26 +470,35 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT>, p);
+  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS>, p);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) {
   const int mt = decode_mt(L.M);
-  static int done[64] = {0};
-  const size_t prep_smem = (size_t)((L.K + 7) / 8) * 16;
   cudaError_t e = cudaSuccess;
-  if (prep_smem > 48 * 1024) {
-    if (prep_smem > 227 * 1024) return cudaErrorInvalidValue;
-    e = allow_smem(k_prep_a, 227 * 1024, done);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)L.M, (unsigned)((L.KT + kPrepTiles - 1) / kPrepTiles));
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_prep_a, reinterpret_cast<const __nv_bfloat16*>(L.A), L.lda,
+                           L.K, L.KT, L.M, reinterpret_cast<__half*>(L.Ap), L.ascale);
     if (e != cudaSuccess) return e;
   }
-  k_prep_a<<<L.M, 256, prep_smem, s>>>(reinterpret_cast<const __nv_bfloat16*>(L.A), L.lda,
-                                       L.K, L.KT, mt, reinterpret_cast<__half*>(L.Ap),
-                                       L.rowscale);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8>(L, s) : launch_t<FMT_NV, 16>(L, s);
-  else e = (mt == 8) ? launch_t<FMT_MX, 8>(L, s) : launch_t<FMT_MX, 16>(L, s);
+  // stage width in k tiles (KS): 4 or 8
+  if (L.ks == 4) {
+    if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 4>(L, s) : launch_t<FMT_NV, 16, 4>(L, s);
+    else e = (mt == 8) ? launch_t<FMT_MX, 8, 4>(L, s) : launch_t<FMT_MX, 16, 4>(L, s);
+  } else {
+    if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 8>(L, s) : launch_t<FMT_NV, 16, 8>(L, s);
+    else e = (mt == 8) ? launch_t<FMT_MX, 8, 8>(L, s) : launch_t<FMT_MX, 16, 8>(L, s);
+  }
   if (launches) *launches = 2;
   return e;
 }

@@ -28,15 +28,15 @@ struct DecodeLaunch {
   // workspace pieces
   int* status;
   int* counters;          // [RT]
-  float* rowscale;        // [16]
-  void* Ap;               // f16 [KT][MT][64]
+  float* ascale;          // [KT][16] activation scale per (k tile, token)
+  void* Ap;               // f16 [KT][M][64]
   float* partials;        // [grid*2][MT][128]
   // launch shape
-  int grid, warps, stages;
+  int grid, ks, stages;  // CTAs, k tiles per stage (4 or 8), ring depth
 };
 int decode_mt(int M);  // 8 or 16
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
-size_t decode_smem_bytes(int fmt, int mt, int warps, int stages);
+size_t decode_smem_bytes(int fmt, int M, int ks, int stages);
 
 // Prefill tile GEMM (tensor cores), any M.
 struct PrefillLaunch {

@@ -113,55 +113,28 @@ __global__ void __launch_bounds__(256) k_pack(SrcPair s, int fmt, int64_t N, int
   *reinterpret_cast<uint4*>(out + j * 512 + lane * 16) =
       make_uint4(words[0], words[1], words[2], words[3]);
 
-  if (fmt == FMT_NV) {
-    if (i < 32) {
-      const int64_t gpr = K / 16;
-      const int64_t grp = kt * 4 + t;
-      uint32_t w4[4] = {0, 0, 0, 0};
+  // scale bytes: thread (j, lane) writes the pair (rows g, g+8) of row block j for NVFP4;
+  // for MXFP4 the threads with t < 2 write the pair of (j, g, h = t)
+  const bool nv = (fmt == FMT_NV);
+  if (nv || t < 2) {
+    const int64_t gpr = K / (nv ? 16 : 32);
+    const int64_t grp = nv ? kt * 4 + t : kt * 2 + t;
+    uint32_t pair = 0;
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          int64_t row = rt * kTileRows + jj * 16 + g + half * 8;
-          uint32_t v = 0;
-          if (row < N && grp < gpr) {
-            int which;
-            int64_t r;
-            src_row(s, row, which, r);
-            v = s.scales[which][r * gpr + grp];
-          }
-          int byte = jj * 2 + half;
-          w4[byte >> 2] |= v << (8 * (byte & 3));
-        }
+    for (int half = 0; half < 2; ++half) {
+      int64_t row = rt * kTileRows + j * 16 + g + half * 8;
+      uint32_t v = 0;
+      if (row < N && grp < gpr) {
+        int which;
+        int64_t r;
+        src_row(s, row, which, r);
+        const uint8_t b = s.scales[which][r * gpr + grp];
+        v = nv ? b : mx_encode(b, h->emax[which]);
       }
-      *reinterpret_cast<uint4*>(out + kCodeBytes + lane * 16) =
-          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      pair |= v << (8 * half);
     }
-  } else {
-    if (i < 16) {
-      const int gg = i >> 1, hh = i & 1;
-      const int64_t gpr = K / 32;
-      const int64_t grp = kt * 2 + hh;
-      uint32_t w4[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          int64_t row = rt * kTileRows + jj * 16 + gg + half * 8;
-          uint32_t v = 0;
-          if (row < N && grp < gpr) {
-            int which;
-            int64_t r;
-            src_row(s, row, which, r);
-            v = mx_encode(s.scales[which][r * gpr + grp], h->emax[which]);
-          }
-          int byte = jj * 2 + half;
-          w4[byte >> 2] |= v << (8 * (byte & 3));
-        }
-      }
-      *reinterpret_cast<uint4*>(out + kCodeBytes + (gg * 2 + hh) * 16) =
-          make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    }
+    const int off = nv ? scale_offset(FMT_NV, j, g, t) : scale_offset(FMT_MX, j, g, 2 * t);
+    *reinterpret_cast<uint16_t*>(out + off) = static_cast<uint16_t>(pair);
   }
 }
 
@@ -197,34 +170,24 @@ __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, i
       int64_t col = kt * 32 + 8 * t + 2 * q + (b >> 1);
       if (row < N && col < kb) codes[row * kb + col] = (words[q] >> (8 * b)) & 0xFF;
     }
-  if (fmt == FMT_NV) {
-    if (i < 32) {
-      const int64_t gpr = K / 16, grp = kt * 4 + t;
-      uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + lane * 16);
-      uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
-      for (int jj = 0; jj < 8; ++jj)
-        for (int half = 0; half < 2; ++half) {
-          int64_t row = rt * kTileRows + jj * 16 + g + half * 8;
-          int byte = jj * 2 + half;
-          if (row < N && grp < gpr) scales[row * gpr + grp] = (w4[byte >> 2] >> (8 * (byte & 3))) & 0xFF;
+  const bool nv = (fmt == FMT_NV);
+  if (nv || t < 2) {
+    const int64_t gpr = K / (nv ? 16 : 32);
+    const int64_t grp = nv ? kt * 4 + t : kt * 2 + t;
+    const int off = nv ? scale_offset(FMT_NV, j, g, t) : scale_offset(FMT_MX, j, g, 2 * t);
+    const uint32_t pair = *reinterpret_cast<const uint16_t*>(in + off);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      int64_t row = rt * kTileRows + j * 16 + g + half * 8;
+      if (row < N && grp < gpr) {
+        const uint8_t b = (pair >> (8 * half)) & 0xFF;
+        if (nv) {
+          scales[row * gpr + grp] = b;
+        } else {
+          int e = mx_decode(b, h->emax[row < split ? 0 : 1]);
+          scales[row * gpr + grp] = static_cast<uint8_t>(e < 0 ? 0 : e);
         }
-    }
-  } else {
-    if (i < 16) {
-      const int gg = i >> 1, hh = i & 1;
-      const int64_t gpr = K / 32, grp = kt * 2 + hh;
-      uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + (gg * 2 + hh) * 16);
-      uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
-      for (int jj = 0; jj < 8; ++jj)
-        for (int half = 0; half < 2; ++half) {
-          int64_t row = rt * kTileRows + jj * 16 + gg + half * 8;
-          int byte = jj * 2 + half;
-          if (row < N && grp < gpr) {
-            uint8_t enc = (w4[byte >> 2] >> (8 * (byte & 3))) & 0xFF;
-            int e = mx_decode(enc, h->emax[row < split ? 0 : 1]);
-            scales[row * gpr + grp] = static_cast<uint8_t>(e < 0 ? 0 : e);
-          }
-        }
+      }
     }
   }
 }
@@ -241,18 +204,8 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, 
   const int j = i >> 5, lane = i & 31, g = lane >> 2, t = lane & 3;
   uint4 v = *reinterpret_cast<const uint4*>(in + j * 512 + lane * 16);
   uint32_t words[4] = {v.x, v.y, v.z, v.w};
-  uint32_t sc2;
-  if (fmt == FMT_NV) {
-    uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + lane * 16);
-    uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
-    uint32_t two = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
-    sc2 = e4m3x2_to_f16x2(two);
-  } else {
-    uint4 sv = *reinterpret_cast<const uint4*>(in + kCodeBytes + (g * 2 + (t >> 1)) * 16);
-    uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
-    uint32_t two = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
-    sc2 = mxenc2_to_f16x2(two);
-  }
+  const uint32_t two = *reinterpret_cast<const uint16_t*>(in + scale_offset(fmt, j, g, t));
+  const uint32_t sc2 = (fmt == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
   const uint32_t s_g = bcast_lo(sc2), s_g8 = bcast_hi(sc2);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

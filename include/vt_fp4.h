@@ -66,9 +66,9 @@ typedef struct {
 
 /* Optional tuning overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
 typedef struct {
-  int grid;      /* decode: number of CTAs (clamped to [1, 1024]) */
-  int warps;     /* decode: warps per CTA, one of 4, 8, 12, 16 */
-  int stages;    /* decode: TMA ring depth per warp, 2..6 */
+  int grid;      /* decode: number of CTAs (clamped to [1, 512]) */
+  int warps;     /* decode: k tiles (of 64) per pipeline stage, 4 or 8 */
+  int stages;    /* decode: depth of the CTA's TMA ring, 2..16 */
   int force_path;/* 1 decode (requires M <= 16), 2 prefill */
 } vt_fp4_gemm_opts;
 

@@ -37,8 +37,9 @@ def test_nvfp4_dequant_every_code_and_scale_byte(G):
 @pytest.mark.parametrize("e0", [0, 30, 60, 90, 120, 150, 180, 210, 225])
 def test_mxfp4_dequant_every_code_and_scale_byte(e0):
     # the kernels hold MXFP4 scales as f16 powers of two relative to the tensor's largest
-    # scale: a window of 30 exponents is represented exactly
-    N, K = 32, 64
+    # finite scale: the 30 exponents [emax-29, emax] are represented exactly (smaller ones
+    # flush to zero, see test_mxfp4_scale_window_flush)
+    N, K = 31, 64
     codes = np.tile(np.arange(16, dtype=np.uint8), (N, K // 16))
     eb = np.minimum(e0 + np.arange(N), 254).astype(np.uint8)
     eb[-1] = 0xFF  # one NaN row
@@ -47,6 +48,16 @@ def test_mxfp4_dequant_every_code_and_scale_byte(e0):
     got = W.dequant().cpu().numpy()
     want = oracle.dequant(oracle.MXFP4, _pack_codes(codes), scales, 1.0, N, K)
     assert _same_floats(got, want)
+
+
+def test_mxfp4_scale_window_flush():
+    # an exponent more than 29 below the tensor's largest finite exponent contributes zero
+    N, K = 2, 32
+    codes = np.full((N, K), 7, np.uint8)  # +6
+    scales = np.array([[200], [170]], np.uint8)  # 30 below the maximum
+    W = vt.PackedWeight.from_codes(to_dev(_pack_codes(codes)), to_dev(scales), 1.0, vt.MXFP4, N, K)
+    got = W.dequant().cpu().numpy()
+    assert np.all(got[0] == 6.0 * 2.0 ** 73) and np.all(got[1] == 0.0)
 
 
 @pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])

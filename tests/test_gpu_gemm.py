@@ -79,7 +79,7 @@ def test_deterministic_and_launch_shape_independent(fmt):
             again = bf16_host_bits(vt.w4a16_gemm(A, W, workspace=ws))
             assert np.array_equal(first, again)  # same launch shape -> same bits
         for opts in ({"grid": 1}, {"grid": 7}, {"grid": 300}, {"warps": 4}, {"stages": 2},
-                     {"stages": 6, "warps": 4}, {"grid": 512}):
+                     {"stages": 3, "warps": 8}, {"grid": 512}, {"warps": 4, "stages": 7}):
             y = vt.w4a16_gemm(A, W, workspace=ws, opts=opts)
             torch.cuda.synchronize()
             check_rows(y.float().cpu().numpy(), ref, what=f"{opts}")
@@ -105,12 +105,14 @@ def test_strided_operands_and_empty_batch():
 
 
 def test_activation_range_extremes():
-    """Rows of zeros, tiny (1e-30) and huge (1e30) activations: the per-row power-of-two
-    conversion keeps every row within tolerance (and zero rows exactly zero)."""
+    """Rows of zeros, tiny (1e-30) and huge (1e30) activations, and a row whose k tiles differ
+    by 1e20: the per-(token, k tile) power-of-two conversion keeps every row within tolerance
+    (and zero rows exactly zero)."""
     fmt, N, K = vt.NVFP4, 256, 512
     W, codes, scales, G = _packed(fmt, N, K, synth.tensor_id(64, 0, 1))
     base = synth.bf16_bits_to_f32(make_acts(synth.tensor_id(64, 0, 2), 6, K)).astype(np.float64)
     rows = [np.zeros(K), base[1] * 1e-30, base[2] * 1e30, base[3] * 3e4, base[4], base[5] * 1e-3]
+    rows[4][: K // 2] *= 1e20  # two halves of one row 20 orders of magnitude apart
     A = np.stack(rows)
     Ab = torch.tensor(A).to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     y = vt.w4a16_gemm(bf16_dev(Ab), W)
