@@ -17,7 +17,8 @@ from ._lib import GemmOpts, LaunchInfo, VtError, check, lib
 NVFP4, MXFP4 = 0, 1
 GROUP = {NVFP4: 16, MXFP4: 32}
 
-__all__ = ["NVFP4", "MXFP4", "GROUP", "PackedWeight", "w4a16_gemm", "quantize", "prepack_bytes",
+__all__ = ["NVFP4", "MXFP4", "GROUP", "PackedWeight", "w4a16_gemm", "w4a16_gemm_noalloc",
+           "quantize", "prepack_bytes",
            "workspace_status", "VtError", "algorithmic_bytes"]
 
 
@@ -155,6 +156,22 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
                                      out.stride(0), _ptr(workspace), workspace.numel(),
                                      _stream(stream), ctypes.byref(o) if o else None),
           "vt_fp4_w4a16_gemm")
+    return out
+
+
+def w4a16_gemm_noalloc(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """The decode GEMM (M <= 16) on the library's fixed scratch area instead of a caller
+    workspace, for callers that cannot allocate device memory (see vt_fp4_w4a16_gemm_noalloc
+    in include/vt_fp4.h).  Calls must not overlap on the GPU."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    check(lib().vt_fp4_w4a16_gemm_noalloc(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
+                                          out.stride(0), _stream(stream)),
+          "vt_fp4_w4a16_gemm_noalloc")
     return out
 
 

@@ -11,18 +11,10 @@
 
 #include "vt_fp4.h"
 #include "common.cuh"
+#include "handle.h"
 #include "kernels.h"
 
 using namespace vt;
-
-struct vt_fp4_weight_s {
-  int fmt;
-  int64_t N, K, RT, KT;
-  int64_t seg_split;
-  const void* packed;
-  size_t packed_bytes;
-  vt_fp4_launch_info info;
-};
 
 namespace {
 
@@ -153,6 +145,8 @@ vt_status check_handle(vt_fp4_handle W) {
 }
 
 }  // namespace
+
+vt_status vt::set_last_error(vt_status st, const char* msg) { return fail(st, "%s", msg); }
 
 extern "C" {
 

@@ -141,6 +141,23 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
                                void* C, int64_t ldc, void* workspace, size_t ws_bytes,
                                vt_stream_t s, const vt_fp4_gemm_opts* opts);
 
+/* The decode GEMM (M <= 16) without a caller workspace, for callers that cannot allocate
+ * device memory: a host program whose HBM belongs to another allocator (a serving engine
+ * that reserves memory up front, a plugin whose host forbids foreign allocations) or a
+ * call path that must not depend on a runtime allocation.  The pages have no counterpart
+ * of this entry point; it exists for such callers only.
+ *   A, M, lda, W, C, ldc, s  as for vt_fp4_w4a16_gemm (M <= 16; M == 0 is a no-op).
+ * It uses one scratch area of 4 MiB inside the library's device image instead of a
+ * workspace; every GPU that loads the library holds that area until the process exits.
+ * A weight and M whose scratch needs exceed it are rejected with VT_ERR_UNSUPPORTED.
+ * It allocates nothing: no cudaMalloc, no cudaFree.  The first call on a device looks up
+ * the scratch area's device address (with that device current), so make that first call
+ * before any stream capture.  Every call shares the same area and clears its counters on
+ * the stream first: calls that may overlap on the GPU (other streams, other threads) race
+ * and must not be issued. */
+vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                    void* C, int64_t ldc, vt_stream_t s);
+
 /* Reads the workspace status word (synchronises `s`): *status = VT_OK, or VT_ERR_TIMEOUT
  * if a bounded device-side wait gave up during an earlier call; the word is then cleared. */
 vt_status vt_fp4_workspace_status(void* workspace, vt_stream_t s, int* status);
