@@ -310,7 +310,7 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   W->info.path = 2;
   W->info.grid = grid;
-  W->info.warps_per_cta = 0;
+  W->info.warps_per_cta = 14;  // TMA, MMA, 8 dequantiser and 4 epilogue warps
   W->info.m_tile = 128;
   W->info.items = tiles;
   W->info.launches = launches;
