@@ -30,6 +30,7 @@ if ROOT not in sys.path:
 import numpy as np
 
 METRIC = "FP4 W4A16 decode GEMM: HBM GB/s (% of GB300 peak) and µs/call at M=1–8"
+PREFILL_METRIC = "FP4 W4A16 prefill GEMM: tensor TFLOP/s (% of GB300 dense peak)"
 NVFP4, MXFP4 = 0, 1
 GROUP = {NVFP4: 16, MXFP4: 32}
 L2_BYTES = 129 * 10 ** 6
@@ -72,11 +73,26 @@ class Workload:
     projs: list
     layers: int = 1
     note: str = ""
+    kind: str = "decode"   # "decode": HBM GB/s; "prefill": tensor TFLOP/s
     extra: dict = field(default_factory=dict)
+
+    @property
+    def unit(self) -> str:
+        return "TFLOP/s" if self.kind == "prefill" else "GB/s"
 
 
 def _algo_bytes(fmt, N, K, M):
     return N * K // 2 + N * K // GROUP[fmt] + (4 if fmt == NVFP4 else 0) + 2 * M * K
+
+
+def _work(w, N, K, M):
+    """The workload's unit of work for one call: algorithmic bytes (decode) or flops."""
+    return 2 * M * N * K if w.kind == "prefill" else _algo_bytes(w.fmt, N, K, M)
+
+
+def _rate(w, work, seconds):
+    """work per second in the workload's unit (GB/s or TFLOP/s)."""
+    return work / seconds / (1e12 if w.kind == "prefill" else 1e9)
 
 
 WORKLOADS = {
@@ -105,6 +121,11 @@ WORKLOADS = {
         layers=16,
         note="NVFP4 decode layer sweep, 16 layers of distinct weights: gate_up N=2x17408 "
              "K=5120, down N=5120 K=17408, o_proj N=5120 K=6144, M in {1,2,4,8,16}"),
+    "nvfp4_prefill_gate_up_34816x5120": Workload(
+        "nvfp4_prefill_gate_up_34816x5120", 5, NVFP4, [512, 2048, 4096],
+        [Proj("gate_up", 5120, I=17408, wid=5, role=ROLE_GATE)], kind="prefill",
+        note="NVFP4 prefill-shaped GEMM on the tensor-core tile path: fused gate_up "
+             "N=2x17408 K=5120, M in {512,2048,4096}; TFLOP/s = 2*M*N*K / time"),
 }
 DEFAULT_WORKLOAD = "mxfp4_mlp_12288x4096"
 
@@ -254,7 +275,7 @@ def run_gpu(args, rank: int, world: int):
     C = {(M, p.N): torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
          for M in w.Ms for p in w.projs}
     stream = torch.cuda.Stream(device=dev)
-    step_bytes = sum(_algo_bytes(w.fmt, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
+    step_bytes = sum(_work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
     n_calls = len(calls)
 
     def issue(timing_events=None):
@@ -311,7 +332,7 @@ def run_gpu(args, rank: int, world: int):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_total = float(tt.item())
     ms_step = ms_total / args.steps
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = _rate(w, step_bytes * world, ms_step * 1e-3)
 
     # per-call durations: a second graph with an event record node around every call (the
     # event nodes break the overlap between calls, so these durations are slightly larger
@@ -345,7 +366,7 @@ def run_gpu(args, rank: int, world: int):
     for i, (c, layer, pi, M) in enumerate(calls):
         p = w.projs[pi]
         key = (p.name, M)
-        b = _algo_bytes(w.fmt, p.N, p.K, M)
+        b = _work(w, p.N, p.K, M)
         a = agg.setdefault(key, [0.0, 0, 0])
         a[0] += durs[i]
         a[1] += 1
@@ -353,10 +374,10 @@ def run_gpu(args, rank: int, world: int):
     for (name, M), (ms, n, b) in agg.items():
         us = ms * 1e3 / n
         per_call.append({"proj": name, "M": M, "us_per_call": round(us, 3),
-                         "GBps": round(b / n / (us * 1e-6) / 1e9, 1)})
+                         w.unit.replace("/", "p"): round(_rate(w, b / n, us * 1e-6), 1)})
     kernel_ms = sum(durs)
     # the step runs nothing but GEMM calls: their average throughput over the timed region
-    achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    achieved = _rate(w, step_bytes, ms_step * 1e-3)
 
     # end to end: pinned host activations in, host logits out, every call
     e2e = run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist)
@@ -418,7 +439,7 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     ms_step = ms / args.steps
-    return {"value": round(step_bytes * world / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(_rate(w, step_bytes * world, ms_step * 1e-3), 2), "unit": w.unit,
             "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -459,7 +480,7 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0):
         nbytes = 0
         for p, M, n, Ab, c, s, G in inputs:
             oracle.gemm(w.fmt, Ab, c, s, G, n)
-            nbytes += _algo_bytes(w.fmt, n, p.K, M)
+            nbytes += _work(w, n, p.K, M)
         return nbytes, time.perf_counter() - t
 
     frac = 1.0 / 1024
@@ -468,16 +489,20 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0):
     nbytes, dt = run(frac)
     desc = (f"every (projection, M) call of one step of {w.name} on the first "
             f"{frac * 100:.3g}% of each projection's output columns")
-    return nbytes / dt / 1e9, dt, oracle.threads(), desc
+    return _rate(w, nbytes, dt), dt, oracle.threads(), desc
 
 
 # ------------------------------------------------------------------------ main
-def _peak():
+def _peak(w: Workload):
+    """The roofline denominator: measured HBM copy GB/s (decode), or the measured sustained
+    dense bf16 tensor TFLOP/s (prefill; f16 runs at the bf16 rate), else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
+        if w.kind == "prefill":
+            return float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured (sustained bf16)"
         return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+    return (1700.0, "fallback") if w.kind == "prefill" else (6800.0, "fallback")
 
 
 def _profiled_traffic(workload: str):
@@ -521,14 +546,15 @@ def main():
             per_step.append((gbps, dt))
         value = statistics.median(g for g, _ in per_step)
         ms = statistics.median(d for _, d in per_step) * 1e3
-        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        line = {"impl": "reference", "metric": PREFILL_METRIC if w.kind == "prefill" else METRIC,
+                "value": round(value, 4), "unit": w.unit,
                 "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": dict(config, l2="CPU oracle; no GPU"),
-                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                "cpu_baseline": {"value": round(value, 4), "unit": w.unit, "cores": threads,
                                  "kind": "oracle", "sample": desc},
-                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "e2e": {"value": round(value, 4), "unit": w.unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -544,19 +570,25 @@ def main():
         if world > 1:
             dist.destroy_process_group()
         return
-    peak, peak_kind = _peak()
+    peak, peak_kind = _peak(w)
     traffic = _profiled_traffic(w.name)
+    prefill = w.kind == "prefill"
     line = {
-        "metric": METRIC, "value": round(r["value"], 2), "unit": "GB/s", "n_gpus": world,
+        "metric": PREFILL_METRIC if prefill else METRIC, "value": round(r["value"], 2),
+        "unit": w.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16-mma-f32-acc", "data": "synthetic",
         "config": dict(config, parallelism=f"replicas{world}",
-                       l2=f"inputs larger than L2: {r['copies']} weight copies rotate, "
-                          f"{r['step_bytes'] / 1e6:.1f} MB streamed per step",
+                       l2=(f"{r['copies']} weight copies rotate (one per M); activations and "
+                           f"weight tiles are reused through L2 by design" if prefill else
+                           f"inputs larger than L2: {r['copies']} weight copies rotate, "
+                           f"{r['step_bytes'] / 1e6:.1f} MB streamed per step"),
                        calls_per_step=r["calls_per_step"]),
-        "roofline": {"bound": "hbm", "kernel": "k_decode (+ k_prep_a, one GEMM call)",
-                     "achieved": round(r["achieved"], 1), "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "tensor" if prefill else "hbm",
+                     "kernel": ("k_prefill (+ k_prep_rows, one GEMM call)" if prefill else
+                                "k_decode (+ k_prep_a, one GEMM call)"),
+                     "achieved": round(r["achieved"], 1), "peak": peak, "unit": w.unit,
                      "frac": round(r["achieved"] / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic},
         "per_call": r["per_call"],
@@ -567,7 +599,7 @@ def main():
     }
     if not args.no_cpu_baseline:
         gbps, dt, threads, desc = run_oracle_sample(w)
-        line["cpu_baseline"] = {"value": round(gbps, 4), "unit": "GB/s", "cores": threads,
+        line["cpu_baseline"] = {"value": round(gbps, 4), "unit": w.unit, "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
     print(json.dumps(line))
     if world > 1:
