@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   constexpr int SLOT = MT * kSlotPad;  // floats per warp reduction slot (32 rows + pad)
   constexpr int WBYTES = KS * TB;      // weight bytes of a full stage
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_flag;
+  __shared__ int s_flag, s_ncon, s_sello;
+  __shared__ int64_t s_clo;
   // The next kernel in the stream may launch now: it only waits (griddepcontrol.wait)
   // for this grid to finish before it touches anything this grid reads or writes.
   pdl_launch_dependents();
@@ -242,6 +243,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   int64_t pos = i0;
   int kt = kt_first, slot = 0;
   uint32_t par = 0;
+  const int64_t rt_first = i0 / KT;
+  int64_t rt = rt_first;  // row tile of the current segment
   while (pos < i1) {
     const int n = stage_len(pos, kt);
     if (ok) ok = mbar_wait_bounded(full_u + 8 * slot, par, kWaitLimitNs);
@@ -337,8 +340,18 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
     if (kt == KTi) kt = 0;
     if (pos != i1 && kt != 0) continue;
 
-    // ---- end of a row-tile segment: warp partials -> slots -> fixed-order sums
-    const int64_t rt = (pos - 1) / KT;
+    // ---- end of a row-tile segment: warp partials -> slots -> fixed-order sums.  The tile
+    // is complete when it lies inside this CTA's item range; otherwise one thread finds the
+    // CTAs that share it (64-bit divisions, so once per CTA, not per thread).
+    const bool complete = (rt * KT >= i0) && (rt * KT + KT <= i1);
+    const int sel = (rt == rt_first) ? 0 : 1;
+    if (!complete && threadIdx.x == 0) {
+      const int64_t c_lo = owner_of(rt * KT, I, G), c_hi = owner_of(rt * KT + KT - 1, I, G);
+      s_clo = c_lo;
+      s_ncon = (int)(c_hi - c_lo + 1);
+      // contributor c_lo wrote its slot 0 only if its range starts exactly at the tile
+      s_sello = ((c_lo * I / G) == rt * KT) ? 0 : 1;
+    }
     float* my = slots + warp * SLOT;
 #pragma unroll
     for (int b = 0; b < 2; ++b)
@@ -354,9 +367,6 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
         for (int r = 0; r < 4; ++r) acc[b][u][r] = 0.0f;
       }
     consumer_sync(CT);
-    const int64_t c_lo = owner_of(rt * KT, I, G), c_hi = owner_of(rt * KT + KT - 1, I, G);
-    const bool complete = (c_lo == c_hi);
-    const int sel = (rt == i0 / KT) ? 0 : 1;
     const int nout = M * 128;
     for (int idx = threadIdx.x; idx < nout; idx += CT) {
       const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
@@ -374,11 +384,11 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       }
     }
     if (!complete) {
-      __threadfence();
+      if (threadIdx.x < nout) __threadfence();  // the writers publish their partials
       consumer_sync(CT);
       if (threadIdx.x == 0) {
         const int prev = atomicAdd(&p.counters[rt], 1);
-        const int last = (prev == (int)(c_hi - c_lo));
+        const int last = (prev == s_ncon - 1);
         if (last) {
           __threadfence();
           p.counters[rt] = 0;  // self-reset for the next call
@@ -387,11 +397,11 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       }
       consumer_sync(CT);
       if (s_flag) {
-        // Contributor cc > c_lo starts inside this row tile (its slot 0); c_lo's slot is 0
-        // only if its range starts exactly at the tile.  Loads are issued in batches of 8
-        // and added in contributor order.
-        const int sel_lo = ((c_lo * I / G) == rt * KT) ? 0 : 1;
-        const int ncon = (int)(c_hi - c_lo + 1);
+        // Contributor cc > c_lo starts inside this row tile (its slot 0).  Loads are issued
+        // in batches of 8 and added in contributor order.
+        const int64_t c_lo = s_clo;
+        const int sel_lo = s_sello;
+        const int ncon = s_ncon;
         for (int idx = threadIdx.x; idx < nout; idx += CT) {
           const int m = idx >> 7, row = idx & 127;
           const size_t off = (size_t)m * 128 + row;
@@ -419,6 +429,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       }
     }
     consumer_sync(CT);  // slots are rewritten by the next segment
+    ++rt;
   }
   if (!ok && lane == 0) atomicExch(p.status, 5);
 }
