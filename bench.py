@@ -505,14 +505,28 @@ def _peak(w: Workload):
     return (1700.0, "fallback") if w.kind == "prefill" else (6800.0, "fallback")
 
 
-def _profiled_traffic(workload: str):
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if one
-    matches this workload (None otherwise)."""
+def _profiled_traffic(w: Workload, step_work: float, calls: int):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/traffic.json), or None when there is none for this workload or the kernel
+    source changed since it was captured.  Decode traffic grows with the bytes a launch
+    streams, so the captured launch's DRAM/algorithmic ratio is applied to this step's
+    average launch; prefill reports the captured launch as it is."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(path):
-        d = json.load(open(path))
-        return d.get(workload)
-    return None
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(w.name)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha256_16"]:
+        return None
+    if "algorithmic_bytes" in d:
+        ratio = d["dram_bytes"] / d["algorithmic_bytes"]
+        return {"bytes_per_launch": round(ratio * step_work / calls), "dram_over_algorithmic": round(ratio, 4),
+                "captured_launch": d["captured_launch"], "summary": d["summary"]}
+    return {"bytes_per_launch": d["dram_bytes"], "captured_launch": d["captured_launch"],
+            "summary": d["summary"]}
 
 
 def main():
@@ -571,7 +585,7 @@ def main():
             dist.destroy_process_group()
         return
     peak, peak_kind = _peak(w)
-    traffic = _profiled_traffic(w.name)
+    traffic = _profiled_traffic(w, r["step_bytes"], r["calls_per_step"])
     prefill = w.kind == "prefill"
     line = {
         "metric": PREFILL_METRIC if prefill else METRIC, "value": round(r["value"], 2),
@@ -590,7 +604,8 @@ def main():
                                 "k_decode (+ k_prep_a, one GEMM call)"),
                      "achieved": round(r["achieved"], 1), "peak": peak, "unit": w.unit,
                      "frac": round(r["achieved"] / peak, 4), "peak_kind": peak_kind,
-                     "traffic": traffic},
+                     "traffic": traffic["bytes_per_launch"] if traffic else None,
+                     "traffic_detail": traffic},
         "per_call": r["per_call"],
         "e2e": r["e2e"],
         "gpu_launches": r["gpu_launches"],
