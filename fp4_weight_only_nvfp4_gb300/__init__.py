@@ -151,7 +151,8 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
     o = None
     if opts:
         o = GemmOpts(int(opts.get("grid", 0)), int(opts.get("warps", 0)),
-                     int(opts.get("stages", 0)), int(opts.get("force_path", 0)))
+                     int(opts.get("stages", 0)), int(opts.get("force_path", 0)),
+                     int(opts.get("wait_limit_us", 0)), int(opts.get("withhold_weights", 0)))
     check(lib().vt_fp4_w4a16_gemm_ex(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
                                      out.stride(0), _ptr(workspace), workspace.numel(),
                                      _stream(stream), ctypes.byref(o) if o else None),

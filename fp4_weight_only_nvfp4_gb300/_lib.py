@@ -26,7 +26,8 @@ class LaunchInfo(ctypes.Structure):
 
 class GemmOpts(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int), ("warps", ctypes.c_int), ("stages", ctypes.c_int),
-                ("force_path", ctypes.c_int)]
+                ("force_path", ctypes.c_int), ("wait_limit_us", ctypes.c_int),
+                ("withhold_weights", ctypes.c_int)]
 
 
 SIGNATURES = {

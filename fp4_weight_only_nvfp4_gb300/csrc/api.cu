@@ -273,6 +273,8 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
     D.grid = (int)grid;
     D.ks = ks;
     D.stages = stages;
+    D.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
+    D.withhold = opts ? opts->withhold_weights : 0;
     int launches = 0;
     cudaError_t e = launch_decode(D, (cudaStream_t)s, &launches);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -302,6 +304,8 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
   P.rowscale = reinterpret_cast<float*>(ws + L.rowscale);
   P.Ap = ws + L.ap;
   P.grid = (opts && opts->grid) ? opts->grid : sm_count();
+  P.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
+  P.withhold = opts ? opts->withhold_weights : 0;
   int launches = 0, grid = 0;
   int64_t tiles = 0;
   cudaError_t e = launch_prefill(P, (cudaStream_t)s, &launches, &grid, &tiles);

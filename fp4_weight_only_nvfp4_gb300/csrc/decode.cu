@@ -23,7 +23,6 @@
 
 namespace vt {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 constexpr int kAScaleStride = 16;   // floats per k tile in the activation-scale array
 constexpr int kConsumerWarps = 16;
 constexpr int kSlotPad = 36;        // floats per token row of a warp's reduction slot
@@ -106,6 +105,8 @@ struct DecodeParams {
   float* partials;
   int* counters;
   int* status;
+  uint64_t wait_ns;  // limit of every bounded wait
+  int withhold;      // test hook: issue no copies (the waits then run out)
 };
 
 __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t I, int64_t G) {
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
 
   if (warp == CW) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
+    if (lane == 0 && !p.withhold) {
       const uint64_t pol = l2_evict_first_policy();   // weights: streamed once
       const uint64_t pol_a = l2_evict_last_policy();  // activations: re-read by every CTA
       const uint32_t per_tile = (uint32_t)(TB + M * 128 + kAScaleStride * 4);
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       int slot = s == S ? 0 : s;
       uint32_t par = 0;  // phase parity of the empty barrier of `slot` to wait for
       while (pos < i1) {
-        if (!mbar_wait_bounded(empty_u + 8 * slot, par, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(empty_u + 8 * slot, par, p.wait_ns)) {
           atomicExch(p.status, 5);
           break;
         }
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   int64_t rt = rt_first;  // row tile of the current segment
   while (pos < i1) {
     const int n = stage_len(pos, kt);
-    if (ok) ok = mbar_wait_bounded(full_u + 8 * slot, par, kWaitLimitNs);
+    if (ok) ok = mbar_wait_bounded(full_u + 8 * slot, par, p.wait_ns);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       const uint32_t sbase = ring_u + slot * STAGE;
@@ -470,6 +471,8 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.partials = L.partials;
   p.counters = L.counters;
   p.status = L.status;
+  p.wait_ns = L.wait_ns ? L.wait_ns : 2000000000ull;
+  p.withhold = L.withhold;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);

@@ -33,6 +33,8 @@ struct DecodeLaunch {
   float* partials;        // [grid*2][MT][128]
   // launch shape
   int grid, ks, stages;  // CTAs, k tiles per stage (4 or 8), ring depth
+  uint64_t wait_ns;      // limit of every bounded wait
+  int withhold;          // test hook: the producer issues no copies
 };
 int decode_mt(int M);  // 8 or 16
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
@@ -53,6 +55,8 @@ struct PrefillLaunch {
   float* rowscale;        // [Mp]
   void* Ap;               // f16 [Mp][Kp]
   int grid;
+  uint64_t wait_ns;       // limit of every bounded wait
+  int withhold;           // test hook: the producer issues no copies
 };
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches, int* grid_out,
                            int64_t* tiles_out);

@@ -34,7 +34,7 @@ namespace vt {
 
 namespace {
 
-constexpr uint64_t kPfWaitNs = 2000000000ull;
+constexpr uint64_t kPfWaitNs = 2000000000ull;  // drains of copies and MMAs in flight
 constexpr int kBM = 128;          // tokens per tile (MMA M)
 constexpr int kBN = 256;          // weight rows per tile (MMA N): two packed row tiles
 constexpr int kAStages = 4;
@@ -140,13 +140,14 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
 }
 
 // Bounded wait that also gives up when another role has already given up.
-__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                        uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kPfWaitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
@@ -161,7 +162,9 @@ struct PrefillParams {
   const float* rowscale;
   __nv_bfloat16* C;
   int* status;
-  int vec_store;  // C 16-byte aligned and ldc % 8 == 0
+  int vec_store;     // C 16-byte aligned and ldc % 8 == 0
+  uint64_t wait_ns;  // limit of every bounded wait
+  int withhold;      // test hook: issue no copies (the waits then run out)
 };
 
 template <int FMT>
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !p.withhold) {
       // a weight tile serves the token tiles running beside it; an activation tile serves
       // every weight tile over the whole run
       const uint64_t pol_w = l2_evict_normal_policy();
@@ -228,13 +231,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int64_t rt0 = 2 * nt;
         const int nrt = (RT - rt0) >= 2 ? 2 : 1;
         for (int64_t kt = 0; kt < KT; ++kt) {
-          if (!(ok = pf_wait(a_empty + 8 * ia, pa ^ 1u, abort))) break;
+          if (!(ok = pf_wait(a_empty + 8 * ia, pa ^ 1u, abort, p.wait_ns))) break;
           mbar_expect_tx(a_full + 8 * ia, kABytes);
           tma_load_2d(sA + ia * kABytes, &tmA, (int)(kt * kTileK), (int)(mt * kBM), a_full + 8 * ia,
                       pol_a);
           ++a_issued;
           if (++ia == kAStages) { ia = 0; pa ^= 1u; }
-          if (!(ok = pf_wait(p_empty + 8 * ip, pp ^ 1u, abort))) break;
+          if (!(ok = pf_wait(p_empty + 8 * ip, pp ^ 1u, abort, p.wait_ns))) break;
           mbar_expect_tx(p_full + 8 * ip, (uint32_t)(nrt * TB));
           for (int r = 0; r < nrt; ++r)
             bulk_g2s(sP + (ip * 2 + r) * TB, p.tiles + ((rt0 + r) * KT + kt) * TB, TB,
@@ -267,12 +270,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint32_t ia = 0, pa = 0, ib = 0, pb = 0, ab = 0, pab = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
-        if (!(ok = pf_wait(acc_empty + 8 * ab, pab ^ 1u, abort))) break;
+        if (!(ok = pf_wait(acc_empty + 8 * ab, pab ^ 1u, abort, p.wait_ns))) break;
         tc_fence_after();
         const uint32_t d = tmem + ab * kBN;
         for (int64_t kt = 0; kt < KT; ++kt) {
-          if (!(ok = pf_wait(a_full + 8 * ia, pa, abort))) break;
-          if (!(ok = pf_wait(b_full + 8 * ib, pb, abort))) break;
+          if (!(ok = pf_wait(a_full + 8 * ia, pa, abort, p.wait_ns))) break;
+          if (!(ok = pf_wait(b_full + 8 * ib, pb, abort, p.wait_ns))) break;
           tc_fence_after();
           const uint64_t ad = desc_sw128(sA + ia * kABytes);
           const uint64_t bd = desc_sw128(sB + ib * kBBytes);
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int64_t nt = tile / mtiles;
       const int nrt = (RT - 2 * nt) >= 2 ? 2 : 1;
       for (int64_t kt = 0; kt < KT; ++kt) {
-        if (!(ok = pf_wait(p_full + 8 * ip, pp, abort))) break;
+        if (!(ok = pf_wait(p_full + 8 * ip, pp, abort, p.wait_ns))) break;
         int4 cw[2];
         uint32_t sc[2];
 #pragma unroll
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             o8[r][2 * q + 1] = *reinterpret_cast<uint32_t*>(&h3);
           }
         }
-        if (!(ok = pf_wait(b_empty + 8 * ib, pb ^ 1u, abort))) break;
+        if (!(ok = pf_wait(b_empty + 8 * ib, pb ^ 1u, abort, p.wait_ns))) break;
         const uint32_t bt = sB + ib * kBBytes;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     bool ok = true;
     for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
       const int64_t nt = tile / mtiles, mt = tile % mtiles;
-      if (!(ok = pf_wait(acc_full + 8 * ab, pab, abort))) break;
+      if (!(ok = pf_wait(acc_full + 8 * ab, pab, abort, p.wait_ns))) break;
       tc_fence_after();
       const int64_t m = mt * kBM + qd * 32 + lane;
       const bool live = m < p.M;
@@ -557,6 +560,8 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   pp.C = reinterpret_cast<__nv_bfloat16*>(L.C);
   pp.status = L.status;
   pp.vec_store = ((uintptr_t)L.C % 16 == 0) && (L.ldc % 8 == 0);
+  pp.wait_ns = L.wait_ns ? L.wait_ns : 2000000000ull;
+  pp.withhold = L.withhold;
   int64_t grid = L.grid > 0 ? L.grid : 1;
   if (grid > pp.tiles_total) grid = pp.tiles_total;
   e = (L.fmt == FMT_NV) ? launch_main<FMT_NV>(tm, pp, (int)grid, s)

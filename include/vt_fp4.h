@@ -64,12 +64,19 @@ typedef struct {
   int64_t calls;      /* GEMM calls made on this handle so far */
 } vt_fp4_launch_info;
 
-/* Optional tuning overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
+/* Optional overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
 typedef struct {
-  int grid;      /* decode: number of CTAs (clamped to [1, 512]) */
+  int grid;      /* decode: number of CTAs (clamped to [1, 512]); prefill: CTAs (>= 1) */
   int warps;     /* decode: k tiles (of 64) per pipeline stage, 4 or 8 */
   int stages;    /* decode: depth of the CTA's TMA ring, 2..16 */
   int force_path;/* 1 decode (requires M <= 16), 2 prefill */
+  int wait_limit_us;   /* limit of every bounded device-side wait, in microseconds
+                        * (0 = 2 s); a wait that runs out sets VT_ERR_TIMEOUT in the
+                        * workspace status word and the kernel finishes without waiting */
+  int withhold_weights;/* test hook for the failure path: when nonzero the kernels' weight
+                        * producer issues no copies, so the bounded waits run out; the call
+                        * completes, the status word reads VT_ERR_TIMEOUT and the output is
+                        * undefined.  The workspace stays reusable. */
 } vt_fp4_gemm_opts;
 
 /* ---------------------------------------------------------------------- sizes */
