@@ -67,6 +67,10 @@ def _load():
         lib.orc_gemm.argtypes = [ctypes.c_int, _P, _I64, _I64, _P, _P, ctypes.c_float, _I64,
                                  _P, _I64, _P, _P, _P, ctypes.c_int]
         lib.orc_gemm.restype = ctypes.c_int
+        lib.orc_greedy.argtypes = [_P, _I64, _I64, _P, _P]
+        lib.orc_greedy.restype = ctypes.c_int
+        lib.orc_silu_mul.argtypes = [_P, _I64, _I64, _P]
+        lib.orc_silu_mul.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -177,6 +181,31 @@ def gemm(fmt: int, A, codes, scales, G: float, N: int, cols=None, want_f64: bool
     if rc:
         raise ValueError("orc_gemm rejected the input")
     return (y, ybf, y64) if want_f64 else (y, ybf)
+
+
+def greedy(ybf):
+    """Greedy choice per row of bf16 outputs [M, N] (bits): (index int32 [M], value bits
+    uint16 [M]); the largest value, ties to the lowest index, NaN above every number."""
+    ybf, yp = _c(ybf, np.uint16)
+    M, N = ybf.shape
+    idx = np.empty(M, np.int32)
+    val = np.empty(M, np.uint16)
+    if _load().orc_greedy(yp, M, N, idx.ctypes.data, val.ctypes.data):
+        raise ValueError("orc_greedy rejected the input")
+    return idx, val
+
+
+def silu_mul(y):
+    """SiLU-gated MLP input from fused gate_up sums y fp32 [M, 2I]: bf16 bits [M, I] of
+    silu(gate) * up, evaluated in fp64 and rounded once."""
+    y, yp = _c(y, np.float32)
+    M, N2 = y.shape
+    if N2 % 2:
+        raise ValueError("a fused gate_up output has an even number of columns")
+    out = np.empty((M, N2 // 2), np.uint16)
+    if _load().orc_silu_mul(yp, M, N2 // 2, out.ctypes.data):
+        raise ValueError("orc_silu_mul rejected the input")
+    return out
 
 
 def bf16_to_f32(x: np.ndarray) -> np.ndarray:

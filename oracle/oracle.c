@@ -379,3 +379,65 @@ int orc_gemm(int fmt, const uint16_t* A, int64_t M, int64_t K, const uint8_t* co
   free(Af);
   return 0;
 }
+
+/* ------------------------------------------------------------ greedy head */
+/* Greedy token choice over each row of bf16 outputs ybf [M][N]: the index of the largest
+ * value, and among equal values the lowest index.  Source: "re-verify 27B NVFP4 on the
+ * nvidia ModelOpt checkpoint" (PR #178), section "Correctness -- resolved, not fixed": the
+ * greedy argmax breaks a tie by the lowest index (on the true global index); section
+ * "Speed -- warp-shuffle MoE router top-k": under that total order the argmax gives the
+ * same (value, index) in any reduction order.  Values compare as numbers, so -0 equals +0;
+ * a NaN counts as larger than every number and the first NaN wins (a NaN-propagating
+ * argmax).  val (optional) receives the chosen bf16 value. */
+static int greedy_better(double a, double b) {
+  if (isnan(b)) return 0;
+  if (isnan(a)) return 1;
+  return a > b;
+}
+
+int orc_greedy(const uint16_t* ybf, int64_t M, int64_t N, int32_t* idx, uint16_t* val) {
+  if (M < 0 || N <= 0 || N > 2147483647LL) return -1;
+  for (int64_t m = 0; m < M; ++m) {
+    const uint16_t* row = ybf + m * N;
+    int64_t best = 0;
+    for (int64_t n = 1; n < N; ++n)
+      if (greedy_better(bf16_value(row[n]), bf16_value(row[best]))) best = n;
+    idx[m] = (int32_t)best;
+    if (val) val[m] = row[best];
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------- SiLU-gated MLP input */
+/* fp64 -> bf16, one rounding to nearest (ties to even): 8 significant bits for normal
+ * values, multiples of 2^-133 below 2^-126, infinity past the largest bf16. */
+static uint16_t f64_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  const double a = fabs(x);
+  int e = 0;
+  const double mnt = frexp(a, &e);  /* a = mnt * 2^e, mnt in [0.5, 1) */
+  double q;
+  if (a == 0.0) q = 0.0;
+  else if (e - 1 >= -126) q = ldexp(rint(ldexp(mnt, 8)), e - 8);
+  else q = ldexp(rint(ldexp(a, 133)), -133);
+  const float f = (q >= 0x1p128) ? INFINITY : (float)q; /* exact: q fits bf16 */
+  return orc_f32_to_bf16(signbit(x) ? -f : f);
+}
+
+/* The input of the down projection from a fused gate_up output: for gate and up sums
+ * g = y[m][i] and u = y[m][I + i] (fp32, as the GEMM sums them),
+ *   out[m][i] = bf16_RNE( silu(g) * u ),  silu(x) = x / (1 + e^-x),
+ * evaluated in fp64 from the fp32 sums.  Source: "MXFP4 decode-graph + gate_up FUSION
+ * default-ON" (PR #54), "Step 2": gate and up are one GEMM of N = 2I whose halves feed the
+ * SiLU-and-multiply step before down; "Attribution": that glue between the GEMMs is a
+ * measured cost of the decode step. */
+int orc_silu_mul(const float* y, int64_t M, int64_t I, uint16_t* out) {
+  if (M < 0 || I <= 0) return -1;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t i = 0; i < I; ++i) {
+      const double g = (double)y[m * 2 * I + i], u = (double)y[m * 2 * I + I + i];
+      const double s = g / (1.0 + exp(-g));
+      out[m * I + i] = f64_to_bf16(s * u);
+    }
+  return 0;
+}
