@@ -73,7 +73,7 @@ class Workload:
     projs: list
     layers: int = 1
     note: str = ""
-    kind: str = "decode"   # "decode": HBM GB/s; "prefill": tensor TFLOP/s
+    kind: str = "decode"   # "decode"/"greedy": HBM GB/s; "prefill": tensor TFLOP/s
     extra: dict = field(default_factory=dict)
 
     @property
@@ -113,6 +113,11 @@ WORKLOADS = {
         "nvfp4_lm_head_248320x5120", 6, NVFP4, [1, 2, 4, 8],
         [Proj("lm_head", 5120, N=248320, wid=6)],
         note="NVFP4 packed lm_head N=248320, K=5120 (0.666 GiB packed), M in {1,2,4,8}"),
+    "nvfp4_lm_head_greedy_248320x2560": Workload(
+        "nvfp4_lm_head_greedy_248320x2560", 3, NVFP4, [1, 2, 4, 8],
+        [Proj("lm_head", 2560, N=248320, wid=3)], kind="greedy",
+        note="NVFP4 packed lm_head N=248320, K=2560 with the fused greedy head (per-token "
+             "argmax, ties to the lowest index; no logits written), M in {1,2,4,8}"),
     "nvfp4_layer_sweep_5120": Workload(
         "nvfp4_layer_sweep_5120", 4, NVFP4, [1, 2, 4, 8, 16],
         [Proj("gate_up", 5120, I=17408, wid=4, role=ROLE_GATE),
@@ -278,13 +283,23 @@ def run_gpu(args, rank: int, world: int):
     step_bytes = sum(_work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
     n_calls = len(calls)
 
-    def issue(timing_events=None):
+    greedy = w.kind == "greedy"
+
+    def one_call(c, layer, pi, M, unfused=False):
+        p = w.projs[pi]
+        if greedy and not unfused:
+            vt.w4a16_gemm_greedy(A[(M, p.K)], sets[c][layer][pi], workspace=ws, stream=stream)
+            return
+        vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
+                      stream=stream)
+        if unfused:  # the unfused greedy step: logits out, then a separate argmax
+            torch.argmax(C[(M, p.N)], dim=1)
+
+    def issue(timing_events=None, unfused=False):
         for i, (c, layer, pi, M) in enumerate(calls):
-            p = w.projs[pi]
             if timing_events is not None:
                 timing_events[i][0].record(stream)
-            vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
-                          stream=stream)
+            one_call(c, layer, pi, M, unfused)
             if timing_events is not None:
                 timing_events[i][1].record(stream)
 
@@ -356,8 +371,7 @@ def run_gpu(args, rank: int, world: int):
             c, layer, pi, M = calls[i]
             p = w.projs[pi]
             e0.record(stream)
-            vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
-                          stream=stream)
+            one_call(c, layer, pi, M)
             e1.record(stream)
             stream.synchronize()
             durs.append(e0.elapsed_time(e1))
@@ -376,6 +390,29 @@ def run_gpu(args, rank: int, world: int):
         per_call.append({"proj": name, "M": M, "us_per_call": round(us, 3),
                          w.unit.replace("/", "p"): round(_rate(w, b / n, us * 1e-6), 1)})
     kernel_ms = sum(durs)
+    unfused = None
+    if greedy:
+        # the same step with the logits written and a separate argmax per call
+        g3 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                issue(None, unfused=True)
+            with torch.cuda.graph(g3, stream=stream):
+                issue(None, unfused=True)
+            for _ in range(3):
+                g3.replay()
+        stream.synchronize()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            u0.record(stream)
+            for _ in range(args.steps):
+                g3.replay()
+            u1.record(stream)
+        stream.synchronize()
+        ums = u0.elapsed_time(u1) / args.steps
+        unfused = {"ms_per_step": round(ums, 5),
+                   "value": round(_rate(w, step_bytes * world, ums * 1e-3), 2),
+                   "what": "same calls with bf16 logits written and torch.argmax per call"}
     # the step runs nothing but GEMM calls: their average throughput over the timed region
     achieved = _rate(w, step_bytes, ms_step * 1e-3)
 
@@ -386,7 +423,7 @@ def run_gpu(args, rank: int, world: int):
         "value": value, "ms_per_step": ms_step, "step_bytes": step_bytes, "clocks": clocks,
         "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
         "gpu_launches": launches_per_call * n_calls * args.steps, "copies": copies,
-        "calls_per_step": n_calls, "ws_status": ws_status,
+        "calls_per_step": n_calls, "ws_status": ws_status, "unfused": unfused,
     }
 
 
@@ -400,13 +437,20 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
             dA[(M, p.K)] = torch.empty((M, p.K), dtype=torch.bfloat16, device=dev)
             hC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16).pin_memory()
             dC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+    greedy = w.kind == "greedy"
+    hT = {M: torch.empty(M, dtype=torch.int32).pin_memory() for M in w.Ms}
     h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls)
-    d2h = sum(M * w.projs[pi].N * 2 for _, _, pi, M in calls)
+    d2h = sum(M * (4 if greedy else w.projs[pi].N * 2) for _, _, pi, M in calls)
 
     def issue():
         for c, layer, pi, M in calls:
             p = w.projs[pi]
             dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
+            if greedy:
+                tok, _ = vt.w4a16_gemm_greedy(dA[(M, p.K)], sets[c][layer][pi], workspace=ws,
+                                              stream=stream, want_value=False)
+                hT[M].copy_(tok, non_blocking=True)
+                continue
             vt.w4a16_gemm(dA[(M, p.K)], sets[c][layer][pi], out=dC[(M, p.N)], workspace=ws,
                           stream=stream)
             hC[(M, p.N)].copy_(dC[(M, p.N)], non_blocking=True)
@@ -612,6 +656,8 @@ def main():
         "clocks": r["clocks"],
         "workspace_status": r["ws_status"],
     }
+    if r.get("unfused"):
+        line["unfused"] = r["unfused"]
     if not args.no_cpu_baseline:
         gbps, dt, threads, desc = run_oracle_sample(w)
         line["cpu_baseline"] = {"value": round(gbps, 4), "unit": w.unit, "cores": threads,

@@ -160,6 +160,24 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
     return out
 
 
+def w4a16_gemm_greedy(A: torch.Tensor, W: PackedWeight, workspace: torch.Tensor | None = None,
+                      stream=None, want_value: bool = True):
+    """Greedy head (M <= 16): per token, the index (int32 [M]) of the largest bf16 output of
+    A . W^T, ties to the lowest index, and that value (fp32 [M]) -- without writing the
+    outputs.  See vt_fp4_w4a16_gemm_greedy in include/vt_fp4.h."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    M = A.shape[0]
+    token = torch.empty(M, dtype=torch.int32, device=A.device)
+    value = torch.empty(M, dtype=torch.float32, device=A.device) if want_value else None
+    if workspace is None:
+        workspace = W.new_workspace(M)
+    check(lib().vt_fp4_w4a16_gemm_greedy(_ptr(A), M, A.stride(0), W.handle, _ptr(token),
+                                         _ptr(value), _ptr(workspace), workspace.numel(),
+                                         _stream(stream)), "vt_fp4_w4a16_gemm_greedy")
+    return token, value
+
+
 def w4a16_gemm_noalloc(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
                        stream=None) -> torch.Tensor:
     """The decode GEMM (M <= 16) on the library's fixed scratch area instead of a caller

@@ -32,6 +32,11 @@ vt_status cuda_fail(cudaError_t e, const char* where) {
   return fail(VT_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+// Greedy head state inside the workspace's first 256 bytes (after the status word): one
+// 64-bit key per token and the finished-CTA counter; zero between calls.
+constexpr size_t kGreedyKeysOff = 64;
+constexpr size_t kGreedyDoneOff = 64 + 16 * 8;
+
 inline int group_of(int fmt) { return fmt == VT_FP4_NVFP4 ? 16 : 32; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -207,19 +212,27 @@ vt_status vt_fp4_workspace_bytes(vt_fp4_handle W, int64_t M_max, size_t* bytes) 
   return VT_OK;
 }
 
-vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
-                               int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
-                               const vt_fp4_gemm_opts* opts) {
+}  // extern "C"
+
+namespace {
+
+// The GEMM behind vt_fp4_w4a16_gemm_ex and vt_fp4_w4a16_gemm_greedy: with g_idx set, the
+// decode kernel keeps the per-token greedy choice instead of writing C.
+vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
+                    int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
+                    const vt_fp4_gemm_opts* opts, int32_t* g_idx, float* g_val) {
   if (vt_status st = check_handle(W)) return st;
   if (M < 0) return fail(VT_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
   if (M == 0) return VT_OK;
-  if (!A || !C || !workspace) return fail(VT_ERR_INVALID_ARG, "A, C and workspace must be set");
-  if (lda < W->K || ldc < W->N)
+  if (!A || !workspace || !(C || g_idx))
+    return fail(VT_ERR_INVALID_ARG, "A, C and workspace must be set");
+  if (lda < W->K || (!g_idx && ldc < W->N))
     return fail(VT_ERR_INVALID_ARG, "lda (%lld) must be >= K and ldc (%lld) >= N",
                 (long long)lda, (long long)ldc);
   if (!aligned(A, 16) || lda % 8)
     return fail(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda %% 8 == 0");
-  if (!aligned(C, 4) || ldc % 2) return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
+  if (!g_idx && (!aligned(C, 4) || ldc % 2))
+    return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
   if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   const int force = opts ? opts->force_path : 0;
   const bool decode = force ? force == 1 : M <= 16;
@@ -275,6 +288,12 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
     D.stages = stages;
     D.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
     D.withhold = opts ? opts->withhold_weights : 0;
+    if (g_idx) {
+      D.g_idx = g_idx;
+      D.g_val = g_val;
+      D.g_keys = reinterpret_cast<unsigned long long*>(ws + kGreedyKeysOff);
+      D.g_done = reinterpret_cast<unsigned int*>(ws + kGreedyDoneOff);
+    }
     int launches = 0;
     cudaError_t e = launch_decode(D, (cudaStream_t)s, &launches);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -320,6 +339,29 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
   W->info.launches = launches;
   W->info.calls += 1;
   return VT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
+                               int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
+                               const vt_fp4_gemm_opts* opts) {
+  return gemm_impl(A, M, lda, W, C, ldc, workspace, ws_bytes, s, opts, nullptr, nullptr);
+}
+
+vt_status vt_fp4_w4a16_gemm_greedy(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                   int32_t* token, float* value, void* workspace,
+                                   size_t ws_bytes, vt_stream_t s) {
+  if (!token) return fail(VT_ERR_INVALID_ARG, "token must be set");
+  if (M > 16) return fail(VT_ERR_UNSUPPORTED, "the greedy head serves M <= 16");
+  if (W && W->N > 2147483647LL) return fail(VT_ERR_UNSUPPORTED, "N must fit in int32");
+  if (!aligned(token, 4) || (value && !aligned(value, 4)))
+    return fail(VT_ERR_MISALIGNED, "token and value must be 4-byte aligned");
+  vt_fp4_gemm_opts o = {};
+  o.force_path = 1;
+  return gemm_impl(A, M, lda, W, nullptr, 0, workspace, ws_bytes, s, &o, token, value);
 }
 
 vt_status vt_fp4_w4a16_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,

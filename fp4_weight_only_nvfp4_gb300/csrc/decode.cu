@@ -107,10 +107,60 @@ struct DecodeParams {
   int* status;
   uint64_t wait_ns;  // limit of every bounded wait
   int withhold;      // test hook: issue no copies (the waits then run out)
+  // greedy head (g_idx != nullptr): no output is written; per token the largest bf16
+  // output and its lowest index are kept as one 64-bit key, then written to g_idx/g_val
+  int32_t* g_idx;
+  float* g_val;
+  unsigned long long* g_keys;  // [16], zero between calls
+  unsigned int* g_done;        // CTAs finished, zero between calls
 };
+
+// Greedy key of output value h at index n: larger value -> larger key; equal values ->
+// the lower index gives the larger key (ties to the lowest index, "re-verify 27B NVFP4",
+// "Correctness -- resolved, not fixed"); -0 equals +0; NaN above every number.  A max over
+// keys is order-independent, so CTAs may combine them with atomicMax in any order.  Key 0
+// means "no candidate".
+__device__ __forceinline__ unsigned long long greedy_key(__nv_bfloat16 h, int64_t n) {
+  const float v = __bfloat162float(h);
+  uint32_t k;
+  if (v != v) {
+    k = 0xFFFFFFFFu;
+  } else {
+    const uint32_t b = (v == 0.0f) ? 0u : __float_as_uint(v);
+    k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return ((unsigned long long)k << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
+}
+
+__device__ __forceinline__ float greedy_value(unsigned long long key) {
+  const uint32_t k = (uint32_t)(key >> 32);
+  if (k == 0xFFFFFFFFu) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Warp-wide max of the lanes' keys (all 32 lanes take part); lane 0 folds it into the
+// CTA's key of token m in shared memory (keys of one warp always belong to one token m).
+__device__ __forceinline__ void greedy_fold(unsigned long long key, unsigned long long* keys,
+                                            int m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+    key = other > key ? other : key;
+  }
+  if ((threadIdx.x & 31) == 0 && key) atomicMax(keys + m, key);  // shared-memory atomic
+}
 
 __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t I, int64_t G) {
   return ((i + 1) * G - 1) / I;  // the CTA c with c*I/G <= i < (c+1)*I/G
+}
+
+// Arrival on a grid-wide counter: one atomic add with acquire-release semantics at GPU
+// scope.  Preceded by a CTA barrier, it publishes every write the CTA made before the
+// barrier, and the CTA that sees the final count also sees every other CTA's writes.
+__device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* ctr) {
+  unsigned int prev;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+  return prev;
 }
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
@@ -131,6 +181,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   constexpr int WBYTES = KS * TB;      // weight bytes of a full stage
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_flag, s_ncon, s_sello;
+  __shared__ unsigned long long s_gkey[16];  // greedy head: this CTA's best key per token
   __shared__ int64_t s_clo;
   // The next kernel in the stream may launch now: it only waits (griddepcontrol.wait)
   // for this grid to finish before it touches anything this grid reads or writes.
@@ -160,6 +211,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
     return n;
   };
 
+  if (threadIdx.x < 16) s_gkey[threadIdx.x] = 0ull;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_u + 8 * s, 1);
@@ -376,7 +428,11 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
       const int64_t rowg = rt * kTileRows + row;
       if (complete) {
-        if (rowg < p.N) {
+        if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
+          unsigned long long key = 0;
+          if (rowg < p.N) key = greedy_key(__float2bfloat16_rn(sum * (rowg < p.seg_split ? f0 : f1)), rowg);
+          greedy_fold(key, s_gkey, m);
+        } else if (rowg < p.N) {
           const float f = rowg < p.seg_split ? f0 : f1;
           p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(sum * f);
         }
@@ -385,15 +441,11 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       }
     }
     if (!complete) {
-      if (threadIdx.x < nout) __threadfence();  // the writers publish their partials
-      consumer_sync(CT);
+      consumer_sync(CT);  // every partial of this CTA is written
       if (threadIdx.x == 0) {
-        const int prev = atomicAdd(&p.counters[rt], 1);
+        const int prev = (int)arrive_acq_rel(reinterpret_cast<unsigned int*>(&p.counters[rt]));
         const int last = (prev == s_ncon - 1);
-        if (last) {
-          __threadfence();
-          p.counters[rt] = 0;  // self-reset for the next call
-        }
+        if (last) p.counters[rt] = 0;  // self-reset for the next call
         s_flag = last;
       }
       consumer_sync(CT);
@@ -422,7 +474,11 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
               if (b0 + q < ncon) sum += v[q];
           }
           const int64_t rowg = rt * kTileRows + row;
-          if (rowg < p.N) {
+          if (p.g_idx) {
+            unsigned long long key = 0;
+            if (rowg < p.N) key = greedy_key(__float2bfloat16_rn(sum * (rowg < p.seg_split ? f0 : f1)), rowg);
+            greedy_fold(key, s_gkey, m);
+          } else if (rowg < p.N) {
             const float f = rowg < p.seg_split ? f0 : f1;
             p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(sum * f);
           }
@@ -433,6 +489,23 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
     ++rt;
   }
   if (!ok && lane == 0) atomicExch(p.status, 5);
+  if (p.g_idx) {
+    // One global atomic per token per CTA; the last CTA to finish turns the keys into
+    // indices and values and clears them (and the counter) for the next call.
+    consumer_sync(CT);
+    if (threadIdx.x < M && s_gkey[threadIdx.x]) atomicMax(p.g_keys + threadIdx.x, s_gkey[threadIdx.x]);
+    consumer_sync(CT);
+    if (threadIdx.x == 0) s_flag = (arrive_acq_rel(p.g_done) == gridDim.x - 1);
+    consumer_sync(CT);
+    if (s_flag) {
+      if (threadIdx.x < M) {
+        const unsigned long long key = atomicExch(p.g_keys + threadIdx.x, 0ull);
+        p.g_idx[threadIdx.x] = key ? (int32_t)(0xFFFFFFFFu - (uint32_t)key) : -1;
+        if (p.g_val) p.g_val[threadIdx.x] = greedy_value(key);
+      }
+      if (threadIdx.x == 0) atomicExch(p.g_done, 0u);
+    }
+  }
 }
 
 // Raises a kernel's dynamic shared memory limit once per device (the first call on a
@@ -473,6 +546,10 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.status = L.status;
   p.wait_ns = L.wait_ns ? L.wait_ns : 2000000000ull;
   p.withhold = L.withhold;
+  p.g_idx = L.g_idx;
+  p.g_val = L.g_val;
+  p.g_keys = L.g_keys;
+  p.g_done = L.g_done;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);

@@ -35,6 +35,11 @@ struct DecodeLaunch {
   int grid, ks, stages;  // CTAs, k tiles per stage (4 or 8), ring depth
   uint64_t wait_ns;      // limit of every bounded wait
   int withhold;          // test hook: the producer issues no copies
+  // greedy head (g_idx non-null): per-token argmax instead of the output
+  int32_t* g_idx = nullptr;
+  float* g_val = nullptr;
+  unsigned long long* g_keys = nullptr;  // [16] in the workspace
+  unsigned int* g_done = nullptr;
 };
 int decode_mt(int M);  // 8 or 16
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);

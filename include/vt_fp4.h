@@ -148,6 +148,23 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
                                void* C, int64_t ldc, void* workspace, size_t ws_bytes,
                                vt_stream_t s, const vt_fp4_gemm_opts* opts);
 
+/* Greedy head: the decode GEMM (M <= 16) that keeps, per token m, only the index of the
+ * largest output, instead of writing the M x N outputs.  Source: "re-verify 27B NVFP4 on
+ * the nvidia ModelOpt checkpoint" (PR #178), "Correctness -- resolved, not fixed": greedy
+ * sampling takes the argmax with ties broken by the lowest index; "Speed -- warp-shuffle
+ * MoE router top-k": under that total order every reduction order gives the same
+ * (value, index).
+ *   A, M, lda, W, workspace, ws_bytes, s  as for vt_fp4_w4a16_gemm (1 <= M <= 16).
+ *   token  (device) int32 [M]: argmax over n of the bf16 output y[m][n] that
+ *          vt_fp4_w4a16_gemm would write with the same workspace; equal values -> the
+ *          lowest n; -0 equals +0; a NaN output counts as larger than every number.
+ *   value  (device, optional, may be NULL) fp32 [M]: that bf16 output value.
+ * N must fit in int32.  The workspace's first 256 bytes hold the per-token keys between
+ * the kernel's CTAs; they are back to zero when the call completes. */
+vt_status vt_fp4_w4a16_gemm_greedy(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                   int32_t* token, float* value, void* workspace,
+                                   size_t ws_bytes, vt_stream_t s);
+
 /* The decode GEMM (M <= 16) without a caller workspace, for callers that cannot allocate
  * device memory: a host program whose HBM belongs to another allocator (a serving engine
  * that reserves memory up front, a plugin whose host forbids foreign allocations) or a
