@@ -73,7 +73,7 @@ class Workload:
     projs: list
     layers: int = 1
     note: str = ""
-    kind: str = "decode"   # "decode"/"greedy": HBM GB/s; "prefill": tensor TFLOP/s
+    kind: str = "decode"   # "decode"/"greedy"/"mlp_silu": HBM GB/s; "prefill": TFLOP/s
     extra: dict = field(default_factory=dict)
 
     @property
@@ -113,6 +113,12 @@ WORKLOADS = {
         "nvfp4_lm_head_248320x5120", 6, NVFP4, [1, 2, 4, 8],
         [Proj("lm_head", 5120, N=248320, wid=6)],
         note="NVFP4 packed lm_head N=248320, K=5120 (0.666 GiB packed), M in {1,2,4,8}"),
+    "mxfp4_mlp_silu_12288x4096": Workload(
+        "mxfp4_mlp_silu_12288x4096", 2, MXFP4, [1, 2, 4, 8],
+        [Proj("gate_up", 4096, I=12288, wid=2, role=ROLE_GATE),
+         Proj("down", 12288, N=4096, wid=2, role=13)], kind="mlp_silu",
+        note="MXFP4 dense MLP decode as a chain: gate_up (paired) with the SiLU-and-multiply "
+             "epilogue writes act [M][12288], down reads it; M in {1,2,4,8}"),
     "nvfp4_lm_head_greedy_248320x2560": Workload(
         "nvfp4_lm_head_greedy_248320x2560", 3, NVFP4, [1, 2, 4, 8],
         [Proj("lm_head", 2560, N=248320, wid=3)], kind="greedy",
@@ -219,7 +225,8 @@ def _build_weights(w: Workload, copies: int, dev):
                         c_, s_, g_ = vt.quantize(Wb, w.fmt)
                         halves.append((c_, s_, float(g_.item())))
                         del Wb
-                    ws.append(vt.PackedWeight.gate_up(halves[0], halves[1], w.fmt, p.I, p.K))
+                    ws.append(vt.PackedWeight.gate_up(halves[0], halves[1], w.fmt, p.I, p.K,
+                                                      paired=(w.kind == "mlp_silu")))
                 else:
                     Wb = (torch.randn((p.N, p.K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
                     c_, s_, g_ = vt.quantize(Wb, w.fmt)
@@ -284,11 +291,27 @@ def run_gpu(args, rank: int, world: int):
     n_calls = len(calls)
 
     greedy = w.kind == "greedy"
+    silu = w.kind == "mlp_silu"
+    # the MLP chain: gate_up writes act [M][I], down reads it
+    I_mlp = max((p.I for p in w.projs if p.fused), default=0)
+    act = {M: torch.zeros((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms} if silu else {}
 
     def one_call(c, layer, pi, M, unfused=False):
         p = w.projs[pi]
         if greedy and not unfused:
             vt.w4a16_gemm_greedy(A[(M, p.K)], sets[c][layer][pi], workspace=ws, stream=stream)
+            return
+        if silu:
+            if p.fused and not unfused:
+                vt.w4a16_gemm_silu_mul(A[(M, p.K)], sets[c][layer][pi], out=act[M], workspace=ws,
+                                       stream=stream)
+            elif p.fused:  # unfused: [M][2I] out, then SiLU-and-multiply by torch
+                y = C[(M, p.N)]
+                vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=y, workspace=ws, stream=stream)
+                act[M].copy_(torch.nn.functional.silu(y[:, :p.I].float()) * y[:, p.I:].float())
+            else:
+                vt.w4a16_gemm(act[M], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
+                              stream=stream)
             return
         vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
                       stream=stream)
@@ -391,7 +414,7 @@ def run_gpu(args, rank: int, world: int):
                          w.unit.replace("/", "p"): round(_rate(w, b / n, us * 1e-6), 1)})
     kernel_ms = sum(durs)
     unfused = None
-    if greedy:
+    if greedy or silu:
         # the same step with the logits written and a separate argmax per call
         g3 = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
@@ -412,7 +435,8 @@ def run_gpu(args, rank: int, world: int):
         ums = u0.elapsed_time(u1) / args.steps
         unfused = {"ms_per_step": round(ums, 5),
                    "value": round(_rate(w, step_bytes * world, ums * 1e-3), 2),
-                   "what": "same calls with bf16 logits written and torch.argmax per call"}
+                   "what": ("same calls with bf16 logits written and torch.argmax per call" if greedy
+                            else "gate_up writes [M][2I]; torch SiLU-and-multiply; down")}
     # the step runs nothing but GEMM calls: their average throughput over the timed region
     achieved = _rate(w, step_bytes, ms_step * 1e-3)
 
@@ -438,13 +462,30 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
             hC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16).pin_memory()
             dC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
     greedy = w.kind == "greedy"
+    silu = w.kind == "mlp_silu"
     hT = {M: torch.empty(M, dtype=torch.int32).pin_memory() for M in w.Ms}
-    h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls)
-    d2h = sum(M * (4 if greedy else w.projs[pi].N * 2) for _, _, pi, M in calls)
+    if silu:  # the MLP chain: host input of gate_up in, host output of down out
+        I_mlp = max(p.I for p in w.projs if p.fused)
+        dAct = {M: torch.empty((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms}
+        h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls if w.projs[pi].fused)
+        d2h = sum(M * w.projs[pi].N * 2 for _, _, pi, M in calls if not w.projs[pi].fused)
+    else:
+        h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls)
+        d2h = sum(M * (4 if greedy else w.projs[pi].N * 2) for _, _, pi, M in calls)
 
     def issue():
         for c, layer, pi, M in calls:
             p = w.projs[pi]
+            if silu:
+                if p.fused:
+                    dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
+                    vt.w4a16_gemm_silu_mul(dA[(M, p.K)], sets[c][layer][pi], out=dAct[M],
+                                           workspace=ws, stream=stream)
+                else:
+                    vt.w4a16_gemm(dAct[M], sets[c][layer][pi], out=dC[(M, p.N)], workspace=ws,
+                                  stream=stream)
+                    hC[(M, p.N)].copy_(dC[(M, p.N)], non_blocking=True)
+                continue
             dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
             if greedy:
                 tok, _ = vt.w4a16_gemm_greedy(dA[(M, p.K)], sets[c][layer][pi], workspace=ws,

@@ -67,19 +67,25 @@ class PackedWeight:
         return cls(h, packed, fmt, N, K)
 
     @classmethod
-    def gate_up(cls, gate: tuple, up: tuple, fmt: int, I: int, K: int, stream=None) -> "PackedWeight":
-        """Fused gate_up: ``gate``/``up`` are (codes, scales, global); N = 2*I."""
+    def gate_up(cls, gate: tuple, up: tuple, fmt: int, I: int, K: int, stream=None,
+                paired: bool = False) -> "PackedWeight":
+        """Fused gate_up: ``gate``/``up`` are (codes, scales, global); N = 2*I.  ``paired``
+        packs gate and up rows side by side for the SiLU-and-multiply epilogue
+        (vt_fp4_prepack_gate_up_paired)."""
         (gc, gs, gg), (uc, us, ug) = gate, up
         _check_src(gc, gs, I, K, fmt)
         _check_src(uc, us, I, K, fmt)
         nbytes = prepack_bytes(fmt, 2 * I, K)
         packed = torch.empty(nbytes, dtype=torch.uint8, device=gc.device)
         h = ctypes.c_void_p(0)
-        check(lib().vt_fp4_prepack_gate_up(_ptr(gc), _ptr(gs), float(gg), _ptr(uc), _ptr(us),
-                                           float(ug), fmt, I, K, _ptr(packed), nbytes,
-                                           _stream(stream), ctypes.byref(h)),
-              "vt_fp4_prepack_gate_up")
-        return cls(h, packed, fmt, 2 * I, K)
+        name = "vt_fp4_prepack_gate_up_paired" if paired else "vt_fp4_prepack_gate_up"
+        check(getattr(lib(), name)(_ptr(gc), _ptr(gs), float(gg), _ptr(uc), _ptr(us),
+                                   float(ug), fmt, I, K, _ptr(packed), nbytes,
+                                   _stream(stream), ctypes.byref(h)), name)
+        W = cls(h, packed, fmt, 2 * I, K)
+        W.I = I
+        W.paired = paired
+        return W
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -157,6 +163,23 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
                                      out.stride(0), _ptr(workspace), workspace.numel(),
                                      _stream(stream), ctypes.byref(o) if o else None),
           "vt_fp4_w4a16_gemm")
+    return out
+
+
+def w4a16_gemm_silu_mul(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[M, I] (bf16) = silu(gate) * up of a paired gate_up weight, in one call (see
+    vt_fp4_w4a16_gemm_silu_mul in include/vt_fp4.h)."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, W.N // 2), dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = W.new_workspace(M)
+    check(lib().vt_fp4_w4a16_gemm_silu_mul(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
+                                           out.stride(0), _ptr(workspace), workspace.numel(),
+                                           _stream(stream)), "vt_fp4_w4a16_gemm_silu_mul")
     return out
 
 

@@ -36,6 +36,10 @@ SIGNATURES = {
                              ctypes.POINTER(_P)]),
     "vt_fp4_prepack_gate_up": (_ST, [_P, _P, ctypes.c_float, _P, _P, ctypes.c_float, ctypes.c_int,
                                      _I64, _I64, _P, _SZ, _P, ctypes.POINTER(_P)]),
+    "vt_fp4_prepack_gate_up_paired": (_ST, [_P, _P, ctypes.c_float, _P, _P, ctypes.c_float,
+                                            ctypes.c_int, _I64, _I64, _P, _SZ, _P,
+                                            ctypes.POINTER(_P)]),
+    "vt_fp4_w4a16_gemm_silu_mul": (_ST, [_P, _I64, _I64, _P, _P, _I64, _P, _SZ, _P]),
     "vt_fp4_destroy": (_ST, [_P]),
     "vt_fp4_shape": (_ST, [_P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(_I64),
                            ctypes.POINTER(_I64)]),

@@ -97,7 +97,8 @@ int sm_count() {
 
 vt_status do_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
                      const float globals[2], int nsrc, vt_fp4_format fmt, int64_t I, int64_t K,
-                     void* dst, size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out) {
+                     void* dst, size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out,
+                     uint32_t layout = kLayoutRows) {
   if (!out) return fail(VT_ERR_INVALID_ARG, "out handle pointer is NULL");
   *out = nullptr;
   const int64_t N = I * nsrc;
@@ -128,6 +129,7 @@ vt_status do_prepack(const uint8_t* const codes[2], const uint8_t* const scales[
   h->RT = cdiv(N, kTileRows);
   h->KT = cdiv(K, kTileK);
   h->seg_split = nsrc == 2 ? I : N;
+  h->layout = (int)layout;
   h->packed = dst;
   h->packed_bytes = need;
   memset(&h->info, 0, sizeof(h->info));
@@ -135,7 +137,7 @@ vt_status do_prepack(const uint8_t* const codes[2], const uint8_t* const scales[
   const uint8_t* s2[2] = {scales[0], nsrc == 2 ? scales[1] : scales[0]};
   const float f1 = nsrc == 2 ? globals[1] : globals[0];
   cudaError_t e = launch_prepack(c2, s2, h->seg_split, globals[0], f1, fmt, N, K, h->RT, h->KT,
-                                 dst, (cudaStream_t)s);
+                                 layout, dst, (cudaStream_t)s);
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "prepack launch");
@@ -185,6 +187,17 @@ vt_status vt_fp4_prepack_gate_up(const uint8_t* gate_codes, const uint8_t* gate_
   return do_prepack(c, sc, g, 2, fmt, I, K, packed_dst, dst_bytes, s, out);
 }
 
+vt_status vt_fp4_prepack_gate_up_paired(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                        float gate_global, const uint8_t* up_codes,
+                                        const uint8_t* up_scales, float up_global,
+                                        vt_fp4_format fmt, int64_t I, int64_t K, void* packed_dst,
+                                        size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out) {
+  const uint8_t* c[2] = {gate_codes, up_codes};
+  const uint8_t* sc[2] = {gate_scales, up_scales};
+  const float g[2] = {gate_global, up_global};
+  return do_prepack(c, sc, g, 2, fmt, I, K, packed_dst, dst_bytes, s, out, kLayoutPaired);
+}
+
 vt_status vt_fp4_destroy(vt_fp4_handle W) {
   delete W;
   return VT_OK;
@@ -220,13 +233,15 @@ namespace {
 // decode kernel keeps the per-token greedy choice instead of writing C.
 vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
                     int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
-                    const vt_fp4_gemm_opts* opts, int32_t* g_idx, float* g_val) {
+                    const vt_fp4_gemm_opts* opts, int32_t* g_idx, float* g_val,
+                    bool silu = false) {
   if (vt_status st = check_handle(W)) return st;
   if (M < 0) return fail(VT_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
   if (M == 0) return VT_OK;
   if (!A || !workspace || !(C || g_idx))
     return fail(VT_ERR_INVALID_ARG, "A, C and workspace must be set");
-  if (lda < W->K || (!g_idx && ldc < W->N))
+  const int64_t ncols = silu ? W->seg_split : W->N;  // output columns
+  if (lda < W->K || (!g_idx && ldc < ncols))
     return fail(VT_ERR_INVALID_ARG, "lda (%lld) must be >= K and ldc (%lld) >= N",
                 (long long)lda, (long long)ldc);
   if (!aligned(A, 16) || lda % 8)
@@ -288,6 +303,8 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     D.stages = stages;
     D.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
     D.withhold = opts ? opts->withhold_weights : 0;
+    D.layout = (uint32_t)W->layout;
+    D.silu = silu ? 1 : 0;
     if (g_idx) {
       D.g_idx = g_idx;
       D.g_val = g_val;
@@ -325,6 +342,8 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
   P.grid = (opts && opts->grid) ? opts->grid : sm_count();
   P.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
   P.withhold = opts ? opts->withhold_weights : 0;
+  P.layout = (uint32_t)W->layout;
+  P.silu = silu ? 1 : 0;
   int launches = 0, grid = 0;
   int64_t tiles = 0;
   cudaError_t e = launch_prefill(P, (cudaStream_t)s, &launches, &grid, &tiles);
@@ -364,6 +383,16 @@ vt_status vt_fp4_w4a16_gemm_greedy(const void* A, int64_t M, int64_t lda, vt_fp4
   return gemm_impl(A, M, lda, W, nullptr, 0, workspace, ws_bytes, s, &o, token, value);
 }
 
+vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                     void* C, int64_t ldc, void* workspace, size_t ws_bytes,
+                                     vt_stream_t s) {
+  if (vt_status st = check_handle(W)) return st;
+  if (W->layout != kLayoutPaired)
+    return fail(VT_ERR_INVALID_ARG,
+                "the SiLU-and-multiply epilogue needs a weight from vt_fp4_prepack_gate_up_paired");
+  return gemm_impl(A, M, lda, W, C, ldc, workspace, ws_bytes, s, nullptr, nullptr, nullptr, true);
+}
+
 vt_status vt_fp4_w4a16_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
                             int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s) {
   return vt_fp4_w4a16_gemm_ex(A, M, lda, W, C, ldc, workspace, ws_bytes, s, nullptr);
@@ -396,16 +425,16 @@ vt_status vt_fp4_stats(vt_fp4_handle W, vt_fp4_launch_info* info) {
 vt_status vt_fp4_dequant(vt_fp4_handle W, float* out, vt_stream_t s) {
   if (vt_status st = check_handle(W)) return st;
   if (!out) return fail(VT_ERR_INVALID_ARG, "out is NULL");
-  cudaError_t e = launch_dequant(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split, out,
-                                 (cudaStream_t)s);
+  cudaError_t e = launch_dequant(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split,
+                                 (uint32_t)W->layout, out, (cudaStream_t)s);
   return e == cudaSuccess ? VT_OK : cuda_fail(e, "dequant launch");
 }
 
 vt_status vt_fp4_unpack(vt_fp4_handle W, uint8_t* codes, uint8_t* scales, vt_stream_t s) {
   if (vt_status st = check_handle(W)) return st;
   if (!codes || !scales) return fail(VT_ERR_INVALID_ARG, "codes and scales must be set");
-  cudaError_t e = launch_unpack(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split, codes,
-                                scales, (cudaStream_t)s);
+  cudaError_t e = launch_unpack(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split,
+                                (uint32_t)W->layout, codes, scales, (cudaStream_t)s);
   return e == cudaSuccess ? VT_OK : cuda_fail(e, "unpack launch");
 }
 

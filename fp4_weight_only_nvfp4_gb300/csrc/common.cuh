@@ -55,10 +55,30 @@ struct PackedHeader {
   int64_t seg_split;   // rows [0, seg_split) use factor[0], the rest factor[1]
   float factor[2];     // epilogue multiplier per segment (NVFP4 global, MXFP4 2^(emax-140))
   int32_t emax[2];     // MXFP4: largest finite E8M0 byte per segment
-  uint32_t pad[52];
+  uint32_t layout;     // kLayoutRows or kLayoutPaired
+  uint32_t pad[51];
 };
 static_assert(sizeof(PackedHeader) == kHeaderBytes, "header size");
 constexpr uint32_t kMagic = 0x34465456u;  // "VTF4"
+
+// Row order of the packed tiles.  kLayoutRows: packed row p is weight row p (a fused
+// gate_up weight stacks gate rows [0, I) over up rows [I, 2I)).  kLayoutPaired (fused
+// gate_up only): each 128-row tile holds 64 gate rows and the same 64 up rows, so the
+// SiLU-and-multiply of a pair happens inside one tile: packed row p of tile r = p / 128 is
+// gate row 64r + (p % 128) when p % 128 < 64, else up row 64r + (p % 128) - 64.
+enum : uint32_t { kLayoutRows = 0, kLayoutPaired = 1 };
+
+// The weight row (in gate-over-up order, 0 <= n < 2I or < N) that packed row p holds, or
+// -1 for a padding row.  `I` is the gate/up split (the fused weight's half size).
+__host__ __device__ __forceinline__ int64_t packed_to_row(uint32_t layout, int64_t p, int64_t N,
+                                                          int64_t I) {
+  if (layout == kLayoutPaired) {
+    const int64_t r = (p >> 7) * 64 + (p & 63);
+    if (r >= I) return -1;
+    return (p & 64) ? I + r : r;
+  }
+  return p < N ? p : -1;
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

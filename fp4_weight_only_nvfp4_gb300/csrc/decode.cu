@@ -113,7 +113,12 @@ struct DecodeParams {
   float* g_val;
   unsigned long long* g_keys;  // [16], zero between calls
   unsigned int* g_done;        // CTAs finished, zero between calls
+  uint32_t layout;             // packed row order (kLayoutRows / kLayoutPaired)
+  int silu;                    // paired gate_up: write silu(gate) * up, C is [M][I]
 };
+
+// SiLU(x) = x / (1 + e^-x) in fp32 (e^-x overflowing to infinity gives -0 for large -x).
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
 // Greedy key of output value h at index n: larger value -> larger key; equal values ->
 // the lower index gives the larger key (ties to the lowest index, "re-verify 27B NVFP4",
@@ -421,23 +426,40 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       }
     consumer_sync(CT);
     const int nout = M * 128;
-    for (int idx = threadIdx.x; idx < nout; idx += CT) {
-      const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
-      float sum = 0.0f;
+    if (complete && p.silu) {
+      // paired tile: rows j < 64 are gate rows, rows 64 + j the matching up rows
+      for (int idx = threadIdx.x; idx < M * 64; idx += CT) {
+        const int m = idx >> 6, j = idx & 63;
+        float gs = 0.0f, us = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
-      const int64_t rowg = rt * kTileRows + row;
-      if (complete) {
-        if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
-          unsigned long long key = 0;
-          if (rowg < p.N) key = greedy_key(__float2bfloat16_rn(sum * (rowg < p.seg_split ? f0 : f1)), rowg);
-          greedy_fold(key, s_gkey, m);
-        } else if (rowg < p.N) {
-          const float f = rowg < p.seg_split ? f0 : f1;
-          p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(sum * f);
+        for (int q = 0; q < 4; ++q) {
+          gs += slots[(q * 4 + (j >> 5)) * SLOT + m * kSlotPad + (j & 31)];
+          us += slots[(q * 4 + 2 + (j >> 5)) * SLOT + m * kSlotPad + (j & 31)];
         }
-      } else {
-        p.partials[(((size_t)c * 2 + sel) * MT + m) * 128 + row] = sum;
+        const int64_t i = rt * 64 + j;
+        if (i < p.seg_split)
+          p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
+      }
+    } else {
+      for (int idx = threadIdx.x; idx < nout; idx += CT) {
+        const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
+        if (complete) {
+          // the weight row (and output column) this tile row holds, -1 for padding
+          const int64_t n = packed_to_row(p.layout, rt * kTileRows + row, p.N, p.seg_split);
+          if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
+            unsigned long long key = 0;
+            if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
+            greedy_fold(key, s_gkey, m);
+          } else if (n >= 0) {
+            const float f = n < p.seg_split ? f0 : f1;
+            p.C[(int64_t)m * p.ldc + n] = __float2bfloat16_rn(sum * f);
+          }
+        } else {
+          p.partials[(((size_t)c * 2 + sel) * MT + m) * 128 + row] = sum;
+        }
       }
     }
     if (!complete) {
@@ -455,8 +477,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
         const int64_t c_lo = s_clo;
         const int sel_lo = s_sello;
         const int ncon = s_ncon;
-        for (int idx = threadIdx.x; idx < nout; idx += CT) {
-          const int m = idx >> 7, row = idx & 127;
+        // the CTAs' partial sum of (token m, tile row `row`), added in contributor order
+        auto tile_sum = [&](int m, int row) -> float {
           const size_t off = (size_t)m * 128 + row;
           float sum = 0.0f;
           for (int b0 = 0; b0 < ncon; b0 += 8) {
@@ -473,14 +495,28 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
             for (int q = 0; q < 8; ++q)
               if (b0 + q < ncon) sum += v[q];
           }
-          const int64_t rowg = rt * kTileRows + row;
+          return sum;
+        };
+        if (p.silu) {
+          for (int idx = threadIdx.x; idx < M * 64; idx += CT) {
+            const int m = idx >> 6, j = idx & 63;
+            const float gs = tile_sum(m, j), us = tile_sum(m, 64 + j);
+            const int64_t i = rt * 64 + j;
+            if (i < p.seg_split)
+              p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
+          }
+        }
+        for (int idx = threadIdx.x; idx < (p.silu ? 0 : nout); idx += CT) {
+          const int m = idx >> 7, row = idx & 127;
+          const float sum = tile_sum(m, row);
+          const int64_t n = packed_to_row(p.layout, rt * kTileRows + row, p.N, p.seg_split);
           if (p.g_idx) {
             unsigned long long key = 0;
-            if (rowg < p.N) key = greedy_key(__float2bfloat16_rn(sum * (rowg < p.seg_split ? f0 : f1)), rowg);
+            if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
             greedy_fold(key, s_gkey, m);
-          } else if (rowg < p.N) {
-            const float f = rowg < p.seg_split ? f0 : f1;
-            p.C[(int64_t)m * p.ldc + rowg] = __float2bfloat16_rn(sum * f);
+          } else if (n >= 0) {
+            const float f = n < p.seg_split ? f0 : f1;
+            p.C[(int64_t)m * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
         }
       }
@@ -550,6 +586,8 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.g_val = L.g_val;
   p.g_keys = L.g_keys;
   p.g_done = L.g_done;
+  p.layout = L.layout;
+  p.silu = L.silu;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);

@@ -9,6 +9,7 @@ struct vt_fp4_weight_s {
   int fmt;
   int64_t N, K, RT, KT;
   int64_t seg_split;
+  int layout;  // kLayoutRows or kLayoutPaired
   const void* packed;
   size_t packed_bytes;
   vt_fp4_launch_info info;

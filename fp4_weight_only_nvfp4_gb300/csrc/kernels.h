@@ -7,12 +7,13 @@ namespace vt {
 
 cudaError_t launch_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
                            int64_t split, float f0, float f1, int fmt, int64_t N, int64_t K,
-                           int64_t RT, int64_t KT, void* dst, cudaStream_t s);
+                           int64_t RT, int64_t KT, uint32_t layout, void* dst, cudaStream_t s);
 cudaError_t launch_unpack(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
-                          int64_t KT, int64_t split, uint8_t* codes, uint8_t* scales,
-                          cudaStream_t s);
+                          int64_t KT, int64_t split, uint32_t layout, uint8_t* codes,
+                          uint8_t* scales, cudaStream_t s);
 cudaError_t launch_dequant(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
-                           int64_t KT, int64_t split, float* out, cudaStream_t s);
+                           int64_t KT, int64_t split, uint32_t layout, float* out,
+                           cudaStream_t s);
 
 // Decode GEMM (M <= 16).
 struct DecodeLaunch {
@@ -40,6 +41,8 @@ struct DecodeLaunch {
   float* g_val = nullptr;
   unsigned long long* g_keys = nullptr;  // [16] in the workspace
   unsigned int* g_done = nullptr;
+  uint32_t layout = 0;   // packed row order (kLayoutRows / kLayoutPaired)
+  int silu = 0;          // paired gate_up: C[M][I] = silu(gate) * up
 };
 int decode_mt(int M);  // 8 or 16
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
@@ -62,6 +65,8 @@ struct PrefillLaunch {
   int grid;
   uint64_t wait_ns;       // limit of every bounded wait
   int withhold;           // test hook: the producer issues no copies
+  uint32_t layout = 0;    // packed row order (kLayoutRows / kLayoutPaired)
+  int silu = 0;           // paired gate_up: C[M][I] = silu(gate) * up
 };
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches, int* grid_out,
                            int64_t* tiles_out);

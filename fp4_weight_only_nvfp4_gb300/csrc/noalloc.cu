@@ -123,6 +123,7 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   D.stages = stages;
   D.wait_ns = 0;  // the default limit
   D.withhold = 0;
+  D.layout = (uint32_t)W->layout;
   int launches = 0;
   e = launch_decode(D, (cudaStream_t)s, &launches);
   if (e != cudaSuccess) return err(VT_ERR_CUDA, cudaGetErrorString(e));

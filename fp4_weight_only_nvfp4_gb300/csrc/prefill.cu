@@ -165,7 +165,12 @@ struct PrefillParams {
   int vec_store;     // C 16-byte aligned and ldc % 8 == 0
   uint64_t wait_ns;  // limit of every bounded wait
   int withhold;      // test hook: issue no copies (the waits then run out)
+  uint32_t layout;   // packed row order (kLayoutRows / kLayoutPaired)
+  int silu;          // paired gate_up: C[M][I] = silu(gate) * up
 };
+
+// SiLU(x) = x / (1 + e^-x) in fp32 (e^-x overflowing to infinity gives -0 for large -x).
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
 template <int FMT>
 __global__ void __launch_bounds__(kPfThreads, 1)
@@ -384,9 +389,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool live = m < p.M;
       const float rs = live ? p.rowscale[m] : 0.0f;
       __nv_bfloat16* crow = p.C + (live ? m : 0) * p.ldc;
-      for (int c = 0; c < kBN / 32; ++c) {
+      if (p.silu) {
+        // paired tiles: in each 128-column half, columns [0, 64) are gate rows 64r + j and
+        // [64, 128) the matching up rows; chunk c (32 columns) pairs with chunk c + 2
+        for (int c = 0; c < kBN / 32; ++c) {
+          if (c & 2) continue;
+          const int64_t i0 = (nt * 2 + (c >> 2)) * 64 + (c & 1) * 32;  // first output column
+          if (i0 >= p.seg_split) continue;  // warp-uniform
+          uint32_t vg[32], vu[32];
+          tmem_ld32(tmem + ab * kBN + c * 32 + ((uint32_t)(qd * 32) << 16), vg);
+          tmem_ld32(tmem + ab * kBN + (c + 2) * 32 + ((uint32_t)(qd * 32) << 16), vu);
+          if (!live) continue;
+          uint32_t o[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float ya = silu_f(__uint_as_float(vg[2 * e]) * rs * f0) *
+                             (__uint_as_float(vu[2 * e]) * rs * f1);
+            const float yb = silu_f(__uint_as_float(vg[2 * e + 1]) * rs * f0) *
+                             (__uint_as_float(vu[2 * e + 1]) * rs * f1);
+            __nv_bfloat162 h = __floats2bfloat162_rn(ya, yb);
+            o[e] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          if (p.vec_store && i0 + 32 <= p.seg_split) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + i0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int64_t i = i0 + 2 * e;
+              if (i + 1 < p.seg_split) *reinterpret_cast<uint32_t*>(crow + i) = o[e];
+              else if (i < p.seg_split) *reinterpret_cast<uint16_t*>(crow + i) = (uint16_t)(o[e] & 0xFFFFu);
+            }
+          }
+        }
+      }
+      for (int c = 0; c < (p.silu ? 0 : kBN / 32); ++c) {
         const int64_t n0 = nt * kBN + c * 32;
-        if (n0 >= p.N) break;  // warp-uniform
+        // warp-uniform; paired tiles map columns past N onto valid up rows, so they check
+        // each column instead
+        if (p.layout != kLayoutPaired && n0 >= p.N) break;
         uint32_t v[32];
         tmem_ld32(tmem + ab * kBN + c * 32 + ((uint32_t)(qd * 32) << 16), v);
         if (!live) continue;
@@ -400,7 +442,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           __nv_bfloat162 h = __floats2bfloat162_rn(ya, yb);
           o[i] = *reinterpret_cast<uint32_t*>(&h);
         }
-        if (p.vec_store && n0 + 32 <= p.N) {
+        if (p.layout == kLayoutPaired) {
+          // each column is mapped to its weight row (gate-over-up order), one at a time
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int64_t n = packed_to_row(p.layout, n0 + e, p.N, p.seg_split);
+            if (n >= 0) {
+              const float f = n < p.seg_split ? f0 : f1;
+              crow[n] = __float2bfloat16_rn(__uint_as_float(v[e]) * rs * f);
+            }
+          }
+        } else if (p.vec_store && n0 + 32 <= p.N) {
           uint4* dst = reinterpret_cast<uint4*>(crow + n0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
@@ -562,6 +614,8 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   pp.vec_store = ((uintptr_t)L.C % 16 == 0) && (L.ldc % 8 == 0);
   pp.wait_ns = L.wait_ns ? L.wait_ns : 2000000000ull;
   pp.withhold = L.withhold;
+  pp.layout = L.layout;
+  pp.silu = L.silu;
   int64_t grid = L.grid > 0 ? L.grid : 1;
   if (grid > pp.tiles_total) grid = pp.tiles_total;
   e = (L.fmt == FMT_NV) ? launch_main<FMT_NV>(tm, pp, (int)grid, s)

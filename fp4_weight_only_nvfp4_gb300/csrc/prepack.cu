@@ -12,6 +12,7 @@ struct SrcPair {
   const uint8_t* codes[2];
   const uint8_t* scales[2];
   int64_t split;  // rows [0, split) come from source 0, the rest from source 1
+  uint32_t layout;  // packed row order (kLayoutRows / kLayoutPaired)
 };
 
 __device__ __forceinline__ void src_row(const SrcPair& s, int64_t row, int& which,
@@ -21,9 +22,10 @@ __device__ __forceinline__ void src_row(const SrcPair& s, int64_t row, int& whic
 }
 
 __global__ void k_header(PackedHeader* h, int fmt, int64_t N, int64_t K, int64_t split,
-                         float f0, float f1) {
+                         float f0, float f1, uint32_t layout) {
   if (threadIdx.x == 0) {
     h->magic = kMagic;
+    h->layout = layout;
     h->fmt = static_cast<uint32_t>(fmt);
     h->N = N;
     h->K = K;
@@ -97,10 +99,11 @@ __global__ void __launch_bounds__(256) k_pack(SrcPair s, int fmt, int64_t N, int
     uint32_t w = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      int64_t row = rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0);
+      const int64_t row =
+          packed_to_row(s.layout, rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0), N, s.split);
       int64_t col = kt * 32 + 8 * t + 2 * q + (b >> 1);
       uint32_t v = 0;
-      if (row < N && col < kb) {
+      if (row >= 0 && col < kb) {
         int which;
         int64_t r;
         src_row(s, row, which, r);
@@ -122,9 +125,9 @@ __global__ void __launch_bounds__(256) k_pack(SrcPair s, int fmt, int64_t N, int
     uint32_t pair = 0;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      int64_t row = rt * kTileRows + j * 16 + g + half * 8;
+      const int64_t row = packed_to_row(s.layout, rt * kTileRows + j * 16 + g + half * 8, N, s.split);
       uint32_t v = 0;
-      if (row < N && grp < gpr) {
+      if (row >= 0 && grp < gpr) {
         int which;
         int64_t r;
         src_row(s, row, which, r);
@@ -152,8 +155,8 @@ __device__ __forceinline__ int mx_decode(uint8_t enc, int emax) {
 
 __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, int64_t N,
                                                 int64_t K, int64_t KT, int64_t split,
-                                                const PackedHeader* h, uint8_t* codes,
-                                                uint8_t* scales) {
+                                                uint32_t layout, const PackedHeader* h,
+                                                uint8_t* codes, uint8_t* scales) {
   const int64_t tile = blockIdx.x;
   const int64_t rt = tile / KT, kt = tile % KT;
   const uint8_t* in = tiles + tile * tile_bytes(fmt);
@@ -166,9 +169,10 @@ __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, i
   for (int q = 0; q < 4; ++q)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      int64_t row = rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0);
+      const int64_t row =
+          packed_to_row(layout, rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0), N, split);
       int64_t col = kt * 32 + 8 * t + 2 * q + (b >> 1);
-      if (row < N && col < kb) codes[row * kb + col] = (words[q] >> (8 * b)) & 0xFF;
+      if (row >= 0 && col < kb) codes[row * kb + col] = (words[q] >> (8 * b)) & 0xFF;
     }
   const bool nv = (fmt == FMT_NV);
   if (nv || t < 2) {
@@ -178,8 +182,8 @@ __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, i
     const uint32_t pair = *reinterpret_cast<const uint16_t*>(in + off);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      int64_t row = rt * kTileRows + j * 16 + g + half * 8;
-      if (row < N && grp < gpr) {
+      const int64_t row = packed_to_row(layout, rt * kTileRows + j * 16 + g + half * 8, N, split);
+      if (row >= 0 && grp < gpr) {
         const uint8_t b = (pair >> (8 * half)) & 0xFF;
         if (nv) {
           scales[row * gpr + grp] = b;
@@ -196,7 +200,8 @@ __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, i
 // f16x2, one f16 multiply (exact), then fp32 multiply by the segment factor.
 __global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, int64_t N,
                                                  int64_t K, int64_t KT, int64_t split,
-                                                 const PackedHeader* h, float* out) {
+                                                 uint32_t layout, const PackedHeader* h,
+                                                 float* out) {
   const int64_t tile = blockIdx.x;
   const int64_t rt = tile / KT, kt = tile % KT;
   const uint8_t* in = tiles + tile * tile_bytes(fmt);
@@ -215,9 +220,10 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, 
     for (int b = 0; b < 4; ++b) {
       uint32_t p = hmul2_u32(r[b], (b & 1) ? s_g8 : s_g);
       __half2 hp = *reinterpret_cast<__half2*>(&p);
-      int64_t row = rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0);
+      const int64_t row =
+          packed_to_row(layout, rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0), N, split);
       int64_t k0 = kt * kTileK + 16 * t + 4 * q + ((b >> 1) ? 2 : 0);
-      if (row < N && k0 < K) {
+      if (row >= 0 && k0 < K) {
         float f = h->factor[row < split ? 0 : 1];
         out[row * K + k0] = __low2float(hp) * f;
         out[row * K + k0 + 1] = __high2float(hp) * f;
@@ -229,11 +235,11 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, 
 // ------------------------------------------------------------------ host launchers
 cudaError_t launch_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
                            int64_t split, float f0, float f1, int fmt, int64_t N, int64_t K,
-                           int64_t RT, int64_t KT, void* dst, cudaStream_t s) {
+                           int64_t RT, int64_t KT, uint32_t layout, void* dst, cudaStream_t s) {
   PackedHeader* h = reinterpret_cast<PackedHeader*>(dst);
   uint8_t* tiles = reinterpret_cast<uint8_t*>(dst) + kHeaderBytes;
-  SrcPair sp{{codes[0], codes[1]}, {scales[0], scales[1]}, split};
-  k_header<<<1, 32, 0, s>>>(h, fmt, N, K, split, f0, f1);
+  SrcPair sp{{codes[0], codes[1]}, {scales[0], scales[1]}, split, layout};
+  k_header<<<1, 32, 0, s>>>(h, fmt, N, K, split, f0, f1, layout);
   if (fmt == FMT_MX) {
     int64_t total = N * (K / 32);
     int64_t nb = (total + 255) / 256;
@@ -246,21 +252,22 @@ cudaError_t launch_prepack(const uint8_t* const codes[2], const uint8_t* const s
 }
 
 cudaError_t launch_unpack(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
-                          int64_t KT, int64_t split, uint8_t* codes, uint8_t* scales,
-                          cudaStream_t s) {
+                          int64_t KT, int64_t split, uint32_t layout, uint8_t* codes,
+                          uint8_t* scales, cudaStream_t s) {
   const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
   const uint8_t* tiles = reinterpret_cast<const uint8_t*>(packed) + kHeaderBytes;
-  k_unpack<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(tiles, fmt, N, K, KT, split, h,
-                                                          codes, scales);
+  k_unpack<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(tiles, fmt, N, K, KT, split, layout,
+                                                          h, codes, scales);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const void* packed, int fmt, int64_t N, int64_t K, int64_t RT,
-                           int64_t KT, int64_t split, float* out, cudaStream_t s) {
+                           int64_t KT, int64_t split, uint32_t layout, float* out,
+                           cudaStream_t s) {
   const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
   const uint8_t* tiles = reinterpret_cast<const uint8_t*>(packed) + kHeaderBytes;
-  k_dequant<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(tiles, fmt, N, K, KT, split, h,
-                                                           out);
+  k_dequant<<<static_cast<unsigned>(RT * KT), 256, 0, s>>>(tiles, fmt, N, K, KT, split, layout,
+                                                           h, out);
   return cudaGetLastError();
 }
 

@@ -114,6 +114,20 @@ vt_status vt_fp4_prepack_gate_up(const uint8_t* gate_codes, const uint8_t* gate_
                                  int64_t I, int64_t K, void* packed_dst, size_t dst_bytes,
                                  vt_stream_t s, vt_fp4_handle* out);
 
+/* Fused gate_up paired for the SiLU-and-multiply epilogue: the same two weights as
+ * vt_fp4_prepack_gate_up, with each 128-row tile holding 64 gate rows and the same 64 up
+ * rows, so that vt_fp4_w4a16_gemm_silu_mul can form silu(gate) * up inside one tile.
+ * Source: "MXFP4 decode-graph + gate_up FUSION default-ON" (PR #54), "Step 2" (gate and up
+ * as one GEMM) and "Attribution" (the glue between the MLP GEMMs is a measured cost).
+ * Arguments and sizes as vt_fp4_prepack_gate_up.  The handle also serves
+ * vt_fp4_w4a16_gemm (which then writes C[M][2I], gate in columns [0, I)), vt_fp4_unpack
+ * and vt_fp4_dequant (both in gate-over-up row order). */
+vt_status vt_fp4_prepack_gate_up_paired(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                        float gate_global, const uint8_t* up_codes,
+                                        const uint8_t* up_scales, float up_global,
+                                        vt_fp4_format fmt, int64_t I, int64_t K, void* packed_dst,
+                                        size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out);
+
 /* Frees the host-side handle (never device memory). NULL is a no-op. */
 vt_status vt_fp4_destroy(vt_fp4_handle W);
 
@@ -147,6 +161,18 @@ vt_status vt_fp4_w4a16_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle
 vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
                                void* C, int64_t ldc, void* workspace, size_t ws_bytes,
                                vt_stream_t s, const vt_fp4_gemm_opts* opts);
+
+/* The input of the down projection from a paired gate_up weight (from
+ * vt_fp4_prepack_gate_up_paired): C[m][i] = bf16( silu(g) * u ), g and u the fp32 sums of
+ * gate row i and up row i times their globals, silu(x) = x / (1 + e^-x) in fp32 -- the
+ * gate_up GEMM and the SiLU-and-multiply step in one call, without writing the [M][2I]
+ * intermediate.  Any M >= 0 (the decode path for M <= 16, the tile path above).
+ *   C  (device) bf16 [M][ldc], ldc >= I, 4-byte aligned, ldc even.
+ * Other arguments as for vt_fp4_w4a16_gemm.  A weight not prepacked paired is rejected
+ * with VT_ERR_INVALID_ARG. */
+vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                     void* C, int64_t ldc, void* workspace, size_t ws_bytes,
+                                     vt_stream_t s);
 
 /* Greedy head: the decode GEMM (M <= 16) that keeps, per token m, only the index of the
  * largest output, instead of writing the M x N outputs.  Source: "re-verify 27B NVFP4 on
