@@ -73,7 +73,7 @@ class Workload:
     projs: list
     layers: int = 1
     note: str = ""
-    kind: str = "decode"   # "decode"/"greedy"/"mlp_silu": HBM GB/s; "prefill": TFLOP/s
+    kind: str = "decode"   # "decode"/"greedy"/"mlp_silu"/"moe": HBM GB/s; "prefill": TFLOP/s
     extra: dict = field(default_factory=dict)
 
     @property
@@ -119,6 +119,13 @@ WORKLOADS = {
          Proj("down", 12288, N=4096, wid=2, role=13)], kind="mlp_silu",
         note="MXFP4 dense MLP decode as a chain: gate_up (paired) with the SiLU-and-multiply "
              "epilogue writes act [M][12288], down reads it; M in {1,2,4,8}"),
+    "nvfp4_moe_128x1536x2048": Workload(
+        "nvfp4_moe_128x1536x2048", 7, NVFP4, [1, 2, 4, 8],
+        [Proj("experts", 2048, N=1536, wid=7)], kind="moe",
+        extra={"E": 128, "topk": 8},
+        note="NVFP4 mixture-of-experts decode: 128 experts of gate_up 2x768 x 2048, top-8 "
+             "routing (seeded, distinct experts per token), M in {1,2,4,8}; bytes = the "
+             "distinct experts a call streams + activations"),
     "nvfp4_lm_head_greedy_248320x2560": Workload(
         "nvfp4_lm_head_greedy_248320x2560", 3, NVFP4, [1, 2, 4, 8],
         [Proj("lm_head", 2560, N=248320, wid=3)], kind="greedy",
@@ -211,6 +218,23 @@ def _build_weights(w: Workload, copies: int, dev):
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
     sets = []
+    if w.kind == "moe":
+        E, p = w.extra["E"], w.projs[0]
+        for c in range(copies):
+            codes, scales, globs = [], [], []
+            for e in range(E):
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(p.tid(ROLE_W, c * 1024 + e) & 0x7FFFFFFFFFFF)
+                Wb = (torch.randn((p.N, p.K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+                c_, s_, g_ = vt.quantize(Wb, w.fmt)
+                codes.append(c_)
+                scales.append(s_)
+                globs.append(float(g_.item()) if w.fmt == NVFP4 else 1.0)
+            sets.append([[vt.PackedWeight.grouped(torch.stack(codes), torch.stack(scales), globs,
+                                                  w.fmt, E, p.N, p.K)]])
+            del codes, scales
+        torch.cuda.synchronize()
+        return sets
     for c in range(copies):
         layer_sets = []
         for layer in range(w.layers):
@@ -240,6 +264,8 @@ def _build_weights(w: Workload, copies: int, dev):
 
 def _copies_needed(w: Workload) -> int:
     per_copy = sum(_algo_bytes(w.fmt, p.N, p.K, 0) for p in w.projs) * w.layers
+    if w.kind == "moe":
+        per_copy *= w.extra["E"]
     need = 1
     # every M of a step uses its own copy when one copy does not exceed the L2 twice over
     if per_copy < 2 * L2_BYTES:
@@ -277,7 +303,11 @@ def run_gpu(args, rank: int, world: int):
     sets = _build_weights(w, copies, dev)
     calls = _calls(w, sets)
     Mmax = max(w.Ms)
-    wsz = max(Wt.workspace_bytes(Mmax) for layer_sets in sets for ws in layer_sets for Wt in ws)
+    moe = w.kind == "moe"
+    if moe:
+        wsz = sets[0][0][0].moe_workspace(Mmax, w.extra["topk"]).numel()
+    else:
+        wsz = max(Wt.workspace_bytes(Mmax) for layer_sets in sets for ws in layer_sets for Wt in ws)
     ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(12345 + rank)
@@ -287,7 +317,23 @@ def run_gpu(args, rank: int, world: int):
     C = {(M, p.N): torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
          for M in w.Ms for p in w.projs}
     stream = torch.cuda.Stream(device=dev)
-    step_bytes = sum(_work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
+    if moe:
+        # seeded routing per (copy, M): distinct experts per token; the algorithmic bytes of a
+        # call are the distinct experts it streams plus the activations
+        topk, E = w.extra["topk"], w.extra["E"]
+        rng = np.random.default_rng(1234)
+        route = {}
+        for c, layer, pi, M in calls:
+            ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(M)])
+            route[(c, M)] = torch.from_numpy(ids.astype(np.int32)).to(dev)
+        ebytes = _algo_bytes(w.fmt, w.projs[0].N, w.projs[0].K, 0)
+        moe_bytes = {k: len(np.unique(v.cpu().numpy())) * ebytes + 2 * k[1] * w.projs[0].K
+                     for k, v in route.items()}
+        Cm = {M: torch.empty((M * topk, w.projs[0].N), dtype=torch.bfloat16, device=dev)
+              for M in w.Ms}
+        step_bytes = sum(moe_bytes[(c, M)] for c, _, _, M in calls)
+    else:
+        step_bytes = sum(_work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
     n_calls = len(calls)
 
     greedy = w.kind == "greedy"
@@ -298,6 +344,10 @@ def run_gpu(args, rank: int, world: int):
 
     def one_call(c, layer, pi, M, unfused=False):
         p = w.projs[pi]
+        if moe:
+            vt.w4a16_gemm_moe(A[(M, p.K)], sets[c][layer][pi], route[(c, M)], out=Cm[M],
+                              workspace=ws, stream=stream)
+            return
         if greedy and not unfused:
             vt.w4a16_gemm_greedy(A[(M, p.K)], sets[c][layer][pi], workspace=ws, stream=stream)
             return
@@ -403,7 +453,7 @@ def run_gpu(args, rank: int, world: int):
     for i, (c, layer, pi, M) in enumerate(calls):
         p = w.projs[pi]
         key = (p.name, M)
-        b = _work(w, p.N, p.K, M)
+        b = moe_bytes[(c, M)] if moe else _work(w, p.N, p.K, M)
         a = agg.setdefault(key, [0.0, 0, 0])
         a[0] += durs[i]
         a[1] += 1
@@ -441,7 +491,8 @@ def run_gpu(args, rank: int, world: int):
     achieved = _rate(w, step_bytes, ms_step * 1e-3)
 
     # end to end: pinned host activations in, host logits out, every call
-    e2e = run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist)
+    e2e = (run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route)
+           if moe else run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist))
     ws_status = vt.workspace_status(ws, stream)
     return {
         "value": value, "ms_per_step": ms_step, "step_bytes": step_bytes, "clocks": clocks,
@@ -524,6 +575,51 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     ms_step = ms / args.steps
+    return {"value": round(_rate(w, step_bytes * world, ms_step * 1e-3), 2), "unit": w.unit,
+            "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
+    """The MoE step end to end: host activations and routing in, host expert outputs out."""
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    p, topk = w.projs[0], w.extra["topk"]
+    hA = {M: torch.randn((M, p.K)).to(torch.bfloat16).pin_memory() for M in w.Ms}
+    dA = {M: torch.empty((M, p.K), dtype=torch.bfloat16, device=dev) for M in w.Ms}
+    hR = {k: v.cpu().pin_memory() for k, v in route.items()}
+    dR = {k: torch.empty_like(v) for k, v in route.items()}
+    hC = {M: torch.empty((M * topk, p.N), dtype=torch.bfloat16).pin_memory() for M in w.Ms}
+    dC = {M: torch.empty((M * topk, p.N), dtype=torch.bfloat16, device=dev) for M in w.Ms}
+    h2d = sum(M * p.K * 2 + M * topk * 4 for _, _, _, M in calls)
+    d2h = sum(M * topk * p.N * 2 for _, _, _, M in calls)
+
+    def issue():
+        for c, layer, pi, M in calls:
+            dA[M].copy_(hA[M], non_blocking=True)
+            dR[(c, M)].copy_(hR[(c, M)], non_blocking=True)
+            vt.w4a16_gemm_moe(dA[M], sets[c][layer][pi], dR[(c, M)], out=dC[M], workspace=ws,
+                              stream=stream)
+            hC[M].copy_(dC[M], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            issue()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            issue()
+        for _ in range(3):
+            graph.replay()
+    stream.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(stream)
+    stream.synchronize()
+    ms_step = t0.elapsed_time(t1) / args.steps
     return {"value": round(_rate(w, step_bytes * world, ms_step * 1e-3), 2), "unit": w.unit,
             "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 

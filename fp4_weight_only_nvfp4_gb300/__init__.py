@@ -104,15 +104,44 @@ class PackedWeight:
         return torch.zeros(self.workspace_bytes(M_max), dtype=torch.uint8,
                            device=self.packed.device)
 
+    @classmethod
+    def grouped(cls, codes: torch.Tensor, scales: torch.Tensor, globals_: list, fmt: int,
+                E: int, N: int, K: int, stream=None) -> "PackedWeight":
+        """E experts of N x K: codes [E, N, K/2], scales [E, N, K/g], one global per expert
+        (vt_fp4_prepack_grouped)."""
+        if codes.shape != (E, N, K // 2) or scales.shape != (E, N, K // GROUP[fmt]):
+            raise ValueError("codes [E, N, K/2] and scales [E, N, K/g] expected")
+        out = ctypes.c_size_t(0)
+        check(lib().vt_fp4_prepack_grouped_bytes(fmt, E, N, K, ctypes.byref(out)),
+              "vt_fp4_prepack_grouped_bytes")
+        packed = torch.empty(out.value, dtype=torch.uint8, device=codes.device)
+        g = (ctypes.c_float * E)(*[float(x) for x in globals_])
+        h = ctypes.c_void_p(0)
+        check(lib().vt_fp4_prepack_grouped(_ptr(codes.contiguous()), _ptr(scales.contiguous()),
+                                           ctypes.cast(g, ctypes.c_void_p), fmt, E, N, K,
+                                           _ptr(packed), out.value, _stream(stream),
+                                           ctypes.byref(h)), "vt_fp4_prepack_grouped")
+        W = cls(h, packed, fmt, N, K)
+        W.E = E
+        return W
+
+    def moe_workspace(self, M_max: int, topk: int) -> torch.Tensor:
+        out = ctypes.c_size_t(0)
+        check(lib().vt_fp4_moe_workspace_bytes(self.handle, M_max, topk, ctypes.byref(out)),
+              "vt_fp4_moe_workspace_bytes")
+        return torch.zeros(out.value, dtype=torch.uint8, device=self.packed.device)
+
     def dequant(self, stream=None) -> torch.Tensor:
-        out = torch.empty((self.N, self.K), dtype=torch.float32, device=self.packed.device)
+        out = torch.empty((getattr(self, "E", 1) * self.N, self.K), dtype=torch.float32,
+                          device=self.packed.device)
         check(lib().vt_fp4_dequant(self.handle, _ptr(out), _stream(stream)), "vt_fp4_dequant")
         return out
 
     def unpack(self, stream=None):
         dev = self.packed.device
-        codes = torch.empty((self.N, self.K // 2), dtype=torch.uint8, device=dev)
-        scales = torch.empty((self.N, self.K // GROUP[self.fmt]), dtype=torch.uint8, device=dev)
+        rows = getattr(self, "E", 1) * self.N
+        codes = torch.empty((rows, self.K // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((rows, self.K // GROUP[self.fmt]), dtype=torch.uint8, device=dev)
         check(lib().vt_fp4_unpack(self.handle, _ptr(codes), _ptr(scales), _stream(stream)),
               "vt_fp4_unpack")
         return codes, scales
@@ -163,6 +192,28 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
                                      out.stride(0), _ptr(workspace), workspace.numel(),
                                      _stream(stream), ctypes.byref(o) if o else None),
           "vt_fp4_w4a16_gemm")
+    return out
+
+
+def w4a16_gemm_moe(A: torch.Tensor, W: PackedWeight, topk_ids: torch.Tensor,
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Mixture-of-experts decode GEMM: out[m * topk + j] = A[m] . W_e^T with
+    e = topk_ids[m, j] (see vt_fp4_w4a16_gemm_moe in include/vt_fp4.h)."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2 or topk_ids.shape[0] != A.shape[0]:
+        raise ValueError("topk_ids must be an int32 [M, topk] tensor")
+    M, topk = topk_ids.shape
+    topk_ids = topk_ids.contiguous()
+    if out is None:
+        out = torch.empty((M * topk, W.N), dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = W.moe_workspace(max(M, 1), topk)
+    check(lib().vt_fp4_w4a16_gemm_moe(_ptr(A), M, A.stride(0), W.handle, _ptr(topk_ids), topk,
+                                      _ptr(out), out.stride(0), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)),
+          "vt_fp4_w4a16_gemm_moe")
     return out
 
 

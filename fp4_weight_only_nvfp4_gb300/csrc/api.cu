@@ -82,6 +82,29 @@ WsLayout ws_layout(const vt_fp4_weight_s* W, int64_t M) {
   return L;
 }
 
+// Workspace of the grouped (mixture-of-experts) GEMM for `npairs` (token, slot) pairs.
+// Every offset is independent of npairs (so calls of any size can share one workspace
+// without one call's data landing on another's split-K counters): status word, split-K
+// counters per (problem, row tile) for the largest possible problem count, split-K
+// partials, the group table, the activation scales [problems][KT][16], and last the
+// gathered f16 activations [npairs][KT*64], whose size alone depends on npairs.
+struct MoeLayout {
+  size_t status, counters, partials, table, ascale, ap, total;
+};
+
+MoeLayout moe_layout(const vt_fp4_weight_s* W, int64_t npairs) {
+  MoeLayout L;
+  const int64_t pcap = W->E < 128 ? W->E : 128;  // problems: distinct experts of <= 128 pairs
+  L.status = 0;
+  L.counters = 256;
+  L.partials = up256(L.counters + (size_t)pcap * W->RT * 4);
+  L.table = up256(L.partials + (size_t)kMaxDecodeGrid * 2 * 16 * 128 * 4);
+  L.ascale = up256(L.table + (size_t)kGroupTableInts * 4);
+  L.ap = up256(L.ascale + (size_t)pcap * W->KT * 16 * 4);
+  L.total = up256(L.ap + (size_t)npairs * W->KT * kTileK * 2);
+  return L;
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -198,6 +221,51 @@ vt_status vt_fp4_prepack_gate_up_paired(const uint8_t* gate_codes, const uint8_t
   return do_prepack(c, sc, g, 2, fmt, I, K, packed_dst, dst_bytes, s, out, kLayoutPaired);
 }
 
+vt_status vt_fp4_prepack_grouped_bytes(vt_fp4_format fmt, int64_t E, int64_t N, int64_t K,
+                                       size_t* packed_bytes) {
+  if (!packed_bytes) return fail(VT_ERR_INVALID_ARG, "packed_bytes is NULL");
+  if (E <= 0 || E > 65536) return fail(VT_ERR_INVALID_ARG, "E must be in [1, 65536]");
+  vt_status st = check_shape(fmt, N, K);
+  if (st) return st;
+  *packed_bytes = (size_t)E * packed_size(fmt, N, K);
+  return VT_OK;
+}
+
+vt_status vt_fp4_prepack_grouped(const uint8_t* codes, const uint8_t* scales,
+                                 const float* globals, vt_fp4_format fmt, int64_t E, int64_t N,
+                                 int64_t K, void* packed_dst, size_t dst_bytes, vt_stream_t s,
+                                 vt_fp4_handle* out) {
+  if (!out) return fail(VT_ERR_INVALID_ARG, "out handle pointer is NULL");
+  *out = nullptr;
+  size_t need = 0;
+  if (vt_status st = vt_fp4_prepack_grouped_bytes(fmt, E, N, K, &need)) return st;
+  if (!codes || !scales || !globals || !packed_dst)
+    return fail(VT_ERR_INVALID_ARG, "codes, scales, globals and packed_dst must be set");
+  if (dst_bytes < need)
+    return fail(VT_ERR_INVALID_ARG, "packed_dst holds %zu bytes, %zu needed", dst_bytes, need);
+  const size_t per = packed_size(fmt, N, K);
+  const int64_t g = group_of(fmt);
+  vt_fp4_handle first = nullptr;
+  for (int64_t e = 0; e < E; ++e) {
+    const uint8_t* c = codes + e * N * (K / 2);
+    const uint8_t* sc = scales + e * N * (K / g);
+    vt_fp4_handle h = nullptr;
+    vt_status st = vt_fp4_prepack(c, sc, globals[e], fmt, N, K,
+                                  static_cast<uint8_t*>(packed_dst) + e * per, per, s, &h);
+    if (st) {
+      delete first;
+      return st;
+    }
+    if (e == 0) first = h;
+    else delete h;
+  }
+  first->E = E;
+  first->expert_bytes = (int64_t)per;
+  first->packed_bytes = need;
+  *out = first;
+  return VT_OK;
+}
+
 vt_status vt_fp4_destroy(vt_fp4_handle W) {
   delete W;
   return VT_OK;
@@ -236,6 +304,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
                     const vt_fp4_gemm_opts* opts, int32_t* g_idx, float* g_val,
                     bool silu = false) {
   if (vt_status st = check_handle(W)) return st;
+  if (W->E > 1) return fail(VT_ERR_INVALID_ARG, "a grouped weight serves vt_fp4_w4a16_gemm_moe");
   if (M < 0) return fail(VT_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
   if (M == 0) return VT_OK;
   if (!A || !workspace || !(C || g_idx))
@@ -364,6 +433,88 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
 
 extern "C" {
 
+vt_status vt_fp4_moe_workspace_bytes(vt_fp4_handle W, int64_t M_max, int64_t topk,
+                                     size_t* bytes) {
+  if (vt_status st = check_handle(W)) return st;
+  if (!bytes) return fail(VT_ERR_INVALID_ARG, "bytes is NULL");
+  if (M_max < 1 || M_max > 16 || topk < 1 || topk > 8)
+    return fail(VT_ERR_INVALID_ARG, "M_max must be in [1, 16] and topk in [1, 8]");
+  *bytes = moe_layout(W, M_max * topk).total;
+  return VT_OK;
+}
+
+vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                const int32_t* topk_ids, int64_t topk, void* C, int64_t ldc,
+                                void* workspace, size_t ws_bytes, vt_stream_t s) {
+  if (vt_status st = check_handle(W)) return st;
+  if (M < 0 || M > 16) return fail(VT_ERR_UNSUPPORTED, "the grouped GEMM serves 0 <= M <= 16");
+  if (topk < 1 || topk > 8) return fail(VT_ERR_INVALID_ARG, "topk must be in [1, 8]");
+  if (M == 0) return VT_OK;
+  if (!A || !C || !topk_ids || !workspace)
+    return fail(VT_ERR_INVALID_ARG, "A, topk_ids, C and workspace must be set");
+  if (W->layout != kLayoutRows || W->seg_split != W->N)
+    return fail(VT_ERR_INVALID_ARG, "a grouped weight holds plain experts");
+  if (lda < W->K || ldc < W->N)
+    return fail(VT_ERR_INVALID_ARG, "lda must be >= K and ldc >= N");
+  if (!aligned(A, 16) || lda % 8)
+    return fail(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda %% 8 == 0");
+  if (!aligned(C, 4) || ldc % 2) return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
+  if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  if (!aligned(topk_ids, 4)) return fail(VT_ERR_MISALIGNED, "topk_ids must be 4-byte aligned");
+  if (W->K > 110000) return fail(VT_ERR_UNSUPPORTED, "K > 110000 is not supported");
+  const int npairs = (int)(M * topk);
+  MoeLayout L = moe_layout(W, npairs);
+  if (ws_bytes < L.total)
+    return fail(VT_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, L.total);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  const int ks = 8;
+  int stages = 6;
+  while (stages > 2 && decode_smem_bytes(W->fmt, 16, ks, stages) > 226 * 1024) --stages;
+  const int64_t pmax = npairs < W->E ? npairs : W->E;
+  const int64_t items = pmax * W->RT * W->KT;  // an upper bound: the pre-pass finds P
+  int64_t grid = sm_count();
+  if (grid > cdiv(items, 2 * ks)) grid = cdiv(items, 2 * ks);
+  if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
+  if (grid < 1) grid = 1;
+  DecodeLaunch D;
+  D.packed = W->packed;
+  D.fmt = W->fmt;
+  D.N = W->N;
+  D.K = W->K;
+  D.RT = W->RT;
+  D.KT = W->KT;
+  D.seg_split = W->seg_split;
+  D.A = A;
+  D.lda = lda;
+  D.M = 16;
+  D.C = C;
+  D.ldc = ldc;
+  D.status = reinterpret_cast<int*>(ws + L.status);
+  D.counters = reinterpret_cast<int*>(ws + L.counters);
+  D.ascale = reinterpret_cast<float*>(ws + L.ascale);
+  D.Ap = ws + L.ap;
+  D.partials = reinterpret_cast<float*>(ws + L.partials);
+  D.grid = (int)grid;
+  D.ks = ks;
+  D.stages = stages;
+  D.wait_ns = 0;
+  D.withhold = 0;
+  D.gtab = reinterpret_cast<const int*>(ws + L.table);
+  D.expert_bytes = W->expert_bytes ? W->expert_bytes : (int64_t)W->packed_bytes;
+  int launches = 0;
+  cudaError_t e = launch_decode_grouped(D, topk_ids, npairs, (int)topk, (int)W->E,
+                                        (cudaStream_t)s, &launches);
+  if (e != cudaSuccess) return cuda_fail(e, "grouped decode launch");
+  W->info.path = 3;
+  W->info.grid = D.grid;
+  W->info.warps_per_cta = 17;
+  W->info.m_tile = 16;
+  W->info.items = items;
+  W->info.launches = launches;
+  W->info.calls += 1;
+  return VT_OK;
+}
+
 vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
                                int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
                                const vt_fp4_gemm_opts* opts) {
@@ -425,16 +576,24 @@ vt_status vt_fp4_stats(vt_fp4_handle W, vt_fp4_launch_info* info) {
 vt_status vt_fp4_dequant(vt_fp4_handle W, float* out, vt_stream_t s) {
   if (vt_status st = check_handle(W)) return st;
   if (!out) return fail(VT_ERR_INVALID_ARG, "out is NULL");
-  cudaError_t e = launch_dequant(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split,
-                                 (uint32_t)W->layout, out, (cudaStream_t)s);
+  cudaError_t e = cudaSuccess;
+  for (int64_t x = 0; x < W->E && e == cudaSuccess; ++x)  // grouped: experts one after another
+    e = launch_dequant(static_cast<const uint8_t*>(W->packed) + x * W->expert_bytes, W->fmt, W->N,
+                       W->K, W->RT, W->KT, W->seg_split, (uint32_t)W->layout,
+                       out + x * W->N * W->K, (cudaStream_t)s);
   return e == cudaSuccess ? VT_OK : cuda_fail(e, "dequant launch");
 }
 
 vt_status vt_fp4_unpack(vt_fp4_handle W, uint8_t* codes, uint8_t* scales, vt_stream_t s) {
   if (vt_status st = check_handle(W)) return st;
   if (!codes || !scales) return fail(VT_ERR_INVALID_ARG, "codes and scales must be set");
-  cudaError_t e = launch_unpack(W->packed, W->fmt, W->N, W->K, W->RT, W->KT, W->seg_split,
-                                (uint32_t)W->layout, codes, scales, (cudaStream_t)s);
+  cudaError_t e = cudaSuccess;
+  const int64_t g = group_of(W->fmt);
+  for (int64_t x = 0; x < W->E && e == cudaSuccess; ++x)  // grouped: experts one after another
+    e = launch_unpack(static_cast<const uint8_t*>(W->packed) + x * W->expert_bytes, W->fmt, W->N,
+                      W->K, W->RT, W->KT, W->seg_split, (uint32_t)W->layout,
+                      codes + x * W->N * (W->K / 2), scales + x * W->N * (W->K / g),
+                      (cudaStream_t)s);
   return e == cudaSuccess ? VT_OK : cuda_fail(e, "unpack launch");
 }
 

@@ -25,6 +25,16 @@ namespace vt {
 
 constexpr int kAScaleStride = 16;   // floats per k tile in the activation-scale array
 constexpr int kConsumerWarps = 16;
+// Group table of the mixture-of-experts mode (ints, in the workspace): the number of
+// problems P; per problem its expert, token count, first row in the gathered activations,
+// and the output row of each of its (up to 16) tokens.
+constexpr int kGtMaxProblems = 128;
+constexpr int kGtP = 0;
+constexpr int kGtExpert = 1;
+constexpr int kGtCount = kGtExpert + kGtMaxProblems;
+constexpr int kGtRowsum = kGtCount + kGtMaxProblems;
+constexpr int kGtPair = kGtRowsum + kGtMaxProblems;
+constexpr int kGtInts = kGtPair + kGtMaxProblems * 16;
 constexpr int kSlotPad = 36;        // floats per token row of a warp's reduction slot
 
 int decode_mt(int M) { return M <= 8 ? 8 : 16; }
@@ -115,6 +125,10 @@ struct DecodeParams {
   unsigned int* g_done;        // CTAs finished, zero between calls
   uint32_t layout;             // packed row order (kLayoutRows / kLayoutPaired)
   int silu;                    // paired gate_up: write silu(gate) * up, C is [M][I]
+  // grouped (mixture-of-experts) mode: problems = experts in use, from the pre-pass
+  const int* gtab;             // group table (see kGt*)
+  const uint8_t* gbase;        // expert e's packed weight at gbase + e * expert_bytes
+  int64_t expert_bytes, RT;    // bytes per expert; 128-row tiles per expert
 };
 
 // SiLU(x) = x / (1 + e^-x) in fp32 (e^-x overflowing to infinity gives -0 for large -x).
@@ -176,7 +190,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // k tiles of one 128-row tile (one TMA bulk copy of the weights, one of the matching
 // activation slices, one of their scales); consumer warp w owns the row-block pair w % 4
 // (32 rows) and the stage's k tiles w / 4, w / 4 + 4, ... .  The producer is one thread.
-template <int FMT, int MT, int KS>
+template <int FMT, int MT, int KS, bool GRP>
 __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const DecodeParams p) {
   constexpr int TB = tile_bytes(FMT);
   constexpr int NJ = MT / 8;           // n8 MMA column blocks
@@ -192,13 +206,17 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   // for this grid to finish before it touches anything this grid reads or writes.
   pdl_launch_dependents();
 
+  // grouped mode: the number of problems comes from the pre-pass, so every role waits for
+  // it first (the weights to stream depend on the routing)
+  if constexpr (GRP) pdl_wait();
   const int S = p.stages;
-  const int M = p.M;
+  const int M = GRP ? 16 : p.M;  // rows of the stage's activation area
   // stage: weights | activation slices (M rows of 128 B per k tile) | activation scales
   const int SCALES_OFF = WBYTES + KS * M * 128;
   const int STAGE = SCALES_OFF + KS * kAScaleStride * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int64_t G = gridDim.x, c = blockIdx.x, I = p.items, KT = p.KT;
+  const int64_t G = gridDim.x, c = blockIdx.x, KT = p.KT;
+  const int64_t I = GRP ? (int64_t)p.gtab[kGtP] * p.RT * KT : p.items;
   const int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
 
   float* slots = reinterpret_cast<float*>(smem + (size_t)S * STAGE);
@@ -225,6 +243,61 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   }
   fence_mbar_init();
   __syncthreads();
+
+  if constexpr (GRP) {
+    if (warp == CW) {
+      // --------------------------------------------------------- producer (grouped)
+      // virtual row tile rt = problem * RT + rt_l; the weights of expert e = expert[problem]
+      if (lane == 0 && !p.withhold) {
+        const uint64_t pol = l2_evict_first_policy();
+        const uint64_t pol_a = l2_evict_last_policy();
+        int64_t pos = i0, rt = i0 / KT;
+        int kt = kt_first, slot = 0, issued = 0;
+        uint32_t par = 0;
+        int prob = (int)(rt / p.RT);
+        int64_t rtl = rt - (int64_t)prob * p.RT;
+        int e = 0, cnt = 0, rsum = 0;
+        if (pos < i1) {
+          e = p.gtab[kGtExpert + prob];
+          cnt = p.gtab[kGtCount + prob];
+          rsum = p.gtab[kGtRowsum + prob];
+        }
+        while (pos < i1) {
+          if (issued >= S && !mbar_wait_bounded(empty_u + 8 * slot, par ^ 1u, p.wait_ns)) {
+            atomicExch(p.status, 5);
+            break;
+          }
+          const int n = stage_len(pos, kt);
+          const uint32_t dst = ring_u + slot * STAGE;
+          mbar_expect_tx(full_u + 8 * slot, (uint32_t)(n * (TB + cnt * 128 + kAScaleStride * 4)));
+          bulk_g2s(dst, p.gbase + e * p.expert_bytes + kHeaderBytes + (rtl * KT + kt) * TB,
+                   (uint32_t)(n * TB), full_u + 8 * slot, pol);
+          bulk_g2s(dst + WBYTES, p.Ap + ((int64_t)rsum * KT + (int64_t)kt * cnt) * 64,
+                   (uint32_t)(n * cnt * 128), full_u + 8 * slot, pol_a);
+          bulk_g2s(dst + SCALES_OFF, p.ascale + ((int64_t)prob * KT + kt) * kAScaleStride,
+                   (uint32_t)(n * kAScaleStride * 4), full_u + 8 * slot, pol_a);
+          ++issued;
+          pos += n;
+          kt += n;
+          if (kt == KTi) {
+            kt = 0;
+            if (++rtl == p.RT && pos < i1) {
+              rtl = 0;
+              ++prob;
+              e = p.gtab[kGtExpert + prob];
+              cnt = p.gtab[kGtCount + prob];
+              rsum = p.gtab[kGtRowsum + prob];
+            }
+          }
+          if (++slot == S) {
+            slot = 0;
+            par ^= 1u;
+          }
+        }
+      }
+      return;
+    }
+  }
 
   if (warp == CW) {
     // ------------------------------------------------------------- producer
@@ -285,9 +358,12 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   }
 
   // ---------------------------------------------------------------- consumers
-  pdl_wait();
+  if constexpr (!GRP) pdl_wait();
   const int jp = warp & 3, kq = warp >> 2;  // row blocks 2jp, 2jp+1; k tiles kq, kq+4
-  const float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
+  float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
+  // grouped mode: the current problem's token count, output rows and expert factor
+  int Mc = M, gprob = -1;
+  const int* grow = nullptr;
   const int soff = scale_offset(FMT, 2 * jp, g, t);
   float acc[2][NJ][4];
 #pragma unroll
@@ -305,6 +381,17 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   int64_t rt = rt_first;  // row tile of the current segment
   while (pos < i1) {
     const int n = stage_len(pos, kt);
+    if constexpr (GRP) {
+      const int pr = (int)(rt / p.RT);
+      if (pr != gprob) {
+        gprob = pr;
+        Mc = p.gtab[kGtCount + pr];
+        grow = p.gtab + kGtPair + pr * 16;
+        const PackedHeader* he = reinterpret_cast<const PackedHeader*>(
+            p.gbase + p.gtab[kGtExpert + pr] * p.expert_bytes);
+        f0 = f1 = he->factor[0];
+      }
+    }
     if (ok) ok = mbar_wait_bounded(full_u + 8 * slot, par, p.wait_ns);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
@@ -313,13 +400,13 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       for (int kh = kq; kh < KS; kh += 4) {
         if (kh < n) {
           const uint32_t tb = sbase + kh * TB;
-          const uint32_t ab = sbase + WBYTES + kh * M * 128;
+          const uint32_t ab = sbase + WBYTES + kh * Mc * 128;
           // activation fragments (B operand): token rows g (+8), physical k 16t .. 16t+15
           uint32_t bfr[NJ][4][2];
 #pragma unroll
           for (int u = 0; u < NJ; ++u) {
             const int m = g + 8 * u;
-            if (m < M) {
+            if (m < Mc) {
               const uint32_t rowa = ab + m * 128;
               const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (m & 7)) << 4));
               const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (m & 7)) << 4));
@@ -425,7 +512,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
         for (int r = 0; r < 4; ++r) acc[b][u][r] = 0.0f;
       }
     consumer_sync(CT);
-    const int nout = M * 128;
+    const int nout = Mc * 128;
     if (complete && p.silu) {
       // paired tile: rows j < 64 are gate rows, rows 64 + j the matching up rows
       for (int idx = threadIdx.x; idx < M * 64; idx += CT) {
@@ -447,15 +534,19 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
 #pragma unroll
         for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
         if (complete) {
-          // the weight row (and output column) this tile row holds, -1 for padding
-          const int64_t n = packed_to_row(p.layout, rt * kTileRows + row, p.N, p.seg_split);
+          // the weight row (and output column) this tile row holds, -1 for padding; grouped:
+          // the row within the expert, and the output row of the problem's token m
+          const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
+                                   : rt * kTileRows + row;
+          const int64_t n = packed_to_row(p.layout, prow, p.N, p.seg_split);
+          const int64_t crow = GRP ? (int64_t)grow[m] : (int64_t)m;
           if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
             unsigned long long key = 0;
             if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
             greedy_fold(key, s_gkey, m);
           } else if (n >= 0) {
             const float f = n < p.seg_split ? f0 : f1;
-            p.C[(int64_t)m * p.ldc + n] = __float2bfloat16_rn(sum * f);
+            p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
         } else {
           p.partials[(((size_t)c * 2 + sel) * MT + m) * 128 + row] = sum;
@@ -509,14 +600,17 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
         for (int idx = threadIdx.x; idx < (p.silu ? 0 : nout); idx += CT) {
           const int m = idx >> 7, row = idx & 127;
           const float sum = tile_sum(m, row);
-          const int64_t n = packed_to_row(p.layout, rt * kTileRows + row, p.N, p.seg_split);
+          const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
+                                   : rt * kTileRows + row;
+          const int64_t n = packed_to_row(p.layout, prow, p.N, p.seg_split);
+          const int64_t crow = GRP ? (int64_t)grow[m] : (int64_t)m;
           if (p.g_idx) {
             unsigned long long key = 0;
             if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
             greedy_fold(key, s_gkey, m);
           } else if (n >= 0) {
             const float f = n < p.seg_split ? f0 : f1;
-            p.C[(int64_t)m * p.ldc + n] = __float2bfloat16_rn(sum * f);
+            p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
         }
       }
@@ -558,11 +652,11 @@ static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
   return e;
 }
 
-template <int FMT, int MT, int KS>
+template <int FMT, int MT, int KS, bool GRP = false>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   static int done[64] = {0};
-  const size_t smem = decode_smem_bytes(FMT, L.M, KS, L.stages);
-  cudaError_t e = allow_smem(k_decode<FMT, MT, KS>, (int)smem, done);
+  const size_t smem = decode_smem_bytes(FMT, GRP ? 16 : L.M, KS, L.stages);
+  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP>, (int)smem, done);
   if (e != cudaSuccess) return e;
   DecodeParams p;
   p.tiles = reinterpret_cast<const uint8_t*>(L.packed) + kHeaderBytes;
@@ -588,6 +682,10 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.g_done = L.g_done;
   p.layout = L.layout;
   p.silu = L.silu;
+  p.gtab = L.gtab;
+  p.gbase = reinterpret_cast<const uint8_t*>(L.packed);
+  p.expert_bytes = L.expert_bytes;
+  p.RT = L.RT;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
@@ -599,7 +697,155 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS>, p);
+  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP>, p);
+}
+
+// ------------------------------------------------------------- grouped pre-pass
+// Mixture-of-experts decode: each (token m, slot j) pair of topk_ids[M][topk] names an
+// expert.  The pairs are grouped into problems, one per expert in use, in increasing
+// expert order, with each problem's tokens in increasing pair order (m * topk + j): the
+// grouping, and so every output bit, is the same in every run.  Block (b, y) converts the
+// activations of problem b's tokens for k tiles 8y .. 8y+7 exactly as k_prep_a does, into
+// A'[rowsum_b * KT + kt * count_b + s][64] (granules XOR-swizzled by s & 7) with scales
+// ascale[(b * KT + kt) * 16 + s]; block (0, 0) also writes the group table.  A pair whose
+// expert id is out of range sets status 6 and is left out (its output row is not written).
+__global__ void __launch_bounds__(kPrepThreads) k_group_prep(
+    const __nv_bfloat16* __restrict__ A, int64_t lda, int64_t K, int64_t KT,
+    const int32_t* __restrict__ topk_ids, int npairs, int topk, int E,
+    __half* __restrict__ Ap, float* __restrict__ ascale, int* __restrict__ gtab,
+    int* __restrict__ status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int s_e[kGtMaxProblems], s_prob[kGtMaxProblems], s_slot[kGtMaxProblems];
+  __shared__ int s_first[kGtMaxProblems], s_cnt[kGtMaxProblems], s_rsum[kGtMaxProblems];
+  __shared__ int s_pexp[kGtMaxProblems], s_P;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < npairs; i += kPrepThreads) {
+    int e = topk_ids[i];
+    if (e < 0 || e >= E) {
+      if (blockIdx.x == 0 && blockIdx.y == 0) atomicExch(status, 6);
+      e = -1;
+    }
+    s_e[i] = e;
+  }
+  __syncthreads();
+  for (int i = tid; i < npairs; i += kPrepThreads) {
+    const int e = s_e[i];
+    int first = 1, slot = 0;
+    for (int j = 0; j < i; ++j)
+      if (s_e[j] == e) {
+        first = 0;
+        ++slot;
+      }
+    s_first[i] = first && e >= 0;
+    s_slot[i] = slot;
+  }
+  __syncthreads();
+  for (int i = tid; i < npairs; i += kPrepThreads) {
+    const int e = s_e[i];
+    int pidx = 0;
+    for (int j = 0; j < npairs; ++j)
+      if (s_first[j] && s_e[j] < e) ++pidx;
+    s_prob[i] = e >= 0 ? pidx : -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int P = 0;
+    for (int j = 0; j < npairs; ++j) P += s_first[j];
+    for (int q = 0; q < P; ++q) s_cnt[q] = 0;
+    for (int j = 0; j < npairs; ++j)
+      if (s_prob[j] >= 0) {
+        ++s_cnt[s_prob[j]];
+        s_pexp[s_prob[j]] = s_e[j];
+      }
+    int r = 0;
+    for (int q = 0; q < P; ++q) {
+      s_rsum[q] = r;
+      r += s_cnt[q];
+    }
+    s_P = P;
+  }
+  __syncthreads();
+  const int P = s_P;
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int q = tid; q < P; q += kPrepThreads) {
+      gtab[kGtExpert + q] = s_pexp[q];
+      gtab[kGtCount + q] = s_cnt[q];
+      gtab[kGtRowsum + q] = s_rsum[q];
+    }
+    for (int i = tid; i < npairs; i += kPrepThreads)
+      if (s_prob[i] >= 0) gtab[kGtPair + s_prob[i] * 16 + s_slot[i]] = i;
+    if (tid == 0) gtab[kGtP] = P;
+  }
+  const int b = blockIdx.x;
+  if (b >= P) return;
+  const int cnt = s_cnt[b], rsum = s_rsum[b];
+  const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + (tid >> 3);
+  const int gi = tid & 7;
+  const int64_t k0 = kt * 64 + gi * 8;
+  for (int sx = 0; sx < cnt; ++sx) {
+    int pair = 0;
+    for (int j = 0; j < npairs; ++j)
+      if (s_prob[j] == b && s_slot[j] == sx) pair = j;
+    const int64_t m = pair / topk;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int mx = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      mx = max(mx, (int)(w[q] & 0x7FFFu));
+      mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (kt >= KT) continue;
+    int pe = 0;
+    if (mx > 0 && mx <= 0x7F80) {
+      pe = ((mx >> 7) - 127) - 14;
+      pe = pe < -120 ? -120 : (pe > 113 ? 113 : pe);
+    }
+    const float down = ldexpf(1.0f, -pe);
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(w[q] << 16) * down;
+      const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
+      __half2 h = __floats2half2_rn(lo, hi);
+      o[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(
+        Ap + ((rsum * KT + kt * cnt + sx) * 64 + ((gi ^ (sx & 7)) * 8)));
+    *dst = make_uint4(o[0], o[1], o[2], o[3]);
+    if (gi == 0) ascale[((int64_t)b * KT + kt) * kAScaleStride + sx] = ldexpf(1.0f, pe);
+  }
+}
+
+cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids, int npairs,
+                                  int topk, int E, cudaStream_t s, int* launches) {
+  cudaError_t e = cudaSuccess;
+  {
+    const int pmax = npairs < E ? npairs : E;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(pmax > 0 ? pmax : 1),
+                       (unsigned)((L.KT + kPrepTiles - 1) / kPrepTiles));
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_group_prep, reinterpret_cast<const __nv_bfloat16*>(L.A),
+                           L.lda, L.K, L.KT, topk_ids, npairs, topk, E,
+                           reinterpret_cast<__half*>(L.Ap), L.ascale, const_cast<int*>(L.gtab),
+                           L.status);
+    if (e != cudaSuccess) return e;
+  }
+  if (L.ks == 4) e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 16, 4, true>(L, s) : launch_t<FMT_MX, 16, 4, true>(L, s);
+  else e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 16, 8, true>(L, s) : launch_t<FMT_MX, 16, 8, true>(L, s);
+  if (launches) *launches = 2;
+  return e;
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) {

@@ -10,6 +10,8 @@ struct vt_fp4_weight_s {
   int64_t N, K, RT, KT;
   int64_t seg_split;
   int layout;  // kLayoutRows or kLayoutPaired
+  int64_t E = 1;             // experts (grouped weight); 1 otherwise
+  int64_t expert_bytes = 0;  // grouped: bytes of one expert's packed weight
   const void* packed;
   size_t packed_bytes;
   vt_fp4_launch_info info;

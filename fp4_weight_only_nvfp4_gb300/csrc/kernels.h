@@ -43,9 +43,17 @@ struct DecodeLaunch {
   unsigned int* g_done = nullptr;
   uint32_t layout = 0;   // packed row order (kLayoutRows / kLayoutPaired)
   int silu = 0;          // paired gate_up: C[M][I] = silu(gate) * up
+  // grouped (mixture-of-experts) mode: packed = expert 0's packed weight
+  const int* gtab = nullptr;  // group table in the workspace
+  int64_t expert_bytes = 0;   // bytes per expert's packed weight
 };
 int decode_mt(int M);  // 8 or 16
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
+// Grouped decode: a pre-pass groups the (token, slot) pairs of topk_ids [M][topk] by
+// expert and converts their activations, then the decode kernel runs every problem.
+cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids, int npairs,
+                                  int topk, int E, cudaStream_t s, int* launches);
+constexpr int kGroupTableInts = 1 + 3 * 128 + 128 * 16;  // see the decode kernel
 size_t decode_smem_bytes(int fmt, int M, int ks, int stages);
 
 // Prefill tile GEMM (tensor cores), any M.

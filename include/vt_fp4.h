@@ -174,6 +174,41 @@ vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_f
                                      void* C, int64_t ldc, void* workspace, size_t ws_bytes,
                                      vt_stream_t s);
 
+/* Mixture-of-experts (grouped) weights: E experts of the same N x K, prepacked one after
+ * another as E independent packed weights (each with its own global scale, or MXFP4 scale
+ * window).  Source: "keep the ModelOpt NVFP4 lm_head packed" (PR #263), "Why this row
+ * matters" (the MoE shared experts are FP4 linear layers too) and "dense projections take
+ * vLLM's own dense marlin" (the multi-expert route of the same W4A16 GEMM).
+ *   codes   (device) u8 [E][N][K/2];  scales (device) u8 [E][N][K/g];
+ *   globals (host)   fp32 [E]: NVFP4 multipliers (> 0), MXFP4 1.0f.
+ * vt_fp4_prepack_grouped_bytes gives the buffer size (E x vt_fp4_prepack_bytes).  unpack
+ * and dequant write [E][N][...] in expert order; the plain GEMM entry points reject a
+ * grouped handle. */
+vt_status vt_fp4_prepack_grouped_bytes(vt_fp4_format fmt, int64_t E, int64_t N, int64_t K,
+                                       size_t* packed_bytes);
+vt_status vt_fp4_prepack_grouped(const uint8_t* codes, const uint8_t* scales,
+                                 const float* globals, vt_fp4_format fmt, int64_t E, int64_t N,
+                                 int64_t K, void* packed_dst, size_t dst_bytes, vt_stream_t s,
+                                 vt_fp4_handle* out);
+
+/* Workspace bytes of vt_fp4_w4a16_gemm_moe for up to M_max (<= 16) tokens of topk (<= 8)
+ * experts each; zeroed once by the caller, reusable afterwards. */
+vt_status vt_fp4_moe_workspace_bytes(vt_fp4_handle W, int64_t M_max, int64_t topk,
+                                     size_t* bytes);
+
+/* Mixture-of-experts decode GEMM (M <= 16): for every token m and slot j,
+ *   C[m * topk + j][n] = sum_k A[m][k] * W_e[n][k],  e = topk_ids[m * topk + j],
+ * in one call.  A pre-pass on the stream groups the (m, j) pairs by expert (each expert in
+ * use is streamed once, however many tokens chose it), in increasing expert order with
+ * pairs in increasing order, so results do not depend on the routing's order; then one
+ * decode kernel runs every expert's problem.
+ *   topk_ids (device) int32 [M][topk], 1 <= topk <= 8; C (device) bf16 [M*topk][ldc].
+ * A pair whose expert id is outside [0, E) is skipped (its C row is not written) and the
+ * workspace status word reads 6. */
+vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                                const int32_t* topk_ids, int64_t topk, void* C, int64_t ldc,
+                                void* workspace, size_t ws_bytes, vt_stream_t s);
+
 /* Greedy head: the decode GEMM (M <= 16) that keeps, per token m, only the index of the
  * largest output, instead of writing the M x N outputs.  Source: "re-verify 27B NVFP4 on
  * the nvidia ModelOpt checkpoint" (PR #178), "Correctness -- resolved, not fixed": greedy
