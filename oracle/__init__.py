@@ -71,6 +71,12 @@ def _load():
         lib.orc_greedy.restype = ctypes.c_int
         lib.orc_silu_mul.argtypes = [_P, _I64, _I64, _P]
         lib.orc_silu_mul.restype = ctypes.c_int
+        lib.orc_quantize_act.argtypes = [ctypes.c_int, _P, _I64, _I64, ctypes.c_float, _P, _P,
+                                         _P, ctypes.c_int]
+        lib.orc_quantize_act.restype = ctypes.c_int
+        lib.orc_gemm_w4a4.argtypes = [ctypes.c_int, _P, _I64, _I64, ctypes.c_float, _P, _P,
+                                      ctypes.c_float, _I64, _P, _I64, _P, _P, _P, ctypes.c_int]
+        lib.orc_gemm_w4a4.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -180,6 +186,45 @@ def gemm(fmt: int, A, codes, scales, G: float, N: int, cols=None, want_f64: bool
                           y64.ctypes.data if want_f64 else None, ybf.ctypes.data, threads())
     if rc:
         raise ValueError("orc_gemm rejected the input")
+    return (y, ybf, y64) if want_f64 else (y, ybf)
+
+
+def quantize_act(fmt: int, A, alpha: float = 1.0):
+    """W4A4 activation quantiser (decisions in fp32).  A: bf16 bits [M, K] ->
+    (codes u8 [M, K/2], scales u8 [M, K/g], dequantised activations fp32 [M, K])."""
+    A, ap = _c(A, np.uint16)
+    M, K = A.shape
+    g = 16 if fmt == NVFP4 else 32
+    codes = np.empty((M, K // 2), np.uint8)
+    scales = np.empty((M, K // g), np.uint8)
+    aq = np.empty((M, K), np.float32)
+    if _load().orc_quantize_act(fmt, ap, M, K, alpha, codes.ctypes.data, scales.ctypes.data,
+                                aq.ctypes.data, threads()):
+        raise ValueError("orc_quantize_act rejected the input")
+    return codes, scales, aq
+
+
+def gemm_w4a4(fmt: int, A, alpha: float, codes, scales, G: float, N: int, cols=None,
+              want_f64: bool = False):
+    """The W4A4 layer: the activations A (bf16 bits [M, K]) quantised by quantize_act with
+    the activation global ``alpha``, then the same fp32 GEMM as ``gemm``."""
+    A, ap = _c(A, np.uint16)
+    codes, cp = _c(codes, np.uint8)
+    scales, sp = _c(scales, np.uint8)
+    M, K = A.shape
+    if cols is None:
+        ncols, colp, keep = N, None, None
+    else:
+        keep = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+        ncols, colp = keep.size, keep.ctypes.data
+    y = np.empty((M, ncols), np.float32)
+    ybf = np.empty((M, ncols), np.uint16)
+    y64 = np.empty((M, ncols), np.float64) if want_f64 else None
+    rc = _load().orc_gemm_w4a4(fmt, ap, M, K, alpha, cp, sp, G, N, colp, ncols,
+                               y.ctypes.data, y64.ctypes.data if want_f64 else None,
+                               ybf.ctypes.data, threads())
+    if rc:
+        raise ValueError("orc_gemm_w4a4 rejected the input")
     return (y, ybf, y64) if want_f64 else (y, ybf)
 
 

@@ -2,7 +2,9 @@
  * ORACLE -- test infrastructure only.
  *
  * A plain, slow, obviously correct CPU implementation of the FP4 weight-only
- * (W4A16) linear layer: NVFP4 and MXFP4 weights against bf16 activations.
+ * (W4A16) linear layer: NVFP4 and MXFP4 weights against bf16 activations; and of
+ * its W4A4 arm, where the activations are quantised to the same block format
+ * (orc_quantize_act, orc_gemm_w4a4 at the end of the file).
  * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
  * load this library; the product path never does.  It shares no code with the
  * CUDA path.
@@ -36,8 +38,11 @@
  *    MXFP4 e = smallest integer with 2^e >= amax_g / 6 (clamped to
  *    [-127, 127]), codes = E2M1_RNE_sat(w / 2^e); quotients in fp64; ties to
  *    even; a magnitude that rounds to 0 gives code 0 (+0); a group whose
- *    scale decodes to 0 gets all-zero codes; an all-zero tensor gets G = 1.
+ *    scale decodes to 0 gets all-zero codes; an all-zero tensor gets G = 1;
+ *  - W4A4 activation quantiser: the same group rules with the activation global
+ *    alpha in place of G, decisions in fp32 (see orc_quantize_act).
  */
+#include <float.h>
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -361,22 +366,37 @@ static void gemm_cols(void* p, int64_t b, int64_t e) {
   free(w);
 }
 
+int orc_gemm_f32a(int fmt, const float* Af, int64_t M, int64_t K, const uint8_t* codes,
+                  const uint8_t* scales, float G, int64_t N, const int64_t* cols, int64_t ncols,
+                  float* y, double* y64, uint16_t* ybf, int threads);
+
 /* y[m][j] = sum_k fp32(A[m][k]) * w[cols[j]][k] (fp32, increasing k); A is bf16
  * bits [M][K] row-major.  cols == NULL computes all N columns.  y64 (optional)
  * receives the same sum accumulated in fp64; ybf (optional) the bf16 output. */
 int orc_gemm(int fmt, const uint16_t* A, int64_t M, int64_t K, const uint8_t* codes,
              const uint8_t* scales, float G, int64_t N, const int64_t* cols, int64_t ncols,
              float* y, double* y64, uint16_t* ybf, int threads) {
+  if (M < 0 || K <= 0) return -1;
+  float* Af = (float*)malloc((size_t)(M * K + 1) * sizeof(float));
+  if (!Af) return -1;
+  for (int64_t i = 0; i < M * K; ++i) Af[i] = (float)bf16_value(A[i]);
+  const int rc = orc_gemm_f32a(fmt, Af, M, K, codes, scales, G, N, cols, ncols, y, y64, ybf,
+                               threads);
+  free(Af);
+  return rc;
+}
+
+/* The same GEMM with the activations already in fp32 ([M][K], row-major): the W4A4 layer,
+ * whose activations are the dequantised FP4 values fl32(fl32(c s) G_a) (or c 2^(e-127)). */
+int orc_gemm_f32a(int fmt, const float* Af, int64_t M, int64_t K, const uint8_t* codes,
+                  const uint8_t* scales, float G, int64_t N, const int64_t* cols, int64_t ncols,
+                  float* y, double* y64, uint16_t* ybf, int threads) {
   if (M < 0 || N <= 0 || K <= 0 || K % (fmt == ORC_NVFP4 ? 16 : 32)) return -1;
   if (!cols) ncols = N;
   for (int64_t j = 0; cols && j < ncols; ++j)
     if (cols[j] < 0 || cols[j] >= N) return -1;
-  float* Af = (float*)malloc((size_t)(M * K + 1) * sizeof(float));
-  if (!Af) return -1;
-  for (int64_t i = 0; i < M * K; ++i) Af[i] = (float)bf16_value(A[i]);
   gctx_t g = {fmt, Af, M, K, N, codes, scales, G, cols, ncols, y, y64, ybf};
   parallel_for(ncols, threads, gemm_cols, &g);
-  free(Af);
   return 0;
 }
 
@@ -440,4 +460,103 @@ int orc_silu_mul(const float* y, int64_t M, int64_t I, uint16_t* out) {
       out[m * I + i] = f64_to_bf16(s * u);
     }
   return 0;
+}
+
+/* ------------------------------------------------------ W4A4 activations */
+/* The W4A4 arm quantises the activations too, with the same block formats as the weights:
+ * NVFP4 with the per-tensor activation global alpha (the checkpoint's "input_scale", which
+ * sets the GEMM's alpha and makes the layer true W4A4), MXFP4 with no global.  "re-verify 27B
+ * NVFP4 on the nvidia ModelOpt checkpoint" (PR #178), section "W4A16 is the default for
+ * ModelOpt"; "native MXFP4 keep-quant + Qwen e2e" (PR #38), commit "W0" (input_activations
+ * set = true W4A4).  The pages fix no precision for this quantiser; here every rounding
+ * decision is taken in fp32 (IEEE, round to nearest even), the precision of the GPU kernels:
+ *   NVFP4: s = E4M3_RNE_sat(fl32(amax_g / fl32(6 alpha))), d = fl32(val(s) alpha),
+ *          c = E2M1_RNE_sat(fl32(x / d))  (c = 0 for the whole group when s = 0);
+ *          dequantised a = fl32(fl32(val(c) val(s)) alpha).
+ *   MXFP4: e = min{e : 6 2^e >= amax_g} clamped to [-127, 127] (exact),
+ *          c = E2M1_RNE_sat(fl32(x fl32(2^-e))); dequantised a = fl32(val(c) 2^e).
+ * A: bf16 bits [M][K]; codes [M][K/2] (low nibble first), scales [M][K/g]; Aq (optional)
+ * [M][K] fp32 dequantised activations.  Returns -1 for bad sizes, a non-finite input, or
+ * (NVFP4) an alpha that is not a positive normal float; MXFP4 requires alpha == 1. */
+typedef struct {
+  const uint16_t* A;
+  int64_t K;
+  int fmt;
+  float alpha;
+  uint8_t* codes;
+  uint8_t* scales;
+  float* Aq;
+} aqctx_t;
+
+static void act_quant_rows(void* p, int64_t b, int64_t e) {
+  aqctx_t* q = (aqctx_t*)p;
+  const int64_t K = q->K;
+  const int g = (q->fmt == ORC_NVFP4) ? 16 : 32;
+  const float alpha6 = 6.0f * q->alpha;
+  for (int64_t m = b; m < e; ++m) {
+    for (int64_t grp = 0; grp < K / g; ++grp) {
+      const uint16_t* x = q->A + m * K + grp * g;
+      float amax = 0.0f;
+      for (int i = 0; i < g; ++i) amax = fmaxf(amax, fabsf((float)bf16_value(x[i])));
+      float d, step;
+      if (q->fmt == ORC_NVFP4) {
+        const float qs = amax / alpha6;
+        const unsigned sb = orc_e4m3_from_real((double)qs);
+        q->scales[m * (K / g) + grp] = (uint8_t)sb;
+        step = (float)orc_e4m3_value(sb);
+        d = step * q->alpha;
+      } else {
+        const int ex = orc_mx_exponent((double)amax);
+        q->scales[m * (K / g) + grp] = (uint8_t)(ex + 127);
+        step = ldexpf(1.0f, ex);
+        d = ldexpf(1.0f, -ex); /* multiplier for MXFP4 */
+      }
+      for (int i = 0; i < g; ++i) {
+        const float xv = (float)bf16_value(x[i]);
+        unsigned c;
+        if (q->fmt == ORC_NVFP4) c = (step == 0.0f) ? 0u : orc_e2m1_from_real((double)(xv / d));
+        else c = orc_e2m1_from_real((double)(xv * d));
+        put_code(q->codes, K, m, grp * g + i, c);
+        if (q->Aq) {
+          const float cv = (float)orc_e2m1_value(c);
+          q->Aq[m * K + grp * g + i] =
+              (q->fmt == ORC_NVFP4) ? (cv * step) * q->alpha : cv * step;
+        }
+      }
+    }
+  }
+}
+
+int orc_quantize_act(int fmt, const uint16_t* A, int64_t M, int64_t K, float alpha,
+                     uint8_t* codes, uint8_t* scales, float* Aq, int threads) {
+  if (M <= 0 || K <= 0 || K % (fmt == ORC_NVFP4 ? 16 : 32)) return -1;
+  if (fmt == ORC_NVFP4 ? !(isfinite(alpha) && alpha >= FLT_MIN) : alpha != 1.0f) return -1;
+  for (int64_t i = 0; i < M * K; ++i)
+    if (!isfinite(bf16_value(A[i]))) return -1;
+  aqctx_t q = {A, K, fmt, alpha, codes, scales, Aq};
+  memset(codes, 0, (size_t)(M * (K / 2)));
+  parallel_for(M, threads, act_quant_rows, &q);
+  return 0;
+}
+
+/* The W4A4 layer: y[m][j] = sum_k a[m][k] w[cols[j]][k] in fp32 (increasing k) with a the
+ * dequantised activations of orc_quantize_act and w the dequantised weights, the same
+ * accumulation as orc_gemm; y64 and ybf as there. */
+int orc_gemm_w4a4(int fmt, const uint16_t* A, int64_t M, int64_t K, float alpha,
+                  const uint8_t* codes, const uint8_t* scales, float G, int64_t N,
+                  const int64_t* cols, int64_t ncols, float* y, double* y64, uint16_t* ybf,
+                  int threads) {
+  if (M <= 0 || K <= 0) return -1;
+  const int g = (fmt == ORC_NVFP4) ? 16 : 32;
+  if (K % g) return -1;
+  uint8_t* ac = (uint8_t*)malloc((size_t)(M * (K / 2)));
+  uint8_t* as = (uint8_t*)malloc((size_t)(M * (K / g)));
+  float* Aq = (float*)malloc((size_t)(M * K) * sizeof(float));
+  int rc = -1;
+  if (ac && as && Aq && orc_quantize_act(fmt, A, M, K, alpha, ac, as, Aq, threads) == 0)
+    rc = orc_gemm_f32a(fmt, Aq, M, K, codes, scales, G, N, cols, ncols, y, y64, ybf, threads);
+  free(ac);
+  free(as);
+  free(Aq);
+  return rc;
 }
