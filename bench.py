@@ -144,6 +144,20 @@ WORKLOADS = {
         [Proj("gate_up", 5120, I=17408, wid=5, role=ROLE_GATE)], kind="prefill",
         note="NVFP4 prefill-shaped GEMM on the tensor-core tile path: fused gate_up "
              "N=2x17408 K=5120, M in {512,2048,4096}; TFLOP/s = 2*M*N*K / time"),
+    "nvfp4_w4a4_prefill_gate_up_34816x5120": Workload(
+        "nvfp4_w4a4_prefill_gate_up_34816x5120", 5, NVFP4, [512, 2048, 4096],
+        [Proj("gate_up", 5120, I=17408, wid=5, role=ROLE_GATE)], kind="prefill",
+        extra={"w4a4": 0.0078125},
+        note="the W4A4 arm of the NVFP4 prefill GEMM: activations quantised to NVFP4 with "
+             "the activation global 0.0078125, then the tile path; fused gate_up N=2x17408 "
+             "K=5120, M in {512,2048,4096}; TFLOP/s = 2*M*N*K / time"),
+    "mxfp4_w4a4_mlp_12288x4096": Workload(
+        "mxfp4_w4a4_mlp_12288x4096", 2, MXFP4, [1, 2, 4, 8],
+        [Proj("gate_up", 4096, I=12288, wid=2, role=ROLE_GATE),
+         Proj("down", 12288, N=4096, wid=2, role=13)],
+        extra={"w4a4": 1.0},
+        note="the W4A4 arm of the MXFP4 dense MLP decode (activations quantised to MXFP4): "
+             "fused gate_up N=2x12288 K=4096, down N=4096 K=12288, M in {1,2,4,8}"),
 }
 DEFAULT_WORKLOAD = "mxfp4_mlp_12288x4096"
 
@@ -338,6 +352,7 @@ def run_gpu(args, rank: int, world: int):
 
     greedy = w.kind == "greedy"
     silu = w.kind == "mlp_silu"
+    a4 = w.extra.get("w4a4")  # the W4A4 arm: the activation global
     # the MLP chain: gate_up writes act [M][I], down reads it
     I_mlp = max((p.I for p in w.projs if p.fused), default=0)
     act = {M: torch.zeros((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms} if silu else {}
@@ -362,6 +377,10 @@ def run_gpu(args, rank: int, world: int):
             else:
                 vt.w4a16_gemm(act[M], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
                               stream=stream)
+            return
+        if a4 is not None:
+            vt.w4a4_gemm(A[(M, p.K)], sets[c][layer][pi], a4, out=C[(M, p.N)], workspace=ws,
+                         stream=stream)
             return
         vt.w4a16_gemm(A[(M, p.K)], sets[c][layer][pi], out=C[(M, p.N)], workspace=ws,
                       stream=stream)
@@ -528,6 +547,7 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
             dC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
     greedy = w.kind == "greedy"
     silu = w.kind == "mlp_silu"
+    a4 = w.extra.get("w4a4")
     hT = {M: torch.empty(M, dtype=torch.int32).pin_memory() for M in w.Ms}
     if silu:  # the MLP chain: host input of gate_up in, host output of down out
         I_mlp = max(p.I for p in w.projs if p.fused)
@@ -557,8 +577,12 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
                                               stream=stream, want_value=False)
                 hT[M].copy_(tok, non_blocking=True)
                 continue
-            vt.w4a16_gemm(dA[(M, p.K)], sets[c][layer][pi], out=dC[(M, p.N)], workspace=ws,
-                          stream=stream)
+            if a4 is not None:
+                vt.w4a4_gemm(dA[(M, p.K)], sets[c][layer][pi], a4, out=dC[(M, p.N)],
+                             workspace=ws, stream=stream)
+            else:
+                vt.w4a16_gemm(dA[(M, p.K)], sets[c][layer][pi], out=dC[(M, p.N)],
+                              workspace=ws, stream=stream)
             hC[(M, p.N)].copy_(dC[(M, p.N)], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -673,8 +697,12 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0):
             inputs.append((p, M, n, Ab, c, s, G))
         t = time.perf_counter()
         nbytes = 0
+        a4 = w.extra.get("w4a4")
         for p, M, n, Ab, c, s, G in inputs:
-            oracle.gemm(w.fmt, Ab, c, s, G, n)
+            if a4 is not None:
+                oracle.gemm_w4a4(w.fmt, Ab, a4, c, s, G, n)
+            else:
+                oracle.gemm(w.fmt, Ab, c, s, G, n)
             nbytes += _work(w, n, p.K, M)
         return nbytes, time.perf_counter() - t
 

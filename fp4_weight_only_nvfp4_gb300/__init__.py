@@ -172,6 +172,14 @@ def _check_src(codes, scales, N, K, fmt):
         raise ValueError("codes/scales sizes do not match N and K")
 
 
+def _opts(opts: dict | None):
+    if not opts:
+        return None
+    return GemmOpts(int(opts.get("grid", 0)), int(opts.get("warps", 0)),
+                    int(opts.get("stages", 0)), int(opts.get("force_path", 0)),
+                    int(opts.get("wait_limit_us", 0)), int(opts.get("withhold_weights", 0)))
+
+
 def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, stream=None,
                opts: dict | None = None) -> torch.Tensor:
@@ -183,16 +191,46 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
     if workspace is None:
         workspace = W.new_workspace(M)
-    o = None
-    if opts:
-        o = GemmOpts(int(opts.get("grid", 0)), int(opts.get("warps", 0)),
-                     int(opts.get("stages", 0)), int(opts.get("force_path", 0)),
-                     int(opts.get("wait_limit_us", 0)), int(opts.get("withhold_weights", 0)))
+    o = _opts(opts)
     check(lib().vt_fp4_w4a16_gemm_ex(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
                                      out.stride(0), _ptr(workspace), workspace.numel(),
                                      _stream(stream), ctypes.byref(o) if o else None),
           "vt_fp4_w4a16_gemm")
     return out
+
+
+def w4a4_gemm(A: torch.Tensor, W: PackedWeight, input_scale: float = 1.0,
+              out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              stream=None, opts: dict | None = None) -> torch.Tensor:
+    """The W4A4 arm: out[M, N] (bf16) = Q(A) . W^T with the activations quantised to W's
+    block format (NVFP4 with the activation global ``input_scale``; MXFP4: 1.0)."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = W.new_workspace(M)
+    o = _opts(opts)
+    check(lib().vt_fp4_w4a4_gemm_ex(_ptr(A), M, A.stride(0), W.handle, float(input_scale),
+                                    _ptr(out), out.stride(0), _ptr(workspace),
+                                    workspace.numel(), _stream(stream),
+                                    ctypes.byref(o) if o else None), "vt_fp4_w4a4_gemm")
+    return out
+
+
+def quantize_act(A: torch.Tensor, fmt: int, input_scale: float = 1.0, stream=None):
+    """The W4A4 activation quantiser: A bf16 [M, K] (CUDA, unit inner stride) ->
+    (codes u8 [M, K/2], scales u8 [M, K/g])."""
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.stride(1) != 1 or not A.is_cuda:
+        raise ValueError("A must be a bf16 CUDA [M, K] tensor with unit inner stride")
+    M, K = A.shape
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=A.device)
+    scales = torch.empty((M, K // GROUP[fmt]), dtype=torch.uint8, device=A.device)
+    check(lib().vt_fp4_quantize_act(_ptr(A), M, A.stride(0), K, fmt, float(input_scale),
+                                    _ptr(codes), _ptr(scales), _stream(stream)),
+          "vt_fp4_quantize_act")
+    return codes, scales
 
 
 def w4a16_gemm_moe(A: torch.Tensor, W: PackedWeight, topk_ids: torch.Tensor,

@@ -59,6 +59,11 @@ SIGNATURES = {
     "vt_fp4_dequant": (_ST, [_P, _P, _P]),
     "vt_fp4_unpack": (_ST, [_P, _P, _P, _P]),
     "vt_fp4_quantize": (_ST, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, _P]),
+    "vt_fp4_quantize_act": (_ST, [_P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_float, _P, _P,
+                                  _P]),
+    "vt_fp4_w4a4_gemm": (_ST, [_P, _I64, _I64, _P, ctypes.c_float, _P, _I64, _P, _SZ, _P]),
+    "vt_fp4_w4a4_gemm_ex": (_ST, [_P, _I64, _I64, _P, ctypes.c_float, _P, _I64, _P, _SZ, _P,
+                                  ctypes.POINTER(GemmOpts)]),
     "vt_fp4_last_error": (ctypes.c_char_p, []),
 }
 

@@ -1,6 +1,7 @@
 // C ABI of libvtfp4 (declared in include/vt_fp4.h): argument checks, handle state, launch
 // shape selection and kernel launches.  Every check that needs no GPU runs before any
 // CUDA call, so bad arguments are rejected the same way on a host without a device.
+#include <float.h>
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -169,6 +170,15 @@ vt_status do_prepack(const uint8_t* const codes[2], const uint8_t* const scales[
   return VT_OK;
 }
 
+// The W4A4 activation global: NVFP4 takes a positive normal float, MXFP4 has none (1.0).
+vt_status check_input_scale(int fmt, float a) {
+  if (fmt == VT_FP4_NVFP4 ? (isfinite(a) && a >= FLT_MIN) : a == 1.0f) return VT_OK;
+  return fail(VT_ERR_INVALID_ARG,
+              fmt == VT_FP4_NVFP4 ? "input_scale must be a positive normal float (got %g)"
+                                  : "MXFP4 activations have no global scale: input_scale must be 1 (got %g)",
+              (double)a);
+}
+
 vt_status check_handle(vt_fp4_handle W) {
   if (!W) return fail(VT_ERR_INVALID_ARG, "weight handle is NULL");
   return VT_OK;
@@ -302,7 +312,7 @@ namespace {
 vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,
                     int64_t ldc, void* workspace, size_t ws_bytes, vt_stream_t s,
                     const vt_fp4_gemm_opts* opts, int32_t* g_idx, float* g_val,
-                    bool silu = false) {
+                    bool silu = false, bool w4a4 = false, float alpha = 1.0f) {
   if (vt_status st = check_handle(W)) return st;
   if (W->E > 1) return fail(VT_ERR_INVALID_ARG, "a grouped weight serves vt_fp4_w4a16_gemm_moe");
   if (M < 0) return fail(VT_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
@@ -374,6 +384,8 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     D.withhold = opts ? opts->withhold_weights : 0;
     D.layout = (uint32_t)W->layout;
     D.silu = silu ? 1 : 0;
+    D.w4a4 = w4a4 ? 1 : 0;
+    D.alpha = alpha;
     if (g_idx) {
       D.g_idx = g_idx;
       D.g_val = g_val;
@@ -413,6 +425,8 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
   P.withhold = opts ? opts->withhold_weights : 0;
   P.layout = (uint32_t)W->layout;
   P.silu = silu ? 1 : 0;
+  P.w4a4 = w4a4 ? 1 : 0;
+  P.alpha = alpha;
   int launches = 0, grid = 0;
   int64_t tiles = 0;
   cudaError_t e = launch_prefill(P, (cudaStream_t)s, &launches, &grid, &tiles);
@@ -542,6 +556,37 @@ vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_f
     return fail(VT_ERR_INVALID_ARG,
                 "the SiLU-and-multiply epilogue needs a weight from vt_fp4_prepack_gate_up_paired");
   return gemm_impl(A, M, lda, W, C, ldc, workspace, ws_bytes, s, nullptr, nullptr, nullptr, true);
+}
+
+vt_status vt_fp4_w4a4_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                              float input_scale, void* C, int64_t ldc, void* workspace,
+                              size_t ws_bytes, vt_stream_t s, const vt_fp4_gemm_opts* opts) {
+  if (vt_status st = check_handle(W)) return st;
+  if (vt_status st = check_input_scale(W->fmt, input_scale)) return st;
+  return gemm_impl(A, M, lda, W, C, ldc, workspace, ws_bytes, s, opts, nullptr, nullptr, false,
+                   true, input_scale);
+}
+
+vt_status vt_fp4_w4a4_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                           float input_scale, void* C, int64_t ldc, void* workspace,
+                           size_t ws_bytes, vt_stream_t s) {
+  return vt_fp4_w4a4_gemm_ex(A, M, lda, W, input_scale, C, ldc, workspace, ws_bytes, s, nullptr);
+}
+
+vt_status vt_fp4_quantize_act(const void* A, int64_t M, int64_t lda, int64_t K,
+                              vt_fp4_format fmt, float input_scale, uint8_t* codes,
+                              uint8_t* scales, vt_stream_t s) {
+  if (vt_status st = check_shape(fmt, 1, K)) return st;
+  if (vt_status st = check_input_scale(fmt, input_scale)) return st;
+  if (M < 0) return fail(VT_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
+  if (M == 0) return VT_OK;
+  if (!A || !codes || !scales) return fail(VT_ERR_INVALID_ARG, "A, codes and scales must be set");
+  if (lda < K) return fail(VT_ERR_INVALID_ARG, "lda (%lld) must be >= K", (long long)lda);
+  if (!aligned(A, 16) || lda % 8 || !aligned(codes, 16))
+    return fail(VT_ERR_MISALIGNED, "A and codes must be 16-byte aligned with lda %% 8 == 0");
+  cudaError_t e = launch_quantize_act(A, M, lda, K, fmt, input_scale, codes, scales,
+                                      (cudaStream_t)s);
+  return e == cudaSuccess ? VT_OK : cuda_fail(e, "activation quantiser launch");
 }
 
 vt_status vt_fp4_w4a16_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void* C,

@@ -18,6 +18,7 @@
 // finished by the last CTA to arrive, which adds the CTAs' partials in CTA order.
 #include <cuda_bf16.h>
 
+#include "actq.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -101,6 +102,48 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep_a(const __nv_bfloat16* __
   uint4* dst = reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8)));
   *dst = make_uint4(o[0], o[1], o[2], o[3]);
   if (gi == 0) ascale[kt * kAScaleStride + m] = ldexpf(1.0f, p);
+}
+
+// W4A4: the same pre-pass with the activations quantised to the weight's block format
+// (fp32 decisions, actq.cuh) and written as their exact dequantised values: NVFP4 c * s with
+// ascale = alpha; MXFP4 c * 2^(e - p) with p = (largest group exponent of the k tile) - 12,
+// at least -126, and ascale = 2^p.  A group holding an inf or NaN is written as NaN.
+template <int FMT>
+__global__ void __launch_bounds__(kPrepThreads) k_prep_a4(const __nv_bfloat16* __restrict__ A,
+                                                          int64_t lda, int64_t K, int64_t KT,
+                                                          int rows, __half* __restrict__ Ap,
+                                                          float* __restrict__ ascale,
+                                                          float alpha, float alpha6) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int m = blockIdx.x;
+  const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + (threadIdx.x >> 3);
+  const int gi = threadIdx.x & 7;
+  const int64_t k0 = kt * 64 + gi * 8;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // the group's largest magnitude: 2 granules (NVFP4) or 4 (MXFP4) in adjacent lanes
+  int mg = bf16_maxmag8(w);
+  mg = max(mg, __shfl_xor_sync(0xffffffffu, mg, 1));
+  if constexpr (FMT == FMT_MX) mg = max(mg, __shfl_xor_sync(0xffffffffu, mg, 2));
+  const int mt = max(min(mg, 0x7F7F), __shfl_xor_sync(0xffffffffu, min(mg, 0x7F7F), 4));
+  if (kt >= KT) return;
+  const bool bad = mg >= 0x7F80;
+  const float amax = __uint_as_float((uint32_t)(bad ? 0 : mg) << 16);
+  uint4 o;
+  float sc;
+  if constexpr (FMT == FMT_NV) {
+    o = aq_nv_granule(w, aq_nv_group(amax, alpha, alpha6), bad, nullptr);
+    sc = alpha;
+  } else {
+    const int et = aq_mx_exp(__uint_as_float((uint32_t)mt << 16));
+    const int p = max(et - 12, -126);
+    o = aq_mx_granule(w, aq_mx_exp(amax), p, bad, nullptr);
+    sc = ldexpf(1.0f, p);
+  }
+  *reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8))) = o;
+  if (gi == 0) ascale[kt * kAScaleStride + m] = sc;
 }
 
 // ------------------------------------------------------------------- main kernel
@@ -862,8 +905,16 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_prep_a, reinterpret_cast<const __nv_bfloat16*>(L.A), L.lda,
-                           L.K, L.KT, L.M, reinterpret_cast<__half*>(L.Ap), L.ascale);
+    const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(L.A);
+    __half* ap = reinterpret_cast<__half*>(L.Ap);
+    if (!L.w4a4)
+      e = cudaLaunchKernelEx(&cfg, k_prep_a, a, L.lda, L.K, L.KT, L.M, ap, L.ascale);
+    else if (L.fmt == FMT_NV)
+      e = cudaLaunchKernelEx(&cfg, k_prep_a4<FMT_NV>, a, L.lda, L.K, L.KT, L.M, ap, L.ascale,
+                             L.alpha, 6.0f * L.alpha);
+    else
+      e = cudaLaunchKernelEx(&cfg, k_prep_a4<FMT_MX>, a, L.lda, L.K, L.KT, L.M, ap, L.ascale,
+                             L.alpha, 6.0f * L.alpha);
     if (e != cudaSuccess) return e;
   }
   // stage width in k tiles (KS): 4 or 8

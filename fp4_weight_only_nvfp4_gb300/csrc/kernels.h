@@ -46,6 +46,10 @@ struct DecodeLaunch {
   // grouped (mixture-of-experts) mode: packed = expert 0's packed weight
   const int* gtab = nullptr;  // group table in the workspace
   int64_t expert_bytes = 0;   // bytes per expert's packed weight
+  // W4A4: the pre-pass quantises the activations to the weight's block format (alpha:
+  // NVFP4 activation global)
+  int w4a4 = 0;
+  float alpha = 1.0f;
 };
 int decode_mt(int M);  // 8 or 16
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
@@ -75,6 +79,8 @@ struct PrefillLaunch {
   int withhold;           // test hook: the producer issues no copies
   uint32_t layout = 0;    // packed row order (kLayoutRows / kLayoutPaired)
   int silu = 0;           // paired gate_up: C[M][I] = silu(gate) * up
+  int w4a4 = 0;           // quantise the activations first (see DecodeLaunch)
+  float alpha = 1.0f;
 };
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches, int* grid_out,
                            int64_t* tiles_out);
@@ -82,6 +88,9 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
 // Quantiser.
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, int fmt, uint8_t* codes,
                             uint8_t* scales, float* global_out, void* scratch, cudaStream_t s);
+// W4A4 activation quantiser: bf16 A [M][lda] -> codes [M][K/2], scales [M][K/g].
+cudaError_t launch_quantize_act(const void* A, int64_t M, int64_t lda, int64_t K, int fmt,
+                                float alpha, uint8_t* codes, uint8_t* scales, cudaStream_t s);
 
 constexpr int kMaxDecodeGrid = 512;
 

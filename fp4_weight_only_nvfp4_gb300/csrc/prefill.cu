@@ -27,6 +27,7 @@
 
 #include <mutex>
 
+#include "actq.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -539,6 +540,67 @@ __global__ void __launch_bounds__(kRowThreads) k_prep_rows(const __nv_bfloat16* 
   if (threadIdx.x == 0) rowscale[m] = ldexpf(1.0f, p);
 }
 
+// W4A4: the activations quantised to the weight's block format (fp32 decisions, actq.cuh)
+// and written as their exact dequantised values: NVFP4 A' = c * s, rowscale = alpha; MXFP4
+// A' = c * 2^(e - p), p = (the row's largest group exponent) - 12, at least -126,
+// rowscale = 2^p.  One CTA per token row, one group per thread; a group holding an inf or
+// NaN is written as NaN.
+template <int FMT>
+__global__ void __launch_bounds__(kRowThreads) k_prep_rows4(const __nv_bfloat16* __restrict__ A,
+                                                            int64_t lda, int64_t K, int64_t ldp,
+                                                            __half* __restrict__ Ap,
+                                                            float* __restrict__ rowscale,
+                                                            float alpha, float alpha6) {
+  constexpr int G = FMT == FMT_NV ? 16 : 32, NG = G / 8;
+  const int64_t m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(A + m * lda);
+  const int64_t ngr = K / G;
+  int p = 0;
+  if constexpr (FMT == FMT_MX) {
+    __shared__ int s_max[kRowThreads / 32];
+    int mx = 0;
+    for (int64_t i = threadIdx.x; i < K / 8; i += kRowThreads) {
+      const uint4 v = __ldg(row + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      mx = max(mx, min(bf16_maxmag8(w), 0x7F7F));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0;
+#pragma unroll
+    for (int i = 0; i < kRowThreads / 32; ++i) mx = max(mx, s_max[i]);
+    p = max(aq_mx_exp(__uint_as_float((uint32_t)mx << 16)) - 12, -126);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(Ap + m * ldp);
+  for (int64_t grp = threadIdx.x; grp < ngr; grp += kRowThreads) {
+    uint32_t w[NG][4];
+    int mg = 0;
+#pragma unroll
+    for (int v = 0; v < NG; ++v) {
+      const uint4 x = __ldg(row + grp * NG + v);
+      w[v][0] = x.x;
+      w[v][1] = x.y;
+      w[v][2] = x.z;
+      w[v][3] = x.w;
+      mg = max(mg, bf16_maxmag8(w[v]));
+    }
+    const bool bad = mg >= 0x7F80;
+    const float amax = __uint_as_float((uint32_t)(bad ? 0 : mg) << 16);
+    if constexpr (FMT == FMT_NV) {
+      const AqNvGroup g = aq_nv_group(amax, alpha, alpha6);
+#pragma unroll
+      for (int v = 0; v < NG; ++v) dst[grp * NG + v] = aq_nv_granule(w[v], g, bad, nullptr);
+    } else {
+      const int e = aq_mx_exp(amax);
+#pragma unroll
+      for (int v = 0; v < NG; ++v) dst[grp * NG + v] = aq_mx_granule(w[v], e, p, bad, nullptr);
+    }
+  }
+  if (threadIdx.x == 0) rowscale[m] = FMT == FMT_NV ? alpha : ldexpf(1.0f, p);
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -581,9 +643,16 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   // the activation pre-pass writes A' rows [0, M) with row stride Kp
-  k_prep_rows<<<(unsigned)L.M, kRowThreads, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(L.A), L.lda, L.K, Kp,
-      reinterpret_cast<__half*>(L.Ap), L.rowscale);
+  const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(L.A);
+  __half* ap = reinterpret_cast<__half*>(L.Ap);
+  if (!L.w4a4)
+    k_prep_rows<<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale);
+  else if (L.fmt == FMT_NV)
+    k_prep_rows4<FMT_NV><<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale,
+                                                              L.alpha, 6.0f * L.alpha);
+  else
+    k_prep_rows4<FMT_MX><<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale,
+                                                              L.alpha, 6.0f * L.alpha);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // A' as a 2-D tensor {K, M}: reads past K or M return zeros

@@ -8,6 +8,7 @@
 // keep-quant + Qwen e2e" (PR #38), commit "W2" (E8M0 scale per 32, no global).
 #include <cuda_bf16.h>
 
+#include "actq.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -163,6 +164,60 @@ __global__ void k_q_mx(const uint16_t* __restrict__ W, int64_t N, int64_t K,
   *reinterpret_cast<uint4*>(codes + n * (K / 2) + grp * 16) =
       make_uint4(packed[0], packed[1], packed[2], packed[3]);
   scales[i] = (uint8_t)(e + 127);
+}
+
+// W4A4 activation quantiser (fp32 decisions, actq.cuh): one thread per group.  A group
+// holding an inf or NaN gets the format's NaN scale byte (E4M3 0x7F, E8M0 0xFF) and zero codes.
+template <int FMT>
+__global__ void k_qa(const uint16_t* __restrict__ A, int64_t M, int64_t lda, int64_t K,
+                     float alpha, float alpha6, uint8_t* __restrict__ codes,
+                     uint8_t* __restrict__ scales) {
+  constexpr int G = FMT == FMT_NV ? 16 : 32, NG = G / 8;
+  const int64_t gpr = K / G, total = M * gpr;
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int64_t m = i / gpr, grp = i % gpr;
+  const uint4* src = reinterpret_cast<const uint4*>(A + m * lda + grp * G);
+  uint32_t w[NG][4];
+  int mx = 0;
+#pragma unroll
+  for (int v = 0; v < NG; ++v) {
+    const uint4 x = src[v];
+    w[v][0] = x.x;
+    w[v][1] = x.y;
+    w[v][2] = x.z;
+    w[v][3] = x.w;
+    mx = max(mx, bf16_maxmag8(w[v]));
+  }
+  const bool bad = mx >= 0x7F80;
+  const float amax = __uint_as_float((uint32_t)(bad ? 0 : mx) << 16);
+  uint32_t cw[NG];
+  uint32_t sbyte;
+  if constexpr (FMT == FMT_NV) {
+    const AqNvGroup g = aq_nv_group(amax, alpha, alpha6);
+#pragma unroll
+    for (int v = 0; v < NG; ++v) aq_nv_granule(w[v], g, bad, &cw[v]);
+    sbyte = bad ? 0x7Fu : g.sbyte;
+  } else {
+    const int e = aq_mx_exp(amax);
+#pragma unroll
+    for (int v = 0; v < NG; ++v) aq_mx_granule(w[v], e, e, bad, &cw[v]);
+    sbyte = bad ? 0xFFu : (uint32_t)(e + 127);
+  }
+  uint8_t* dst = codes + m * (K / 2) + grp * (G / 2);
+  if constexpr (FMT == FMT_NV) *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+  else *reinterpret_cast<uint4*>(dst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  scales[i] = (uint8_t)sbyte;
+}
+
+cudaError_t launch_quantize_act(const void* A, int64_t M, int64_t lda, int64_t K, int fmt,
+                                float alpha, uint8_t* codes, uint8_t* scales, cudaStream_t s) {
+  const uint16_t* a = reinterpret_cast<const uint16_t*>(A);
+  const int64_t groups = M * (K / (fmt == FMT_NV ? 16 : 32));
+  const unsigned blocks = (unsigned)((groups + 255) / 256);
+  if (fmt == FMT_NV) k_qa<FMT_NV><<<blocks, 256, 0, s>>>(a, M, lda, K, alpha, 6.0f * alpha, codes, scales);
+  else k_qa<FMT_MX><<<blocks, 256, 0, s>>>(a, M, lda, K, alpha, 6.0f * alpha, codes, scales);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, int fmt, uint8_t* codes,

@@ -250,6 +250,43 @@ vt_status vt_fp4_workspace_status(void* workspace, vt_stream_t s, int* status);
 /* Host-side record of the last GEMM launched on W. */
 vt_status vt_fp4_stats(vt_fp4_handle W, vt_fp4_launch_info* info);
 
+/* -------------------------------------------------------------------- W4A4 */
+
+/* The W4A4 arm: C = Q(A) . W^T with Q the activation quantiser below (activations in the
+ * weight's block format), fp32 accumulation, bf16 output.  NVFP4: input_scale is the
+ * per-tensor activation global (the checkpoint's input_scale, a multiplier like the
+ * weight's global), a positive normal float; MXFP4: input_scale must be 1.0f.  Source:
+ * "re-verify 27B NVFP4 on the nvidia ModelOpt checkpoint" (PR #178), section "W4A16 is
+ * the default for ModelOpt" (consuming input_scale makes the layer true W4A4 and routes
+ * it to the fp4-activation GEMM; the W4A16 arm stays the default); "native MXFP4
+ * keep-quant + Qwen e2e" (PR #38), commit "W0" (MXFP4 activations, group 32).  The
+ * quantised activations are held as their exact dequantised values in f16 and multiplied
+ * on the same tensor-core paths as vt_fp4_w4a16_gemm (decode M <= 16, tile kernel above).
+ * A group of activations holding an inf or NaN yields NaN outputs for its tokens.
+ * Arguments, workspace, determinism and errors as vt_fp4_w4a16_gemm; a bad input_scale
+ * is VT_ERR_INVALID_ARG. */
+vt_status vt_fp4_w4a4_gemm(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                           float input_scale, void* C, int64_t ldc, void* workspace,
+                           size_t ws_bytes, vt_stream_t s);
+
+/* As vt_fp4_w4a4_gemm with tuning overrides (NULL opts = defaults). */
+vt_status vt_fp4_w4a4_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
+                              float input_scale, void* C, int64_t ldc, void* workspace,
+                              size_t ws_bytes, vt_stream_t s, const vt_fp4_gemm_opts* opts);
+
+/* The W4A4 activation quantiser on its own: A (device) bf16 [M][lda] (16-byte aligned,
+ * lda % 8 == 0, lda >= K, K % g == 0) -> codes (device, 16-byte aligned) u8 [M][K/2]
+ * (low nibble = even k) and scales (device) u8 [M][K/g].  Decisions in fp32, round to
+ * nearest even, saturating:
+ *   NVFP4: s = E4M3(amax_g / fl32(6 input_scale)); code = E2M1(x / fl32(s input_scale))
+ *          (all codes 0 when s = 0)
+ *   MXFP4: e = min{e : 6 2^e >= amax_g} in [-127, 127], byte e + 127; code = E2M1(x 2^-e)
+ * A group holding an inf or NaN gets the NaN scale byte (0x7F E4M3, 0xFF E8M0) and zero
+ * codes.  Asynchronous on `s`. */
+vt_status vt_fp4_quantize_act(const void* A, int64_t M, int64_t lda, int64_t K,
+                              vt_fp4_format fmt, float input_scale, uint8_t* codes,
+                              uint8_t* scales, vt_stream_t s);
+
 /* ------------------------------------------------------------ debug / tests */
 
 /* out (device) fp32 [N][K]: the dequantised weight as the kernels see it,

@@ -105,6 +105,23 @@ def test_quantize_rejects_bad_shapes(L):
     assert L.vt_fp4_quantize(None, 4, 64, 0, fake, fake, fake, fake, None) == 1
 
 
+def test_w4a4_rejects_bad_arguments_without_a_gpu(L):
+    """The activation quantiser and the W4A4 GEMM check shapes, the activation global and
+    the pointers before any CUDA call."""
+    fake = ctypes.c_void_p(0x1000)
+    q = L.vt_fp4_quantize_act
+    assert q(fake, 4, 64, 24, 0, 1.0, fake, fake, None) == 1       # K % 16
+    assert q(fake, 4, 64, 48, 1, 1.0, fake, fake, None) == 1       # K % 32
+    for alpha in (0.0, -2.0, float("nan"), float("inf"), 1e-40):
+        assert q(fake, 4, 64, 64, 0, alpha, fake, fake, None) == 1
+    assert q(fake, 4, 64, 64, 1, 0.5, fake, fake, None) == 1       # MXFP4: no global
+    assert q(None, 4, 64, 64, 0, 1.0, fake, fake, None) == 1
+    assert q(fake, 4, 32, 64, 0, 1.0, fake, fake, None) == 1       # lda < K
+    assert q(ctypes.c_void_p(0x1008), 4, 64, 64, 0, 1.0, fake, fake, None) == 3  # misaligned
+    assert q(fake, 0, 64, 64, 0, 1.0, fake, fake, None) == 0       # M == 0: no-op
+    assert L.vt_fp4_w4a4_gemm(fake, 4, 64, None, 1.0, fake, 64, fake, 1 << 20, None) == 1
+
+
 def test_algorithmic_bytes_reproduce_the_pages_figures():
     """tests/golden/footprint_pages.txt: the packed head is 0.6660 GiB, its bf16 expansion
     2.3683 GiB, the avoidable traffic 1.702 GiB."""
