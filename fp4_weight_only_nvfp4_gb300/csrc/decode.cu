@@ -37,6 +37,10 @@ constexpr int kGtRowsum = kGtCount + kGtMaxProblems;
 constexpr int kGtPair = kGtRowsum + kGtMaxProblems;
 constexpr int kGtInts = kGtPair + kGtMaxProblems * 16;
 constexpr int kSlotPad = 36;        // floats per token row of a warp's reduction slot
+#ifndef VT_DECODE_PREFETCH
+#define VT_DECODE_PREFETCH 2
+#endif
+constexpr int kPrefetchStages = VT_DECODE_PREFETCH;  // stages requested before the pre-pass ends
 
 int decode_mt(int M) { return M <= 8 ? 8 : 16; }
 
@@ -348,35 +352,43 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       const uint64_t pol = l2_evict_first_policy();   // weights: streamed once
       const uint64_t pol_a = l2_evict_last_policy();  // activations: re-read by every CTA
       const uint32_t per_tile = (uint32_t)(TB + M * 128 + kAScaleStride * 4);
-      // the weights do not depend on the activation pre-pass: start them first
+      // The weights do not depend on the activation pre-pass: the first stages' weights are
+      // requested before waiting for it.  Only a few: the consumers run at about the HBM
+      // rate, so a deeper head start does not shorten the call, while every weight byte
+      // queued ahead delays the first activation copies behind it.
+      const int P = S < kPrefetchStages ? S : kPrefetchStages;
       int64_t pos = i0;
-      int kt = kt_first, s = 0;
-      for (; s < S && pos < i1; ++s) {
+      int kt = kt_first, issued = 0;
+      for (; issued < P && pos < i1; ++issued) {
         const int n = stage_len(pos, kt);
-        mbar_expect_tx(full_u + 8 * s, n * per_tile);
-        bulk_g2s(ring_u + s * STAGE, p.tiles + pos * TB, (uint32_t)(n * TB), full_u + 8 * s, pol);
+        mbar_expect_tx(full_u + 8 * issued, n * per_tile);
+        bulk_g2s(ring_u + issued * STAGE, p.tiles + pos * TB, (uint32_t)(n * TB),
+                 full_u + 8 * issued, pol);
         pos += n;
         kt += n;
         if (kt == KTi) kt = 0;
       }
       pdl_wait();
       fence_proxy_async_all();
-      pos = i0;
-      kt = kt_first;
-      for (int s2 = 0; s2 < s; ++s2) {
-        const int n = stage_len(pos, kt);
-        bulk_g2s(ring_u + s2 * STAGE + WBYTES, p.Ap + (int64_t)kt * M * 64,
-                 (uint32_t)(n * M * 128), full_u + 8 * s2, pol_a);
-        bulk_g2s(ring_u + s2 * STAGE + SCALES_OFF, p.ascale + (int64_t)kt * kAScaleStride,
-                 (uint32_t)(n * kAScaleStride * 4), full_u + 8 * s2, pol_a);
-        pos += n;
-        kt += n;
-        if (kt == KTi) kt = 0;
+      {
+        int64_t pos2 = i0;
+        int kt2 = kt_first;
+        for (int s2 = 0; s2 < issued; ++s2) {
+          const int n = stage_len(pos2, kt2);
+          bulk_g2s(ring_u + s2 * STAGE + WBYTES, p.Ap + (int64_t)kt2 * M * 64,
+                   (uint32_t)(n * M * 128), full_u + 8 * s2, pol_a);
+          bulk_g2s(ring_u + s2 * STAGE + SCALES_OFF, p.ascale + (int64_t)kt2 * kAScaleStride,
+                   (uint32_t)(n * kAScaleStride * 4), full_u + 8 * s2, pol_a);
+          pos2 += n;
+          kt2 += n;
+          if (kt2 == KTi) kt2 = 0;
+        }
       }
-      int slot = s == S ? 0 : s;
-      uint32_t par = 0;  // phase parity of the empty barrier of `slot` to wait for
+      // then whole stages; slot issued % S, reused once its previous use has been consumed
+      int slot = issued % S;
       while (pos < i1) {
-        if (!mbar_wait_bounded(empty_u + 8 * slot, par, p.wait_ns)) {
+        if (issued >= S &&
+            !mbar_wait_bounded(empty_u + 8 * slot, (uint32_t)((issued / S - 1) & 1), p.wait_ns)) {
           atomicExch(p.status, 5);
           break;
         }
@@ -391,10 +403,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
         pos += n;
         kt += n;
         if (kt == KTi) kt = 0;
-        if (++slot == S) {
-          slot = 0;
-          par ^= 1u;
-        }
+        ++issued;
+        if (++slot == S) slot = 0;
       }
     }
     return;
