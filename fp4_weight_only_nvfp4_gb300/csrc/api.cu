@@ -397,7 +397,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     W->info.path = 1;
     W->info.grid = D.grid;
-    W->info.warps_per_cta = 17;  // 16 consumer warps + the TMA producer warp
+    W->info.warps_per_cta = 18;  // 16 consumer warps, the TMA producer, the publisher
     W->info.m_tile = mt;
     W->info.items = items;
     W->info.launches = launches;
@@ -521,7 +521,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   if (e != cudaSuccess) return cuda_fail(e, "grouped decode launch");
   W->info.path = 3;
   W->info.grid = D.grid;
-  W->info.warps_per_cta = 17;
+  W->info.warps_per_cta = 18;
   W->info.m_tile = 16;
   W->info.items = items;
   W->info.launches = launches;

@@ -64,14 +64,27 @@ size_t decode_smem_bytes(int fmt, int M, int ks, int stages) {
 constexpr int kPrepThreads = 64;
 constexpr int kPrepTiles = 8;
 
+// Zeroes the split-K counters of this call's decode kernel.  The pre-pass runs after the
+// previous call has finished (griddepcontrol.wait) and before this call's decode kernel
+// counts, so the counters start at zero even when one workspace serves weights of other
+// shapes, whose activation and partial-sum regions overlap this weight's counters.
+__device__ __forceinline__ void zero_counters(int* counters, int64_t n) {
+  const int64_t nb = (int64_t)gridDim.x * gridDim.y;
+  const int64_t b = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+  for (int64_t i = b * blockDim.x + threadIdx.x; i < n; i += nb * blockDim.x) counters[i] = 0;
+}
+
 __global__ void __launch_bounds__(kPrepThreads) k_prep_a(const __nv_bfloat16* __restrict__ A,
                                                          int64_t lda, int64_t K, int64_t KT,
                                                          int rows, __half* __restrict__ Ap,
-                                                         float* __restrict__ ascale) {
+                                                         float* __restrict__ ascale,
+                                                         int* __restrict__ counters,
+                                                         int64_t ncounters) {
   // Let the GEMM kernel launch (it starts streaming weights), then wait for whatever
   // produced A (and for the previous GEMM, which may still read the workspace).
   pdl_launch_dependents();
   pdl_wait();
+  zero_counters(counters, ncounters);
   const int m = blockIdx.x;
   const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + (threadIdx.x >> 3);
   const int gi = threadIdx.x & 7;
@@ -117,9 +130,12 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep_a4(const __nv_bfloat16* _
                                                           int64_t lda, int64_t K, int64_t KT,
                                                           int rows, __half* __restrict__ Ap,
                                                           float* __restrict__ ascale,
-                                                          float alpha, float alpha6) {
+                                                          float alpha, float alpha6,
+                                                          int* __restrict__ counters,
+                                                          int64_t ncounters) {
   pdl_launch_dependents();
   pdl_wait();
+  zero_counters(counters, ncounters);
   const int m = blockIdx.x;
   const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + (threadIdx.x >> 3);
   const int gi = threadIdx.x & 7;
@@ -229,16 +245,48 @@ __device__ __forceinline__ unsigned int arrive_acq_rel(unsigned int* ctr) {
   return prev;
 }
 
+// Publication of a partial sum: a release add at GPU scope (the writes it publishes reach
+// this thread through a CTA-scope barrier first); the issuing thread does not wait for it.
+__device__ __forceinline__ void publish_release(unsigned int* ctr) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* ctr) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v;
+}
+
+// Bounded wait until *ctr == target (acquire); false once `limit_ns` of wall time passed.
+__device__ __forceinline__ bool wait_count(const unsigned int* ctr, unsigned int target,
+                                           uint64_t limit_ns) {
+  if (ld_acquire_gpu(ctr) == target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(ctr) == target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// CTA layout: 16 consumer warps and one producer warp.  A stage holds up to KS consecutive
-// k tiles of one 128-row tile (one TMA bulk copy of the weights, one of the matching
-// activation slices, one of their scales); consumer warp w owns the row-block pair w % 4
-// (32 rows) and the stage's k tiles w / 4, w / 4 + 4, ... .  The producer is one thread.
+// CTA layout: 16 consumer warps, one producer warp and one publisher warp.  A stage holds
+// up to KS consecutive k tiles of one 128-row tile (one TMA bulk copy of the weights, one
+// of the matching activation slices, one of their scales); consumer warp w owns the
+// row-block pair w % 4 (32 rows) and the stage's k tiles w / 4, w / 4 + 4, ... .  The
+// producer is one thread.
+//
+// Row tiles shared by several CTAs (stream-K): the tile's first contributor c_lo -- for
+// which the tile is its last segment -- reduces it; every later contributor meets the tile
+// as its first segment, writes its partial sums, and the publisher warp announces them with
+// a release add on the tile's counter, so that no consumer waits on a global round trip in
+// the middle of a call.  c_lo waits (bounded) for the count, adds the partials in
+// contributor order to its own and resets the counter for the next call.
 template <int FMT, int MT, int KS, bool GRP>
-__global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const DecodeParams p) {
+__global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const DecodeParams p) {
   constexpr int TB = tile_bytes(FMT);
   constexpr int NJ = MT / 8;           // n8 MMA column blocks
   constexpr int CW = kConsumerWarps;
@@ -246,7 +294,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   constexpr int SLOT = MT * kSlotPad;  // floats per warp reduction slot (32 rows + pad)
   constexpr int WBYTES = KS * TB;      // weight bytes of a full stage
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_flag, s_ncon, s_sello;
+  __shared__ int s_flag, s_ncon;
   __shared__ unsigned long long s_gkey[16];  // greedy head: this CTA's best key per token
   __shared__ int64_t s_clo;
   // The next kernel in the stream may launch now: it only waits (griddepcontrol.wait)
@@ -270,6 +318,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE + (size_t)CW * SLOT * 4);
   uint64_t* empty = full + S;
   const uint32_t ring_u = smem_u32(smem), full_u = smem_u32(full), empty_u = smem_u32(empty);
+  const uint32_t pub_u = smem_u32(empty + S);  // consumers -> publisher: partial written
 
   // Stages walk the CTA's items in order; all loop state advances incrementally.
   const int kt_first = (int)(i0 % KT);
@@ -287,9 +336,23 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
       mbar_init(full_u + 8 * s, 1);
       mbar_init(empty_u + 8 * s, CW);
     }
+    mbar_init(pub_u, CW);
   }
   fence_mbar_init();
   __syncthreads();
+
+  if (warp == CW + 1) {
+    // ------------------------------------------------------------- publisher
+    // A CTA whose range starts inside a row tile shares that tile with the CTA before it:
+    // publish this CTA's partial of it once the consumers have written it.
+    if (lane == 0 && i0 < i1 && i0 % KT != 0) {
+      if (mbar_wait_bounded(pub_u, 0, p.wait_ns))
+        publish_release(reinterpret_cast<unsigned int*>(&p.counters[i0 / KT]));
+      else
+        atomicExch(p.status, 5);
+    }
+    return;
+  }
 
   if constexpr (GRP) {
     if (warp == CW) {
@@ -542,13 +605,13 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
     // is complete when it lies inside this CTA's item range; otherwise one thread finds the
     // CTAs that share it (64-bit divisions, so once per CTA, not per thread).
     const bool complete = (rt * KT >= i0) && (rt * KT + KT <= i1);
-    const int sel = (rt == rt_first) ? 0 : 1;
-    if (!complete && threadIdx.x == 0) {
-      const int64_t c_lo = owner_of(rt * KT, I, G), c_hi = owner_of(rt * KT + KT - 1, I, G);
-      s_clo = c_lo;
-      s_ncon = (int)(c_hi - c_lo + 1);
-      // contributor c_lo wrote its slot 0 only if its range starts exactly at the tile
-      s_sello = ((c_lo * I / G) == rt * KT) ? 0 : 1;
+    // shared tile: this CTA reduces it when the tile starts inside its range (then it is
+    // this CTA's last segment), else it contributes its first segment's partial
+    const bool reducer = !complete && rt * KT >= i0;
+    if (reducer && threadIdx.x == 0) {
+      const int64_t c_hi = owner_of(rt * KT + KT - 1, I, G);
+      s_clo = c;
+      s_ncon = (int)(c_hi - c + 1);
     }
     float* my = slots + warp * SLOT;
 #pragma unroll
@@ -580,7 +643,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
         if (i < p.seg_split)
           p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
       }
-    } else {
+    } else if (!reducer) {  // a reducer adds its slots when the other partials are in
       for (int idx = threadIdx.x; idx < nout; idx += CT) {
         const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
         float sum = 0.0f;
@@ -601,39 +664,42 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 32, 1) k_decode(const De
             const float f = n < p.seg_split ? f0 : f1;
             p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
-        } else {
-          p.partials[(((size_t)c * 2 + sel) * MT + m) * 128 + row] = sum;
+        } else if (!reducer) {
+          p.partials[((size_t)c * 2 * MT + m) * 128 + row] = sum;
         }
       }
     }
-    if (!complete) {
-      consumer_sync(CT);  // every partial of this CTA is written
+    if (!complete && !reducer) {
+      // this CTA's partial of a tile reduced by an earlier CTA: hand it to the publisher
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pub_u);
+    }
+    if (reducer) {
       if (threadIdx.x == 0) {
-        const int prev = (int)arrive_acq_rel(reinterpret_cast<unsigned int*>(&p.counters[rt]));
-        const int last = (prev == s_ncon - 1);
-        if (last) p.counters[rt] = 0;  // self-reset for the next call
-        s_flag = last;
+        unsigned int* ctr = reinterpret_cast<unsigned int*>(&p.counters[rt]);
+        const bool got = wait_count(ctr, (unsigned int)(s_ncon - 1), p.wait_ns);
+        if (got) *ctr = 0;  // every contributor has arrived: reset for the next call
+        else atomicExch(p.status, 5);
+        s_flag = got;
       }
       consumer_sync(CT);
       if (s_flag) {
-        // Contributor cc > c_lo starts inside this row tile (its slot 0).  Loads are issued
-        // in batches of 8 and added in contributor order.
+        // this CTA's own partial (its slots, in fixed order) first, then the later
+        // contributors' partials in contributor order, loaded in batches of 8
         const int64_t c_lo = s_clo;
-        const int sel_lo = s_sello;
         const int ncon = s_ncon;
-        // the CTAs' partial sum of (token m, tile row `row`), added in contributor order
         auto tile_sum = [&](int m, int row) -> float {
-          const size_t off = (size_t)m * 128 + row;
+          const int pr = row >> 5, rr = row & 31;
           float sum = 0.0f;
-          for (int b0 = 0; b0 < ncon; b0 += 8) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
+          const size_t off = (size_t)m * 128 + row;
+          for (int b0 = 1; b0 < ncon; b0 += 8) {
             float v[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const int64_t cc = c_lo + b0 + q;
-              const int selc = (b0 + q == 0) ? sel_lo : 0;
-              v[q] = (b0 + q < ncon)
-                         ? __ldcg(&p.partials[((size_t)cc * 2 + selc) * MT * 128 + off])
-                         : 0.0f;
+              v[q] = (b0 + q < ncon) ? __ldcg(&p.partials[(size_t)cc * 2 * MT * 128 + off]) : 0.0f;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -742,7 +808,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
-  cfg.blockDim = dim3((unsigned)(kConsumerWarps * 32 + 32));
+  cfg.blockDim = dim3((unsigned)(kConsumerWarps * 32 + 64));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -766,9 +832,10 @@ __global__ void __launch_bounds__(kPrepThreads) k_group_prep(
     const __nv_bfloat16* __restrict__ A, int64_t lda, int64_t K, int64_t KT,
     const int32_t* __restrict__ topk_ids, int npairs, int topk, int E,
     __half* __restrict__ Ap, float* __restrict__ ascale, int* __restrict__ gtab,
-    int* __restrict__ status) {
+    int* __restrict__ status, int* __restrict__ counters, int64_t ncounters) {
   pdl_launch_dependents();
   pdl_wait();
+  zero_counters(counters, ncounters);
   __shared__ int s_e[kGtMaxProblems], s_prob[kGtMaxProblems], s_slot[kGtMaxProblems];
   __shared__ int s_first[kGtMaxProblems], s_cnt[kGtMaxProblems], s_rsum[kGtMaxProblems];
   __shared__ int s_pexp[kGtMaxProblems], s_P;
@@ -892,7 +959,7 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids
     e = cudaLaunchKernelEx(&cfg, k_group_prep, reinterpret_cast<const __nv_bfloat16*>(L.A),
                            L.lda, L.K, L.KT, topk_ids, npairs, topk, E,
                            reinterpret_cast<__half*>(L.Ap), L.ascale, const_cast<int*>(L.gtab),
-                           L.status);
+                           L.status, L.counters, (int64_t)(pmax < kGtMaxProblems ? pmax : kGtMaxProblems) * L.RT);
     if (e != cudaSuccess) return e;
   }
   if (L.ks == 4) e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 16, 4, true>(L, s) : launch_t<FMT_MX, 16, 4, true>(L, s);
@@ -918,13 +985,14 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) 
     const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(L.A);
     __half* ap = reinterpret_cast<__half*>(L.Ap);
     if (!L.w4a4)
-      e = cudaLaunchKernelEx(&cfg, k_prep_a, a, L.lda, L.K, L.KT, L.M, ap, L.ascale);
+      e = cudaLaunchKernelEx(&cfg, k_prep_a, a, L.lda, L.K, L.KT, L.M, ap, L.ascale, L.counters,
+                             L.RT);
     else if (L.fmt == FMT_NV)
       e = cudaLaunchKernelEx(&cfg, k_prep_a4<FMT_NV>, a, L.lda, L.K, L.KT, L.M, ap, L.ascale,
-                             L.alpha, 6.0f * L.alpha);
+                             L.alpha, 6.0f * L.alpha, L.counters, L.RT);
     else
       e = cudaLaunchKernelEx(&cfg, k_prep_a4<FMT_MX>, a, L.lda, L.K, L.KT, L.M, ap, L.ascale,
-                             L.alpha, 6.0f * L.alpha);
+                             L.alpha, 6.0f * L.alpha, L.counters, L.RT);
     if (e != cudaSuccess) return e;
   }
   // stage width in k tiles (KS): 4 or 8

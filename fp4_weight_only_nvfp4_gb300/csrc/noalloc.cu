@@ -129,7 +129,7 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   if (e != cudaSuccess) return err(VT_ERR_CUDA, cudaGetErrorString(e));
   W->info.path = 1;
   W->info.grid = D.grid;
-  W->info.warps_per_cta = 17;
+  W->info.warps_per_cta = 18;
   W->info.m_tile = mt;
   W->info.items = items;
   W->info.launches = launches;

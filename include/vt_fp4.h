@@ -138,10 +138,10 @@ vt_status vt_fp4_shape(vt_fp4_handle W, vt_fp4_format* fmt, int64_t* N, int64_t*
 
 /* Bytes of workspace a GEMM on W with M <= M_max needs.  The workspace holds the
  * activations converted for the tensor cores, split-K partial sums, per-tile arrival
- * counters and a status word.  The caller zeroes it ONCE after allocation; the library
- * leaves the counters at zero after every call (self-resetting), so it can be reused by
- * later calls in stream order.  A workspace must not be used by two calls that may run
- * at the same time. */
+ * counters and a status word.  The caller zeroes it ONCE after allocation.  Each call's
+ * activation pre-pass zeroes the counters it will use, so one workspace, large enough for
+ * each of them, may serve calls on weights of any shape and any M in stream order.  A
+ * workspace must not be used by two calls that may run at the same time. */
 vt_status vt_fp4_workspace_bytes(vt_fp4_handle W, int64_t M_max, size_t* bytes);
 
 /* C = A . W^T in bf16 with fp32 accumulation.
