@@ -400,7 +400,14 @@ def run_gpu(args, rank: int, world: int):
         for _ in range(max(1, args.warmup)):
             issue()
     stream.synchronize()
-    launches_per_call = sets[0][0][0].stats()["launches"]
+    # kernels per step, as each call reports them (small calls run one kernel, larger ones
+    # a pre-pass and the GEMM)
+    launches_per_step = 0
+    with torch.cuda.stream(stream):
+        for c, layer, pi, M in calls:
+            one_call(c, layer, pi, M)
+            launches_per_step += sets[c][layer][pi].stats()["launches"]
+    stream.synchronize()
 
     # the timed step: one CUDA graph of all the step's calls, back to back (consecutive
     # calls overlap through programmatic dependent launch)
@@ -530,7 +537,7 @@ def run_gpu(args, rank: int, world: int):
     return {
         "value": value, "ms_per_step": ms_step, "step_bytes": step_bytes, "clocks": clocks,
         "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
-        "gpu_launches": launches_per_call * n_calls * args.steps, "copies": copies,
+        "gpu_launches": launches_per_step * args.steps, "copies": copies,
         "calls_per_step": n_calls, "ws_status": ws_status, "unfused": unfused,
     }
 

@@ -73,8 +73,11 @@ WsLayout ws_layout(const vt_fp4_weight_s* W, int64_t M) {
   const int64_t mrows = M <= 16 ? 16 : cdiv(M, 128) * 128;
   L.status = 0;
   L.counters = 256;
+  // the counters keep a fixed region (64 KB, or more for weights of more row tiles), so that
+  // no data of another weight sharing the workspace lands on them
+  const size_t nctr = (size_t)(W->RT > kFixedCounterTiles ? W->RT : kFixedCounterTiles);
   // activation scales: decode [KT][16] floats; prefill one per token row
-  L.rowscale = up256(L.counters + (size_t)W->RT * 4);
+  L.rowscale = up256(L.counters + nctr * 4);
   const size_t nscale = M <= 16 ? (size_t)W->KT * 16 : (size_t)mrows;
   L.ap = up256(L.rowscale + nscale * 4);
   L.partials = up256(L.ap + (size_t)mrows * Kp * 2);
@@ -98,7 +101,8 @@ MoeLayout moe_layout(const vt_fp4_weight_s* W, int64_t npairs) {
   const int64_t pcap = W->E < 128 ? W->E : 128;  // problems: distinct experts of <= 128 pairs
   L.status = 0;
   L.counters = 256;
-  L.partials = up256(L.counters + (size_t)pcap * W->RT * 4);
+  const size_t nctr = (size_t)pcap * W->RT;
+  L.partials = up256(L.counters + (nctr > (size_t)kFixedCounterTiles ? nctr : kFixedCounterTiles) * 4);
   L.table = up256(L.partials + (size_t)kMaxDecodeGrid * 2 * 16 * 128 * 4);
   L.ascale = up256(L.table + (size_t)kGroupTableInts * 4);
   L.ap = up256(L.ascale + (size_t)pcap * W->KT * 16 * 4);
@@ -329,8 +333,9 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
   if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   const int force = opts ? opts->force_path : 0;
-  const bool decode = force ? force == 1 : M <= 16;
-  if (force == 1 && M > 16) return fail(VT_ERR_INVALID_ARG, "decode path needs M <= 16");
+  if (force < 0 || force > 3) return fail(VT_ERR_INVALID_ARG, "force_path must be 0..3");
+  const bool decode = force ? force != 2 : M <= 16;
+  if (decode && M > 16) return fail(VT_ERR_INVALID_ARG, "decode path needs M <= 16");
   if (W->K > 110000) return fail(VT_ERR_UNSUPPORTED, "K > 110000 is not supported");
   WsLayout L = ws_layout(W, decode ? (M < 16 ? M : 16) : M);
   if (ws_bytes < L.total)
@@ -361,13 +366,17 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
     if (ks != 4 && ks != 8) return fail(VT_ERR_INVALID_ARG, "stage width must be 4 or 8 k tiles");
     const int mt = decode_mt((int)M);
+    // small M * K: the decode kernel converts the activations itself (no pre-pass)
+    const bool resident = !w4a4 && !(opts && opts->force_path == 3) &&
+                          decode_resident_ok((int)M, W->KT, W->RT);
+    const int64_t rkt = resident ? W->KT : 0;
     int stages = (opts && opts->stages) ? opts->stages : 0;
     if (!stages) {  // as deep as shared memory allows, at most 6
       stages = 6;
-      while (stages > 2 && decode_smem_bytes(W->fmt, (int)M, ks, stages) > 226 * 1024) --stages;
+      while (stages > 2 && decode_smem_bytes(W->fmt, (int)M, ks, stages, rkt) > 226 * 1024) --stages;
     }
     if (stages < 2 || stages > 16) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 16]");
-    if (decode_smem_bytes(W->fmt, (int)M, ks, stages) > 226 * 1024)
+    if (decode_smem_bytes(W->fmt, (int)M, ks, stages, rkt) > 226 * 1024)
       return fail(VT_ERR_INVALID_ARG, "stage width x stages exceed shared memory");
     int64_t grid = (opts && opts->grid) ? opts->grid : sm_count();
     if (!(opts && opts->grid)) {
@@ -386,6 +395,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     D.silu = silu ? 1 : 0;
     D.w4a4 = w4a4 ? 1 : 0;
     D.alpha = alpha;
+    D.resident = resident ? 1 : 0;
     if (g_idx) {
       D.g_idx = g_idx;
       D.g_val = g_val;

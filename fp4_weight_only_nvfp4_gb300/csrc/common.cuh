@@ -225,6 +225,16 @@ __device__ __forceinline__ int4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ int4 ld_global_nc_v4(const void* p) {
   int4 v;
   asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"

@@ -41,16 +41,29 @@ constexpr int kSlotPad = 36;        // floats per token row of a warp's reductio
 #define VT_DECODE_PREFETCH 2
 #endif
 constexpr int kPrefetchStages = VT_DECODE_PREFETCH;  // stages requested before the pre-pass ends
+#ifndef VT_RESIDENT_PREFETCH
+#define VT_RESIDENT_PREFETCH 2
+#endif
+constexpr int kResidentPrefetch = VT_RESIDENT_PREFETCH;  // resident mode: stages before A is in
 
 int decode_mt(int M) { return M <= 8 ? 8 : 16; }
 
 // Dynamic shared memory of the decode kernel: `stages` stages of `ks` k tiles (weights, M
 // activation rows and the activation scales each), the consumer warps' reduction slots and
 // the barriers.
-size_t decode_smem_bytes(int fmt, int M, int ks, int stages) {
+size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt) {
   const size_t mt = (size_t)decode_mt(M);
-  const size_t stage = (size_t)ks * (tile_bytes(fmt) + (size_t)M * 128 + kAScaleStride * 4);
-  return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 + (size_t)stages * 16 + 64;
+  const size_t stage = resident_kt ? (size_t)ks * tile_bytes(fmt)
+                                   : (size_t)ks * (tile_bytes(fmt) + (size_t)M * 128 + kAScaleStride * 4);
+  return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 +
+         decode_resident_bytes(M, resident_kt) + (size_t)stages * 16 + 64;
+}
+
+bool decode_resident_ok(int M, int64_t KT, int64_t RT) {
+  // measured: converting in every CTA pays off up to about 16 KB of activations (M = 1
+  // at K = 8192, M = 2 at K = 4096); beyond that the pre-pass is faster
+  return M >= 1 && M <= kResidentMaxM && RT <= kFixedCounterTiles &&
+         (size_t)M * KT * 128 <= kResidentMaxBytes;
 }
 
 // ------------------------------------------------------------- activation pre-pass
@@ -190,6 +203,8 @@ struct DecodeParams {
   int silu;                    // paired gate_up: write silu(gate) * up, C is [M][I]
   // grouped (mixture-of-experts) mode: problems = experts in use, from the pre-pass
   const int* gtab;             // group table (see kGt*)
+  const __nv_bfloat16* A;      // resident mode: the bf16 activations [M][lda]
+  int64_t lda, K;
   const uint8_t* gbase;        // expert e's packed weight at gbase + e * expert_bytes
   int64_t expert_bytes, RT;    // bytes per expert; 128-row tiles per expert
 };
@@ -285,7 +300,14 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // a release add on the tile's counter, so that no consumer waits on a global round trip in
 // the middle of a call.  c_lo waits (bounded) for the count, adds the partials in
 // contributor order to its own and resets the counter for the next call.
-template <int FMT, int MT, int KS, bool GRP>
+//
+// Resident mode (RA, small M * K): the kernel converts the whole activation matrix into
+// shared memory itself after griddepcontrol.wait (no pre-pass kernel), the stages carry
+// weights only, and the producer fills the whole ring at once, since no activation copy
+// can queue behind the weights.  The split-K counters then rely on being left at zero by
+// the previous call (each reducer resets its counter; the workspace keeps the counters in a
+// fixed region that no other data of any weight overlaps).
+template <int FMT, int MT, int KS, bool GRP, bool RA>
 __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const DecodeParams p) {
   constexpr int TB = tile_bytes(FMT);
   constexpr int NJ = MT / 8;           // n8 MMA column blocks
@@ -306,19 +328,25 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   if constexpr (GRP) pdl_wait();
   const int S = p.stages;
   const int M = GRP ? 16 : p.M;  // rows of the stage's activation area
-  // stage: weights | activation slices (M rows of 128 B per k tile) | activation scales
+  // stage: weights | activation slices (M rows of 128 B per k tile) | activation scales;
+  // resident mode: weights only
   const int SCALES_OFF = WBYTES + KS * M * 128;
-  const int STAGE = SCALES_OFF + KS * kAScaleStride * 4;
+  const int STAGE = RA ? WBYTES : SCALES_OFF + KS * kAScaleStride * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t G = gridDim.x, c = blockIdx.x, KT = p.KT;
   const int64_t I = GRP ? (int64_t)p.gtab[kGtP] * p.RT * KT : p.items;
   const int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
 
   float* slots = reinterpret_cast<float*>(smem + (size_t)S * STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE + (size_t)CW * SLOT * 4);
+  // resident mode: activations [KT][M][64] f16 (the pre-pass layout) and scales [KT][8]
+  uint8_t* res = smem + (size_t)S * STAGE + (size_t)CW * SLOT * 4;
+  const size_t res_bytes = RA ? decode_resident_bytes(M, KT) : 0;
+  const uint32_t res_u = smem_u32(res), rscale_u = res_u + (uint32_t)(M * KT * 128);
+  uint64_t* full = reinterpret_cast<uint64_t*>(res + res_bytes);
   uint64_t* empty = full + S;
   const uint32_t ring_u = smem_u32(smem), full_u = smem_u32(full), empty_u = smem_u32(empty);
   const uint32_t pub_u = smem_u32(empty + S);  // consumers -> publisher: partial written
+  const uint32_t aready_u = smem_u32(empty + S + 1);  // resident mode: activations converted
 
   // Stages walk the CTA's items in order; all loop state advances incrementally.
   const int kt_first = (int)(i0 % KT);
@@ -337,6 +365,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       mbar_init(empty_u + 8 * s, CW);
     }
     mbar_init(pub_u, CW);
+    mbar_init(aready_u, 1);
   }
   fence_mbar_init();
   __syncthreads();
@@ -409,6 +438,38 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     }
   }
 
+  if (RA && warp == CW) {
+    // ------------------------------------------------------------- producer (resident)
+    // weights only; the first stages are requested at once, the rest once the consumers
+    // have the activations (weight requests queued ahead would delay the activation loads)
+    if (lane == 0 && !p.withhold) {
+      const uint64_t pol = l2_evict_first_policy();
+      int64_t pos = i0;
+      int kt = kt_first, issued = 0, slot = 0;
+      while (pos < i1) {
+        if (issued == kResidentPrefetch && !mbar_wait_bounded(aready_u, 0, p.wait_ns)) {
+          atomicExch(p.status, 5);
+          break;
+        }
+        if (issued >= S &&
+            !mbar_wait_bounded(empty_u + 8 * slot, (uint32_t)((issued / S - 1) & 1), p.wait_ns)) {
+          atomicExch(p.status, 5);
+          break;
+        }
+        const int n = stage_len(pos, kt);
+        mbar_expect_tx(full_u + 8 * slot, (uint32_t)(n * TB));
+        bulk_g2s(ring_u + slot * STAGE, p.tiles + pos * TB, (uint32_t)(n * TB), full_u + 8 * slot,
+                 pol);
+        pos += n;
+        kt += n;
+        if (kt == KTi) kt = 0;
+        ++issued;
+        if (++slot == S) slot = 0;
+      }
+    }
+    return;
+  }
+
   if (warp == CW) {
     // ------------------------------------------------------------- producer
     if (lane == 0 && !p.withhold) {
@@ -475,6 +536,60 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
 
   // ---------------------------------------------------------------- consumers
   if constexpr (!GRP) pdl_wait();
+  if constexpr (RA) {
+    // The activation conversion of the pre-pass, done here into shared memory: A[m][k]
+    // (bf16) -> A'[kt][m][64] (f16) = A * 2^-p with one power of two p per (token m, 64-wide
+    // k tile kt) from the tile's largest magnitude, scales[kt][m] = 2^p; 16-byte granules
+    // XOR-swizzled by (m & 7).  Eight consecutive threads hold one (m, kt) tile row; the
+    // loop runs the same number of times in every warp (the shuffles need all lanes).
+    const int64_t total = (int64_t)M * KT * 8;
+    const __nv_bfloat16* A = p.A;
+    for (int64_t base = 0; base < total; base += CT) {
+      const int64_t idx = base + threadIdx.x;
+      const bool valid = idx < total;
+      const int gi = (int)(idx & 7);
+      const int64_t r = idx >> 3;
+      const int64_t ktr = r / M;
+      const int m = (int)(r - ktr * M);
+      const int64_t k0 = ktr * 64 + gi * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (valid && k0 < p.K) v = __ldg(reinterpret_cast<const uint4*>(A + m * p.lda + k0));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      int mx = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        mx = max(mx, (int)(w[q] & 0x7FFFu));
+        mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (valid) {
+        int pe = 0;
+        if (mx > 0 && mx <= 0x7F80) {
+          const int e = (mx >> 7) - 127;
+          pe = e - 14;
+          pe = pe < -120 ? -120 : (pe > 113 ? 113 : pe);
+        }
+        const float down = ldexpf(1.0f, -pe);
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(w[q] << 16) * down;
+          const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
+          __half2 h = __floats2half2_rn(lo, hi);
+          o[q] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        st_shared_v4(res_u + (uint32_t)(((ktr * M + m) * 64 + ((gi ^ (m & 7)) * 8)) * 2),
+                     o[0], o[1], o[2], o[3]);
+        if (gi == 0) st_shared_f32(rscale_u + (uint32_t)((ktr * kResScaleStride + m) * 4), ldexpf(1.0f, pe));
+      }
+    }
+    // scales of the token columns past M (read by the fragments of absent tokens)
+    for (int64_t i = threadIdx.x; i < KT * kResScaleStride; i += CT)
+      if ((int)(i % kResScaleStride) >= M) st_shared_f32(rscale_u + (uint32_t)(i * 4), 0.0f);
+    consumer_sync(CT);
+    if (threadIdx.x == 0) mbar_arrive(aready_u);
+  }
   const int jp = warp & 3, kq = warp >> 2;  // row blocks 2jp, 2jp+1; k tiles kq, kq+4
   float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
   // grouped mode: the current problem's token count, output rows and expert factor
@@ -516,7 +631,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       for (int kh = kq; kh < KS; kh += 4) {
         if (kh < n) {
           const uint32_t tb = sbase + kh * TB;
-          const uint32_t ab = sbase + WBYTES + kh * Mc * 128;
+          const uint32_t ab = RA ? res_u + (uint32_t)((kt + kh) * M * 128)
+                                 : sbase + WBYTES + kh * Mc * 128;
           // activation fragments (B operand): token rows g (+8), physical k 16t .. 16t+15
           uint32_t bfr[NJ][4][2];
 #pragma unroll
@@ -540,7 +656,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
 #pragma unroll
           for (int u = 0; u < NJ; ++u) {
             const uint32_t sa =
-                sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
+                RA ? rscale_u + (uint32_t)(((kt + kh) * kResScaleStride + 2 * t + 8 * u) * 4)
+                   : sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
             asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
                          : "=f"(as[u][0]), "=f"(as[u][1])
                          : "r"(sa));
@@ -771,11 +888,11 @@ static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
   return e;
 }
 
-template <int FMT, int MT, int KS, bool GRP = false>
+template <int FMT, int MT, int KS, bool GRP = false, bool RA = false>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   static int done[64] = {0};
-  const size_t smem = decode_smem_bytes(FMT, GRP ? 16 : L.M, KS, L.stages);
-  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP>, (int)smem, done);
+  const size_t smem = decode_smem_bytes(FMT, GRP ? 16 : L.M, KS, L.stages, RA ? L.KT : 0);
+  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP, RA>, (int)smem, done);
   if (e != cudaSuccess) return e;
   DecodeParams p;
   p.tiles = reinterpret_cast<const uint8_t*>(L.packed) + kHeaderBytes;
@@ -805,6 +922,9 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.gbase = reinterpret_cast<const uint8_t*>(L.packed);
   p.expert_bytes = L.expert_bytes;
   p.RT = L.RT;
+  p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
+  p.lda = L.lda;
+  p.K = L.K;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
@@ -816,7 +936,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP>, p);
+  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP, RA>, p);
 }
 
 // ------------------------------------------------------------- grouped pre-pass
@@ -971,6 +1091,17 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) {
   const int mt = decode_mt(L.M);
   cudaError_t e = cudaSuccess;
+  if (L.resident) {  // one kernel: it converts the activations itself
+    if (mt != 8 || L.w4a4) return cudaErrorInvalidValue;
+    if (L.ks == 4)
+      e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 4, false, true>(L, s)
+                            : launch_t<FMT_MX, 8, 4, false, true>(L, s);
+    else
+      e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 8, false, true>(L, s)
+                            : launch_t<FMT_MX, 8, 8, false, true>(L, s);
+    if (launches) *launches = 1;
+    return e;
+  }
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)L.M, (unsigned)((L.KT + kPrepTiles - 1) / kPrepTiles));

@@ -50,15 +50,27 @@ struct DecodeLaunch {
   // NVFP4 activation global)
   int w4a4 = 0;
   float alpha = 1.0f;
+  int resident = 0;  // resident-activation mode (decode_resident_ok; not with w4a4 / grouped)
 };
 int decode_mt(int M);  // 8 or 16
+// Resident-activation decode (small M * K): the decode kernel converts A into shared memory
+// itself; no pre-pass.  The workspace keeps the split-K counters of weights with up to
+// kFixedCounterTiles row tiles in a fixed 64 KB region that no other data overlaps.
+constexpr int kResScaleStride = 8;               // floats per k tile of resident scales
+constexpr int kResidentMaxM = 4;
+constexpr size_t kResidentMaxBytes = 16 * 1024;  // of converted activations (M * K * 2)
+constexpr int64_t kFixedCounterTiles = 16384;
+__host__ __device__ inline size_t decode_resident_bytes(int M, int64_t KT) {
+  return KT ? (size_t)M * (size_t)KT * 128 + (size_t)KT * kResScaleStride * 4 : 0;
+}
+bool decode_resident_ok(int M, int64_t KT, int64_t RT);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
 // Grouped decode: a pre-pass groups the (token, slot) pairs of topk_ids [M][topk] by
 // expert and converts their activations, then the decode kernel runs every problem.
 cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids, int npairs,
                                   int topk, int E, cudaStream_t s, int* launches);
 constexpr int kGroupTableInts = 1 + 3 * 128 + 128 * 16;  // see the decode kernel
-size_t decode_smem_bytes(int fmt, int M, int ks, int stages);
+size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt = 0);
 
 // Prefill tile GEMM (tensor cores), any M.
 struct PrefillLaunch {

@@ -69,7 +69,9 @@ typedef struct {
   int grid;      /* decode: number of CTAs (clamped to [1, 512]); prefill: CTAs (>= 1) */
   int warps;     /* decode: k tiles (of 64) per pipeline stage, 4 or 8 */
   int stages;    /* decode: depth of the CTA's TMA ring, 2..16 */
-  int force_path;/* 1 decode (requires M <= 16), 2 prefill */
+  int force_path;/* 1 decode (requires M <= 16), 2 prefill, 3 decode with the activations
+                    always converted by the pre-pass kernel (small M * K otherwise converts
+                    them inside the decode kernel) */
   int wait_limit_us;   /* limit of every bounded device-side wait, in microseconds
                         * (0 = 2 s); a wait that runs out sets VT_ERR_TIMEOUT in the
                         * workspace status word and the kernel finishes without waiting */

@@ -138,3 +138,32 @@ def test_workspace_reuse_across_shapes():
             ref, _ = oracle.gemm(fmt, Ab, codes, scales, G, W.N)
             check_rows(y.float().cpu().numpy(), ref, what=f"reuse {i} {rep}")
     assert vt.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+@pytest.mark.parametrize("N,K", [(2048, 1024), (600, 992), (1000, 4096), (384, 12288)])
+def test_resident_activations_equal_prepass(fmt, N, K):
+    """Small M * K: the decode kernel converts the activations into shared memory itself (one
+    launch); forcing the pre-pass (force_path 3, two launches) must give the same bits, and
+    both match the oracle.  Rows include zeros and magnitudes far apart."""
+    W, codes, scales, G = _packed(fmt, N, K, synth.tensor_id(64, fmt, 1, N + K))
+    ws = W.new_workspace(16)
+    for M in (1, 2, 3, 4):
+        x = synth.bf16_bits_to_f32(make_acts(synth.tensor_id(64, fmt, 2, M * 100 + K), M, K))
+        x = x.astype(np.float64)
+        if M >= 3:
+            x[1] = 0.0
+            x[2][: K // 3] *= 1e20
+        Ab = torch.tensor(x).to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        A = bf16_dev(Ab)
+        y_res = vt.w4a16_gemm(A, W, workspace=ws)
+        launches_res = W.stats()["launches"]
+        y_pre = vt.w4a16_gemm(A, W, workspace=ws, opts={"force_path": 3})
+        launches_pre = W.stats()["launches"]
+        torch.cuda.synchronize()
+        resident = M * ((K + 63) // 64) * 128 <= 16 * 1024
+        assert launches_res == (1 if resident else 2) and launches_pre == 2, (M, launches_res)
+        assert np.array_equal(bf16_host_bits(y_res), bf16_host_bits(y_pre)), f"M={M}"
+        ref, _ = oracle.gemm(fmt, Ab, codes, scales, G, N)
+        check_rows(y_res.float().cpu().numpy(), ref, what=f"resident fmt={fmt} M={M} N={N} K={K}")
+    assert vt.workspace_status(ws) == 0
