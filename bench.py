@@ -303,6 +303,57 @@ def _calls(w: Workload, sets):
     return calls
 
 
+def _dequant_act(A, fmt: int, alpha: float):
+    """The W4A4 arm's quantised activations as values, from the library's activation
+    quantiser (codes and scales) decoded here with PyTorch."""
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    codes, scales = vt.quantize_act(A, fmt, alpha)
+    c = torch.stack([codes & 0xF, codes >> 4], dim=-1).reshape(A.shape[0], -1).long()
+    table = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=A.device)
+    v = table[c & 7] * torch.where((c & 8) != 0, -1.0, 1.0)
+    if fmt == NVFP4:
+        s = scales.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=1)
+        return (v * s) * alpha
+    s = torch.pow(2.0, scales.float() - 127.0).repeat_interleave(32, dim=1)
+    return v * s
+
+
+def self_check(w: Workload, sets, calls, A, C, a4, n_cols: int = 256):
+    """The timed step's outputs against a PyTorch fp64 reference on sampled output columns:
+    A (or the W4A4 arm's quantised A) times the library's dequantised weight
+    (vt_fp4_dequant, itself checked bit for bit by the tests).  Each output buffer holds
+    the last call written to it."""
+    import torch
+    if w.kind not in ("decode", "prefill"):
+        return {"cases": 0, "note": f"{w.kind}: outputs are checked by the test suite"}
+    last = {}
+    for c, layer, pi, M in calls:
+        last[(M, w.projs[pi].N)] = (c, layer, pi)
+    gen = torch.Generator()
+    gen.manual_seed(7)
+    worst, deq = 0.0, {}
+    for (M, N), (c, layer, pi) in last.items():
+        p = w.projs[pi]
+        if (c, layer, pi) not in deq:
+            deq = {(c, layer, pi): sets[c][layer][pi].dequant()}  # fp32 [N][K]; one at a time
+        Wd = deq[(c, layer, pi)]
+        cols = torch.unique(torch.cat([torch.randperm(N, generator=gen)[:n_cols],
+                                       torch.tensor([0, N - 1])])).to(Wd.device)
+        a = _dequant_act(A[(M, p.K)], w.fmt, a4) if a4 is not None else A[(M, p.K)].float()
+        ref = a.double() @ Wd[cols].double().T
+        got = C[(M, N)][:, cols].double()
+        den = ref.abs().amax(dim=1)
+        err = (got - ref).abs().amax(dim=1)
+        ratio = torch.where(den > 0, err / den.clamp_min(1e-300), err * 1e30)
+        worst = max(worst, float(ratio.max()))
+    del deq
+    torch.cuda.synchronize()
+    return {"cases": len(last), "cols_per_case": n_cols, "max_err_over_row_max": worst,
+            "tol": 4e-3, "ok": bool(worst <= 4e-3),
+            "reference": "PyTorch fp64: (quantised) A times the library's dequantised weight"}
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
@@ -461,6 +512,8 @@ def run_gpu(args, rank: int, world: int):
         ms_total = float(tt.item())
     ms_step = ms_total / args.steps
     value = _rate(w, step_bytes * world, ms_step * 1e-3)
+    # the outputs of the timed graph, checked before anything else runs on them
+    check = self_check(w, sets, calls, A, C, w.extra.get("w4a4"))
 
     # per-call durations: a second graph with an event record node around every call (the
     # event nodes break the overlap between calls, so these durations are slightly larger
@@ -539,6 +592,7 @@ def run_gpu(args, rank: int, world: int):
         "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "copies": copies,
         "calls_per_step": n_calls, "ws_status": ws_status, "unfused": unfused,
+        "self_check": check,
     }
 
 
@@ -840,7 +894,8 @@ def main():
                        calls_per_step=r["calls_per_step"]),
         "roofline": {"bound": "tensor" if prefill else "hbm",
                      "kernel": ("k_prefill (+ k_prep_rows, one GEMM call)" if prefill else
-                                "k_decode (+ k_prep_a, one GEMM call)"),
+                                "k_decode (+ k_prep_a where a pre-pass converts the "
+                                "activations; one GEMM call)"),
                      "achieved": round(r["achieved"], 1), "peak": peak, "unit": w.unit,
                      "frac": round(r["achieved"] / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
@@ -850,6 +905,7 @@ def main():
         "gpu_launches": r["gpu_launches"],
         "clocks": r["clocks"],
         "workspace_status": r["ws_status"],
+        "self_check": r["self_check"],
     }
     if r.get("unfused"):
         line["unfused"] = r["unfused"]
@@ -860,6 +916,10 @@ def main():
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+    if not r["self_check"].get("ok", True) or r["ws_status"]:
+        sys.stderr.write("bench: the timed outputs failed the self-check or the workspace "
+                         "reported an error; the numbers above are not valid\n")
+        sys.exit(3)
 
 
 if __name__ == "__main__":

@@ -2,10 +2,11 @@
 the tolerance rule.  Tolerance (per output row m, i.e. per token):
     max_n |y_gpu - y_oracle| <= 4e-3 * max_n |y_oracle|
 with y_oracle the fp32 oracle sum and y_gpu the library's bf16 output; a row whose oracle
-maximum is 0 must be exactly 0.  The bound comes from the arithmetic: the bf16 output alone
-rounds by up to 2^-9 (1.95e-3) of each value, and the fp32 sums of both sides differ by far
-less; it is the bound the workload definition states, and the pages measured 3.8e-3 for the
-same comparison ("native MXFP4 keep-quant + Qwen e2e", PR #38, commit "W3 device unit
+maximum is 0 must be exactly 0.  The bound comes from the arithmetic: rounding to bf16 (8
+significant bits, ties to even) moves a value by up to half an ulp, 2^-8 (3.9e-3) of the
+value just above a power of two, and the fp32 sums of both sides differ by far less; it is
+the bound the workload definition states, and the pages measured 3.8e-3 for the same
+comparison ("native MXFP4 keep-quant + Qwen e2e", PR #38, commit "W3 device unit
 gate")."""
 from __future__ import annotations
 
