@@ -100,7 +100,8 @@ class PackedWeight:
         return out.value
 
     def new_workspace(self, M_max: int) -> torch.Tensor:
-        """A zeroed workspace for calls with M <= M_max (zero once; it self-resets)."""
+        """A zeroed workspace for calls with M <= M_max (zero once; the library keeps its
+        counters usable from call to call, for this or any other weight it is large enough for)."""
         return torch.zeros(self.workspace_bytes(M_max), dtype=torch.uint8,
                            device=self.packed.device)
 

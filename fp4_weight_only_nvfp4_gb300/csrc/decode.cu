@@ -5,17 +5,19 @@
 // "MXFP4 decode-graph + gate_up FUSION" (PR #54), "Step 3" (the CTA count per SM decides the
 // residual; a regrouped fp32 reduce moves bf16 ULPs, so reductions here have a fixed
 // order); "re-verify 27B NVFP4" (PR #178): a split-K workspace whose spin-locks were not
-// zeroed hung the GPU, so this kernel has no spin-locks (the last CTA to arrive reduces).
+// zeroed hung the GPU, so every wait here is bounded and the counters are zeroed by each
+// call's pre-pass (or left at zero by the previous call's reducers).
 //
-// Design (GB300): one persistent CTA per SM with 16 consumer warps and one producer warp.
-// Work items are (128-row tile, 64-k tile) pairs in row-tile-major order; CTA c owns items
-// [c*I/G, (c+1)*I/G).  The producer thread streams the CTA's items through a ring of
-// shared-memory stages with 1-D TMA bulk copies (up to KS consecutive k tiles of weights
-// per copy, plus the matching activation slices and scales).  Consumers dequantise in
-// registers (E2M1 -> f16 by cvt, times the group scale in f16, both exact) and accumulate
-// with m16n8k16 MMAs in fp32.  At the end of each row-tile segment the warps' partial sums
-// are added in a fixed order through shared memory; a row tile shared by several CTAs is
-// finished by the last CTA to arrive, which adds the CTAs' partials in CTA order.
+// Design (GB300): one persistent CTA per SM with 16 consumer warps, one producer warp and
+// one publisher warp.  Work items are (128-row tile, 64-k tile) pairs in row-tile-major
+// order; CTA c owns items [c*I/G, (c+1)*I/G).  The producer thread streams the CTA's items
+// through a ring of shared-memory stages with 1-D TMA bulk copies (up to KS consecutive k
+// tiles of weights per copy, plus the matching activation slices and scales, unless the
+// activations are resident).  Consumers dequantise in registers (E2M1 -> f16 by cvt, times
+// the group scale in f16, both exact) and accumulate with m16n8k16 MMAs in fp32.  At the
+// end of each row-tile segment the warps' partial sums are added in a fixed order through
+// shared memory; a row tile shared by several CTAs is finished by its first contributor
+// (see k_decode), which adds the others' partials in CTA order.
 #include <cuda_bf16.h>
 
 #include "actq.cuh"
