@@ -354,6 +354,22 @@ def self_check(w: Workload, sets, calls, A, C, a4, n_cols: int = 256):
             "reference": "PyTorch fp64: (quantised) A times the library's dequantised weight"}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x: replicas run side by side, so the job's timed region
+    lasts as long as its slowest rank (dist None: one process)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(w: Workload, units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return _rate(w, units_per_rank * world, seconds)
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
@@ -506,12 +522,9 @@ def run_gpu(args, rank: int, world: int):
     load_for(0.6)
     clocks = sampler.stop()
     ms_total = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
-    value = _rate(w, step_bytes * world, ms_step * 1e-3)
+    value = job_rate(w, step_bytes, world, ms_step * 1e-3)
     # the outputs of the timed graph, checked before anything else runs on them
     check = self_check(w, sets, calls, A, C, w.extra.get("w4a4"))
 
@@ -577,7 +590,7 @@ def run_gpu(args, rank: int, world: int):
         stream.synchronize()
         ums = u0.elapsed_time(u1) / args.steps
         unfused = {"ms_per_step": round(ums, 5),
-                   "value": round(_rate(w, step_bytes * world, ums * 1e-3), 2),
+                   "value": round(job_rate(w, step_bytes, world, ums * 1e-3), 2),
                    "what": ("same calls with bf16 logits written and torch.argmax per call" if greedy
                             else "gate_up writes [M][2I]; torch SiLU-and-multiply; down")}
     # the step runs nothing but GEMM calls: their average throughput over the timed region
@@ -669,12 +682,9 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
         t1.record(stream)
     stream.synchronize()
     ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_step = ms / args.steps
-    return {"value": round(_rate(w, step_bytes * world, ms_step * 1e-3), 2), "unit": w.unit,
+    return {"value": round(job_rate(w, step_bytes, world, ms_step * 1e-3), 2), "unit": w.unit,
             "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -711,6 +721,8 @@ def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, 
         for _ in range(3):
             graph.replay()
     stream.synchronize()
+    if dist:
+        dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
@@ -718,8 +730,8 @@ def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, 
             graph.replay()
         t1.record(stream)
     stream.synchronize()
-    ms_step = t0.elapsed_time(t1) / args.steps
-    return {"value": round(_rate(w, step_bytes * world, ms_step * 1e-3), 2), "unit": w.unit,
+    ms_step = max_over_ranks(t0.elapsed_time(t1), dist, dev) / args.steps
+    return {"value": round(job_rate(w, step_bytes, world, ms_step * 1e-3), 2), "unit": w.unit,
             "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -855,7 +867,7 @@ def main():
         ms = statistics.median(d for _, d in per_step) * 1e3
         line = {"impl": "reference", "metric": PREFILL_METRIC if w.kind == "prefill" else METRIC,
                 "value": round(value, 4), "unit": w.unit,
-                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": dict(config, l2="CPU oracle; no GPU"),
