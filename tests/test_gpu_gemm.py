@@ -167,3 +167,19 @@ def test_resident_activations_equal_prepass(fmt, N, K):
         ref, _ = oracle.gemm(fmt, Ab, codes, scales, G, N)
         check_rows(y_res.float().cpu().numpy(), ref, what=f"resident fmt={fmt} M={M} N={N} K={K}")
     assert vt.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+def test_resident_activations_strided(fmt):
+    """The in-kernel activation conversion reads A with its own leading dimension."""
+    N, K = 640, 1024
+    W, codes, scales, G = _packed(fmt, N, K, synth.tensor_id(65, fmt, 1))
+    for M in (1, 2):
+        Ab = make_acts(synth.tensor_id(65, fmt, 2, M), M, K)
+        big = torch.full((M, K + 72), 3.0, dtype=torch.bfloat16, device="cuda")
+        big[:, :K] = bf16_dev(Ab)
+        y = vt.w4a16_gemm(big[:, :K], W)
+        torch.cuda.synchronize()
+        assert W.stats()["launches"] == 1  # resident mode
+        ref, _ = oracle.gemm(fmt, Ab, codes, scales, G, N)
+        check_rows(y.float().cpu().numpy(), ref, what=f"resident strided M={M}")
