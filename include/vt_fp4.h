@@ -246,7 +246,9 @@ vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t lda, vt_fp
                                     void* C, int64_t ldc, vt_stream_t s);
 
 /* Reads the workspace status word (synchronises `s`): *status = VT_OK, or VT_ERR_TIMEOUT
- * if a bounded device-side wait gave up during an earlier call; the word is then cleared. */
+ * if a bounded device-side wait gave up during an earlier call; the word is then cleared.
+ * After VT_ERR_TIMEOUT zero the whole workspace again before reusing it: a call that gave up
+ * may leave split-K arrival counts behind. */
 vt_status vt_fp4_workspace_status(void* workspace, vt_stream_t s, int* status);
 
 /* Host-side record of the last GEMM launched on W. */
