@@ -38,9 +38,9 @@ namespace {
 constexpr uint64_t kPfWaitNs = 2000000000ull;  // drains of copies and MMAs in flight
 constexpr int kBM = 128;          // tokens per tile (MMA M)
 constexpr int kBN = 256;          // weight rows per tile (MMA N): two packed row tiles
-constexpr int kAStages = 4;
+constexpr int kAStages = 6;
 constexpr int kPStages = 4;
-constexpr int kBStages = 3;
+constexpr int kBStages = 2;
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kPfThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
