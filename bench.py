@@ -73,8 +73,7 @@ class Workload:
     projs: list
     layers: int = 1
     note: str = ""
-    kind: str = "decode"   # "decode"/"greedy"/"mlp_silu"/"mlp_fused"/"moe": HBM GB/s;
-    #                        "prefill": TFLOP/s
+    kind: str = "decode"   # "decode"/"greedy"/"mlp_silu"/"moe": HBM GB/s; "prefill": TFLOP/s
     extra: dict = field(default_factory=dict)
 
     @property
@@ -120,13 +119,6 @@ WORKLOADS = {
          Proj("down", 12288, N=4096, wid=2, role=13)], kind="mlp_silu",
         note="MXFP4 dense MLP decode as a chain: gate_up (paired) with the SiLU-and-multiply "
              "epilogue writes act [M][12288], down reads it; M in {1,2,4,8}"),
-    "mxfp4_mlp_fused_12288x4096": Workload(
-        "mxfp4_mlp_fused_12288x4096", 2, MXFP4, [1, 2, 4, 8],
-        [Proj("gate_up", 4096, I=12288, wid=2, role=ROLE_GATE),
-         Proj("down", 12288, N=4096, wid=2, role=13)], kind="mlp_fused",
-        note="MXFP4 dense MLP decode in one GEMM kernel per MLP: gate_up (paired, N=2x12288 "
-             "K=4096) with the SiLU-and-multiply epilogue, then down (N=4096 K=12288) on "
-             "its output behind a grid barrier; M in {1,2,4,8}"),
     "nvfp4_moe_128x1536x2048": Workload(
         "nvfp4_moe_128x1536x2048", 7, NVFP4, [1, 2, 4, 8],
         [Proj("experts", 2048, N=1536, wid=7)], kind="moe",
@@ -272,7 +264,7 @@ def _build_weights(w: Workload, copies: int, dev):
                         halves.append((c_, s_, float(g_.item())))
                         del Wb
                     ws.append(vt.PackedWeight.gate_up(halves[0], halves[1], w.fmt, p.I, p.K,
-                                                      paired=(w.kind in ("mlp_silu", "mlp_fused"))))
+                                                      paired=(w.kind == "mlp_silu")))
                 else:
                     Wb = (torch.randn((p.N, p.K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
                     c_, s_, g_ = vt.quantize(Wb, w.fmt)
@@ -333,8 +325,6 @@ def self_check(w: Workload, sets, calls, A, C, a4, n_cols: int = 256):
     (vt_fp4_dequant, itself checked bit for bit by the tests).  Each output buffer holds
     the last call written to it."""
     import torch
-    if w.kind == "mlp_fused":
-        return _self_check_mlp(w, sets, calls, A, C, n_cols)
     if w.kind not in ("decode", "prefill"):
         return {"cases": 0, "note": f"{w.kind}: outputs are checked by the test suite"}
     last = {}
@@ -362,41 +352,6 @@ def self_check(w: Workload, sets, calls, A, C, a4, n_cols: int = 256):
     return {"cases": len(last), "cols_per_case": n_cols, "max_err_over_row_max": worst,
             "tol": 4e-3, "ok": bool(worst <= 4e-3),
             "reference": "PyTorch fp64: (quantised) A times the library's dequantised weight"}
-
-
-def _self_check_mlp(w: Workload, sets, calls, A, C, n_cols: int):
-    """The fused MLP's timed outputs: per M, the last MLP written, against PyTorch fp64 --
-    silu(gate) * up from the dequantised paired gate_up, rounded to bf16 as the kernel
-    rounds it, times the dequantised down weight on sampled columns."""
-    import torch
-    gate, down = w.projs[0], w.projs[1]
-    last = {}
-    for c, layer, pi, M in calls:
-        if w.projs[pi].fused:
-            last[M] = (c, layer)
-    gen = torch.Generator()
-    gen.manual_seed(7)
-    worst = 0.0
-    for M, (c, layer) in last.items():
-        Wg = sets[c][layer][0].dequant()  # fp32 [2I][K]: gate rows, then up rows
-        y = A[(M, gate.K)].double() @ Wg.double().T
-        del Wg
-        act = (torch.nn.functional.silu(y[:, :gate.I]) * y[:, gate.I:]).to(torch.bfloat16)
-        Wd = sets[c][layer][1].dequant()  # fp32 [N][I]
-        cols = torch.unique(torch.cat([torch.randperm(down.N, generator=gen)[:n_cols],
-                                       torch.tensor([0, down.N - 1])])).to(Wd.device)
-        ref = act.double() @ Wd[cols].double().T
-        del Wd
-        got = C[(M, down.N)][:, cols].double()
-        den = ref.abs().amax(dim=1)
-        err = (got - ref).abs().amax(dim=1)
-        ratio = torch.where(den > 0, err / den.clamp_min(1e-300), err * 1e30)
-        worst = max(worst, float(ratio.max()))
-    torch.cuda.synchronize()
-    return {"cases": len(last), "cols_per_case": n_cols, "max_err_over_row_max": worst,
-            "tol": 4e-3, "ok": bool(worst <= 4e-3),
-            "reference": "PyTorch fp64: silu(gate) * up (bf16) from the dequantised gate_up, "
-                         "times the dequantised down weight"}
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -434,9 +389,6 @@ def run_gpu(args, rank: int, world: int):
         wsz = sets[0][0][0].moe_workspace(Mmax, w.extra["topk"]).numel()
     else:
         wsz = max(Wt.workspace_bytes(Mmax) for layer_sets in sets for ws in layer_sets for Wt in ws)
-    if w.kind == "mlp_fused":
-        wsz = max([wsz] + [vt.mlp_workspace_bytes(ws[0], ws[1]) for layer_sets in sets
-                           for ws in layer_sets])
     ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(12345 + rank)
@@ -466,8 +418,7 @@ def run_gpu(args, rank: int, world: int):
     n_calls = len(calls)
 
     greedy = w.kind == "greedy"
-    fused_mlp = w.kind == "mlp_fused"
-    silu = w.kind == "mlp_silu" or fused_mlp
+    silu = w.kind == "mlp_silu"
     a4 = w.extra.get("w4a4")  # the W4A4 arm: the activation global
     # the MLP chain: gate_up writes act [M][I], down reads it
     I_mlp = max((p.I for p in w.projs if p.fused), default=0)
@@ -475,15 +426,6 @@ def run_gpu(args, rank: int, world: int):
 
     def one_call(c, layer, pi, M, unfused=False):
         p = w.projs[pi]
-        if fused_mlp and not unfused:
-            # the whole MLP in the gate_up call (one GEMM kernel); the down call has no work
-            if p.fused:
-                q = w.projs[pi + 1]
-                vt.w4a16_mlp(A[(M, p.K)], sets[c][layer][pi], sets[c][layer][pi + 1],
-                             out=C[(M, q.N)], workspace=ws, stream=stream)
-            return
-        if fused_mlp:  # the unfused comparison: the same MLP as two calls
-            unfused = False
         if moe:
             vt.w4a16_gemm_moe(A[(M, p.K)], sets[c][layer][pi], route[(c, M)], out=Cm[M],
                               workspace=ws, stream=stream)
@@ -531,8 +473,7 @@ def run_gpu(args, rank: int, world: int):
     with torch.cuda.stream(stream):
         for c, layer, pi, M in calls:
             one_call(c, layer, pi, M)
-            if not (fused_mlp and not w.projs[pi].fused):
-                launches_per_step += sets[c][layer][pi].stats()["launches"]
+            launches_per_step += sets[c][layer][pi].stats()["launches"]
     stream.synchronize()
 
     # the timed step: one CUDA graph of all the step's calls, back to back (consecutive
@@ -617,11 +558,11 @@ def run_gpu(args, rank: int, world: int):
     agg = {}
     for i, (c, layer, pi, M) in enumerate(calls):
         p = w.projs[pi]
-        key = ("mlp" if fused_mlp else p.name, M)
+        key = (p.name, M)
         b = moe_bytes[(c, M)] if moe else _work(w, p.N, p.K, M)
         a = agg.setdefault(key, [0.0, 0, 0])
         a[0] += durs[i]
-        a[1] += 0 if (fused_mlp and not p.fused) else 1  # fused MLP: one call per MLP
+        a[1] += 1
         a[2] += b
     for (name, M), (ms, n, b) in agg.items():
         us = ms * 1e3 / n
@@ -630,8 +571,7 @@ def run_gpu(args, rank: int, world: int):
     kernel_ms = sum(durs)
     unfused = None
     if greedy or silu:
-        # the same step with the logits written and a separate argmax per call (MLP: the
-        # unfused chain; the fused MLP: the same MLP as two calls)
+        # the same step with the logits written and a separate argmax per call
         g3 = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             for _ in range(2):
@@ -652,8 +592,6 @@ def run_gpu(args, rank: int, world: int):
         unfused = {"ms_per_step": round(ums, 5),
                    "value": round(job_rate(w, step_bytes, world, ums * 1e-3), 2),
                    "what": ("same calls with bf16 logits written and torch.argmax per call" if greedy
-                            else "two calls per MLP: gate_up with the SiLU-and-multiply "
-                                 "epilogue, then down" if fused_mlp
                             else "gate_up writes [M][2I]; torch SiLU-and-multiply; down")}
     # the step runs nothing but GEMM calls: their average throughput over the timed region
     achieved = _rate(w, step_bytes, ms_step * 1e-3)
@@ -666,8 +604,7 @@ def run_gpu(args, rank: int, world: int):
         "value": value, "ms_per_step": ms_step, "step_bytes": step_bytes, "clocks": clocks,
         "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "copies": copies,
-        "calls_per_step": (sum(1 for _, _, pi, _ in calls if w.projs[pi].fused) if fused_mlp
-                           else n_calls), "ws_status": ws_status, "unfused": unfused,
+        "calls_per_step": n_calls, "ws_status": ws_status, "unfused": unfused,
         "self_check": check,
     }
 
@@ -683,8 +620,7 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
             hC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16).pin_memory()
             dC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
     greedy = w.kind == "greedy"
-    fused_mlp = w.kind == "mlp_fused"
-    silu = w.kind == "mlp_silu" or fused_mlp
+    silu = w.kind == "mlp_silu"
     a4 = w.extra.get("w4a4")
     hT = {M: torch.empty(M, dtype=torch.int32).pin_memory() for M in w.Ms}
     if silu:  # the MLP chain: host input of gate_up in, host output of down out
@@ -699,14 +635,6 @@ def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
     def issue():
         for c, layer, pi, M in calls:
             p = w.projs[pi]
-            if fused_mlp:
-                if p.fused:
-                    q = w.projs[pi + 1]
-                    dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
-                    vt.w4a16_mlp(dA[(M, p.K)], sets[c][layer][pi], sets[c][layer][pi + 1],
-                                 out=dC[(M, q.N)], workspace=ws, stream=stream)
-                    hC[(M, q.N)].copy_(dC[(M, q.N)], non_blocking=True)
-                continue
             if silu:
                 if p.fused:
                     dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
@@ -978,8 +906,6 @@ def main():
                        calls_per_step=r["calls_per_step"]),
         "roofline": {"bound": "tensor" if prefill else "hbm",
                      "kernel": ("k_prefill (+ k_prep_rows, one GEMM call)" if prefill else
-                                "k_decode in the fused MLP mode (+ k_prep_a; one MLP per "
-                                "launch)" if w.kind == "mlp_fused" else
                                 "k_decode (+ k_prep_a where a pre-pass converts the "
                                 "activations; one GEMM call)"),
                      "achieved": round(r["achieved"], 1), "peak": peak, "unit": w.unit,

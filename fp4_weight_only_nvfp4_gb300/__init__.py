@@ -18,8 +18,7 @@ NVFP4, MXFP4 = 0, 1
 GROUP = {NVFP4: 16, MXFP4: 32}
 
 __all__ = ["NVFP4", "MXFP4", "GROUP", "PackedWeight", "w4a16_gemm", "w4a16_gemm_noalloc",
-           "w4a16_gemm_silu_mul", "w4a16_gemm_greedy", "w4a16_gemm_moe", "w4a16_mlp",
-           "mlp_workspace", "w4a4_gemm", "quantize_act", "quantize", "prepack_bytes",
+           "quantize", "prepack_bytes",
            "workspace_status", "VtError", "algorithmic_bytes"]
 
 
@@ -271,42 +270,6 @@ def w4a16_gemm_silu_mul(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | No
     check(lib().vt_fp4_w4a16_gemm_silu_mul(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
                                            out.stride(0), _ptr(workspace), workspace.numel(),
                                            _stream(stream)), "vt_fp4_w4a16_gemm_silu_mul")
-    return out
-
-
-def mlp_workspace_bytes(gate_up: PackedWeight, down: PackedWeight) -> int:
-    out = ctypes.c_size_t(0)
-    check(lib().vt_fp4_mlp_workspace_bytes(gate_up.handle, down.handle, ctypes.byref(out)),
-          "vt_fp4_mlp_workspace_bytes")
-    return out.value
-
-
-def mlp_workspace(gate_up: PackedWeight, down: PackedWeight) -> torch.Tensor:
-    """A zeroed workspace for w4a16_mlp on these two weights (any M <= 16)."""
-    return torch.zeros(mlp_workspace_bytes(gate_up, down), dtype=torch.uint8,
-                       device=gate_up.packed.device)
-
-
-def w4a16_mlp(A: torch.Tensor, gate_up: PackedWeight, down: PackedWeight,
-              out: torch.Tensor | None = None, act: torch.Tensor | None = None,
-              workspace: torch.Tensor | None = None, stream=None,
-              opts: dict | None = None) -> torch.Tensor:
-    """Fused MLP decode (M <= 16): out[M, N] = down(silu(gate) * up) with a paired gate_up
-    weight, in one GEMM kernel; ``act`` (optional, bf16 [M, I]) receives silu(gate) * up.
-    See vt_fp4_w4a16_mlp in include/vt_fp4.h."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != gate_up.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
-    M = A.shape[0]
-    if out is None:
-        out = torch.empty((M, down.N), dtype=torch.bfloat16, device=A.device)
-    if workspace is None:
-        workspace = mlp_workspace(gate_up, down)
-    o = _opts(opts)
-    check(lib().vt_fp4_w4a16_mlp(_ptr(A), M, A.stride(0), gate_up.handle, down.handle,
-                                 _ptr(act), act.stride(0) if act is not None else 0, _ptr(out),
-                                 out.stride(0), _ptr(workspace), workspace.numel(),
-                                 _stream(stream), ctypes.byref(o) if o else None),
-          "vt_fp4_w4a16_mlp")
     return out
 
 

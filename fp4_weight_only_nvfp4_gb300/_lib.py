@@ -40,9 +40,6 @@ SIGNATURES = {
                                             ctypes.c_int, _I64, _I64, _P, _SZ, _P,
                                             ctypes.POINTER(_P)]),
     "vt_fp4_w4a16_gemm_silu_mul": (_ST, [_P, _I64, _I64, _P, _P, _I64, _P, _SZ, _P]),
-    "vt_fp4_mlp_workspace_bytes": (_ST, [_P, _P, ctypes.POINTER(_SZ)]),
-    "vt_fp4_w4a16_mlp": (_ST, [_P, _I64, _I64, _P, _P, _P, _I64, _P, _I64, _P, _SZ, _P,
-                               ctypes.POINTER(GemmOpts)]),
     "vt_fp4_prepack_grouped_bytes": (_ST, [ctypes.c_int, _I64, _I64, _I64, ctypes.POINTER(_SZ)]),
     "vt_fp4_prepack_grouped": (_ST, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _SZ, _P,
                                      ctypes.POINTER(_P)]),

@@ -110,29 +110,6 @@ MoeLayout moe_layout(const vt_fp4_weight_s* W, int64_t npairs) {
   return L;
 }
 
-// Workspace of the fused MLP decode (vt_fp4_w4a16_mlp), independent of M (<= 16): status
-// word, the split-K counters of both GEMMs (gate_up's row tiles, then down's) followed by the
-// grid-barrier counter, and per GEMM its activation scales, f16 activations and split-K
-// partials.  The down projection's activations are written by the gate_up epilogues.
-struct MlpLayout {
-  size_t counters, ascale0, ap0, partials0, ascale1, ap1, partials1, total;
-};
-
-MlpLayout mlp_layout(const vt_fp4_weight_s* Wg, const vt_fp4_weight_s* Wd) {
-  MlpLayout L;
-  const size_t part = (size_t)kMaxDecodeGrid * 2 * 16 * 128 * 4;
-  L.counters = 256;
-  const size_t nctr = (size_t)(Wg->RT + Wd->RT + 1);
-  L.ascale0 = up256(L.counters + (nctr > (size_t)kFixedCounterTiles ? nctr : kFixedCounterTiles) * 4);
-  L.ap0 = up256(L.ascale0 + (size_t)Wg->KT * 16 * 4);
-  L.partials0 = up256(L.ap0 + (size_t)16 * Wg->KT * kTileK * 2);
-  L.ascale1 = up256(L.partials0 + part);
-  L.ap1 = up256(L.ascale1 + (size_t)Wd->KT * 16 * 4);
-  L.partials1 = up256(L.ap1 + (size_t)16 * Wd->KT * kTileK * 2);
-  L.total = up256(L.partials1 + part);
-  return L;
-}
-
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -589,127 +566,6 @@ vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_f
     return fail(VT_ERR_INVALID_ARG,
                 "the SiLU-and-multiply epilogue needs a weight from vt_fp4_prepack_gate_up_paired");
   return gemm_impl(A, M, lda, W, C, ldc, workspace, ws_bytes, s, nullptr, nullptr, nullptr, true);
-}
-
-vt_status vt_fp4_mlp_workspace_bytes(vt_fp4_handle gate_up, vt_fp4_handle down, size_t* bytes) {
-  if (vt_status st = check_handle(gate_up)) return st;
-  if (vt_status st = check_handle(down)) return st;
-  if (!bytes) return fail(VT_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = mlp_layout(gate_up, down).total;
-  return VT_OK;
-}
-
-vt_status vt_fp4_w4a16_mlp(const void* A, int64_t M, int64_t lda, vt_fp4_handle gate_up,
-                           vt_fp4_handle down, void* act, int64_t ld_act, void* C, int64_t ldc,
-                           void* workspace, size_t ws_bytes, vt_stream_t s,
-                           const vt_fp4_gemm_opts* opts) {
-  if (vt_status st = check_handle(gate_up)) return st;
-  if (vt_status st = check_handle(down)) return st;
-  vt_fp4_weight_s* Wg = gate_up;
-  vt_fp4_weight_s* Wd = down;
-  if (Wg->E > 1 || Wd->E > 1)
-    return fail(VT_ERR_INVALID_ARG, "a grouped weight serves vt_fp4_w4a16_gemm_moe");
-  if (Wg->layout != kLayoutPaired)
-    return fail(VT_ERR_INVALID_ARG, "gate_up must come from vt_fp4_prepack_gate_up_paired");
-  if (Wd->layout != kLayoutRows)
-    return fail(VT_ERR_INVALID_ARG, "down must be a plain weight (vt_fp4_prepack)");
-  if (Wg->fmt != Wd->fmt) return fail(VT_ERR_INVALID_ARG, "gate_up and down differ in format");
-  if (Wd->K != Wg->seg_split)
-    return fail(VT_ERR_INVALID_ARG, "down has K=%lld, the gate_up intermediate size is %lld",
-                (long long)Wd->K, (long long)Wg->seg_split);
-  if (M < 0 || M > 16) return fail(VT_ERR_INVALID_ARG, "M must be in [0, 16] (got %lld)", (long long)M);
-  if (M == 0) return VT_OK;
-  if (!A || !C || !workspace) return fail(VT_ERR_INVALID_ARG, "A, C and workspace must be set");
-  if (lda < Wg->K || ldc < Wd->N || (act && ld_act < Wg->seg_split))
-    return fail(VT_ERR_INVALID_ARG, "lda (%lld) must be >= K, ldc (%lld) >= N of down and "
-                "ld_act (%lld) >= the intermediate size", (long long)lda, (long long)ldc,
-                (long long)ld_act);
-  if (!aligned(A, 16) || lda % 8)
-    return fail(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda %% 8 == 0");
-  if (!aligned(C, 4) || ldc % 2 || (act && (!aligned(act, 4) || ld_act % 2)))
-    return fail(VT_ERR_MISALIGNED, "C and act must be 4-byte aligned, ldc and ld_act even");
-  if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
-  if (Wg->K > 110000 || Wd->K > 110000) return fail(VT_ERR_UNSUPPORTED, "K > 110000 is not supported");
-  if (opts && (opts->force_path || (opts->warps && opts->warps != 8)))
-    return fail(VT_ERR_INVALID_ARG, "the fused MLP runs the decode path with 8 k tiles per stage");
-  const MlpLayout L = mlp_layout(Wg, Wd);
-  if (ws_bytes < L.total)
-    return fail(VT_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, L.total);
-  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  const int ks = 8;
-  int stages = (opts && opts->stages) ? opts->stages : 0;
-  if (!stages) {
-    stages = 6;
-    while (stages > 2 && decode_smem_bytes(Wg->fmt, (int)M, ks, stages, 0, true) > 224 * 1024) --stages;
-  }
-  if (stages < 2 || stages > 16) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 16]");
-  if (decode_smem_bytes(Wg->fmt, (int)M, ks, stages, 0, true) > 224 * 1024)
-    return fail(VT_ERR_INVALID_ARG, "stage width x stages exceed shared memory");
-  // every CTA must be resident at once (the grid barrier): one CTA per SM at most
-  const int64_t items0 = Wg->RT * Wg->KT, items1 = Wd->RT * Wd->KT;
-  const int64_t sms = sm_count();
-  int64_t grid = sms;
-  if (opts && opts->grid) {
-    if (opts->grid > sms)
-      return fail(VT_ERR_INVALID_ARG, "grid %d exceeds the %lld SMs (all CTAs must be resident)",
-                  opts->grid, (long long)sms);
-    grid = opts->grid;
-  } else {
-    const int64_t fewest = items0 < items1 ? items0 : items1;
-    if (grid > cdiv(fewest, 2 * ks)) grid = cdiv(fewest, 2 * ks);
-  }
-  if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
-  if (grid < 1) grid = 1;
-
-  DecodeLaunch D;
-  D.packed = Wg->packed;
-  D.fmt = Wg->fmt;
-  D.N = Wg->N;
-  D.K = Wg->K;
-  D.RT = Wg->RT;
-  D.KT = Wg->KT;
-  D.seg_split = Wg->seg_split;
-  D.A = A;
-  D.lda = lda;
-  D.M = (int)M;
-  D.C = act;
-  D.ldc = act ? ld_act : 0;
-  D.status = reinterpret_cast<int*>(ws);
-  D.counters = reinterpret_cast<int*>(ws + L.counters);
-  D.ascale = reinterpret_cast<float*>(ws + L.ascale0);
-  D.Ap = ws + L.ap0;
-  D.partials = reinterpret_cast<float*>(ws + L.partials0);
-  D.grid = (int)grid;
-  D.ks = ks;
-  D.stages = stages;
-  D.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
-  D.withhold = opts ? opts->withhold_weights : 0;
-  D.layout = kLayoutPaired;
-  D.silu = 1;
-  D.down_packed = Wd->packed;
-  D.N1 = Wd->N;
-  D.RT1 = Wd->RT;
-  D.KT1 = Wd->KT;
-  D.C1 = C;
-  D.ldc1 = ldc;
-  D.partials1 = reinterpret_cast<float*>(ws + L.partials1);
-  D.counters1 = D.counters + Wg->RT;
-  D.Ap1 = ws + L.ap1;
-  D.ascale1 = reinterpret_cast<float*>(ws + L.ascale1);
-  D.gbar = reinterpret_cast<unsigned int*>(D.counters1 + Wd->RT);
-  int launches = 0;
-  cudaError_t e = launch_decode_mlp(D, (cudaStream_t)s, &launches);
-  if (e != cudaSuccess) return cuda_fail(e, "fused MLP launch");
-  for (vt_fp4_weight_s* W : {Wg, Wd}) {
-    W->info.path = 1;
-    W->info.grid = D.grid;
-    W->info.warps_per_cta = 18;
-    W->info.m_tile = decode_mt((int)M);
-    W->info.items = items0 + items1;
-    W->info.launches = launches;
-    W->info.calls += 1;
-  }
-  return VT_OK;
 }
 
 vt_status vt_fp4_w4a4_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,

@@ -53,20 +53,12 @@ int decode_mt(int M) { return M <= 8 ? 8 : 16; }
 // Dynamic shared memory of the decode kernel: `stages` stages of `ks` k tiles (weights, M
 // activation rows and the activation scales each), the consumer warps' reduction slots and
 // the barriers.
-// Fused MLP: after the barriers, one tile's silu(gate) * up as bf16 bits [16][64].
-constexpr int kMlpActBytes = 16 * 64 * 2;
-__host__ __device__ inline size_t decode_mlp_act_offset(int stages, int stage_bytes, int mt) {
-  return (size_t)stages * stage_bytes + (size_t)kConsumerWarps * mt * kSlotPad * 4 +
-         (size_t)stages * 16 + 64;
-}
-
-size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt, bool mlp) {
+size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt) {
   const size_t mt = (size_t)decode_mt(M);
   const size_t stage = resident_kt ? (size_t)ks * tile_bytes(fmt)
                                    : (size_t)ks * (tile_bytes(fmt) + (size_t)M * 128 + kAScaleStride * 4);
   return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 +
-         decode_resident_bytes(M, resident_kt) + (size_t)stages * 16 + 64 +
-         (mlp ? kMlpActBytes : 0);
+         decode_resident_bytes(M, resident_kt) + (size_t)stages * 16 + 64;
 }
 
 bool decode_resident_ok(int M, int64_t KT, int64_t RT) {
@@ -217,18 +209,6 @@ struct DecodeParams {
   int64_t lda, K;
   const uint8_t* gbase;        // expert e's packed weight at gbase + e * expert_bytes
   int64_t expert_bytes, RT;    // bytes per expert; 128-row tiles per expert
-  // fused MLP: a second GEMM (the down projection) follows the paired gate_up in the same
-  // launch; its activations are the first GEMM's silu(gate) * up, which the first GEMM's
-  // epilogues write in the pre-pass layout (Ap1, ascale1) before a grid-wide barrier
-  const uint8_t* tiles1;
-  const PackedHeader* hdr1;
-  int64_t N1, KT1, ldc1;
-  __nv_bfloat16* C1;
-  float* partials1;
-  int* counters1;
-  __half* Ap1;
-  float* ascale1;
-  unsigned int* gbar;  // CTAs past phase 0 (after the counters; zeroed by the pre-pass)
 };
 
 // SiLU(x) = x / (1 + e^-x) in fp32 (e^-x overflowing to infinity gives -0 for large -x).
@@ -329,21 +309,8 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // can queue behind the weights.  The split-K counters then rely on being left at zero by
 // the previous call (each reducer resets its counter; the workspace keeps the counters in a
 // fixed region that no other data of any weight overlaps).
-//
-// Fused MLP mode (MLP): two GEMMs in one launch.  Phase 0 is the paired gate_up with the
-// SiLU-and-multiply epilogue, which also converts each finished 64-wide block of silu(gate) *
-// up into the pre-pass layout (Ap1, ascale1) -- the same conversion as k_prep_a applies to
-// the bf16 values, so the result equals the two separate calls bit for bit.  Phase 1 is the
-// down projection reading those activations.  The ring runs on across the phases: the
-// producer requests phase 1's weights as soon as slots free up and its activation copies
-// once every CTA has passed a grid-wide barrier after its phase-0 epilogues.  The barrier is
-// a counter after the split-K counters, zeroed by the call's pre-pass: each CTA adds one with
-// release semantics when its phase-0 writes are done, and the producers wait (bounded) until
-// it reaches the grid size.  Every CTA is resident at once (one per SM, the grid no larger
-// than the SM count).
-template <int FMT, int MT, int KS, bool GRP, bool RA, bool MLP = false>
+template <int FMT, int MT, int KS, bool GRP, bool RA>
 __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const DecodeParams p) {
-  static_assert(!(MLP && (GRP || RA)), "the fused MLP streams its activations");
   constexpr int TB = tile_bytes(FMT);
   constexpr int NJ = MT / 8;           // n8 MMA column blocks
   constexpr int CW = kConsumerWarps;
@@ -368,13 +335,9 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   const int SCALES_OFF = WBYTES + KS * M * 128;
   const int STAGE = RA ? WBYTES : SCALES_OFF + KS * kAScaleStride * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int64_t G = gridDim.x, c = blockIdx.x;
-  int64_t KT = p.KT;
-  int64_t I = GRP ? (int64_t)p.gtab[kGtP] * p.RT * KT : p.items;
-  int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
-  // fused MLP: phase 1's item range (k tiles of the down projection = row tiles of phase 0)
-  const int64_t I1 = MLP ? (p.N1 + kTileRows - 1) / kTileRows * p.KT1 : 0;
-  const int64_t i0b = c * I1 / G, i1b = (c + 1) * I1 / G;
+  const int64_t G = gridDim.x, c = blockIdx.x, KT = p.KT;
+  const int64_t I = GRP ? (int64_t)p.gtab[kGtP] * p.RT * KT : p.items;
+  const int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
 
   float* slots = reinterpret_cast<float*>(smem + (size_t)S * STAGE);
   // resident mode: activations [KT][M][64] f16 (the pre-pass layout) and scales [KT][8]
@@ -388,8 +351,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   const uint32_t aready_u = smem_u32(empty + S + 1);  // resident mode: activations converted
 
   // Stages walk the CTA's items in order; all loop state advances incrementally.
-  int kt_first = (int)(i0 % KT);
-  int KTi = (int)KT;
+  const int kt_first = (int)(i0 % KT);
+  const int KTi = (int)KT;
   auto stage_len = [&](int64_t pos, int kt) -> int {
     int n = KS;
     if (n > KTi - kt) n = KTi - kt;
@@ -412,24 +375,12 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   if (warp == CW + 1) {
     // ------------------------------------------------------------- publisher
     // A CTA whose range starts inside a row tile shares that tile with the CTA before it:
-    // publish this CTA's partial of it once the consumers have written it (in each phase).
-    if (lane == 0) {
-      uint32_t npub = 0;
-      if (i0 < i1 && i0 % KT != 0) {
-        if (mbar_wait_bounded(pub_u, 0, p.wait_ns))
-          publish_release(reinterpret_cast<unsigned int*>(&p.counters[i0 / KT]));
-        else
-          atomicExch(p.status, 5);
-        ++npub;
-      }
-      if constexpr (MLP) {
-        if (i0b < i1b && i0b % p.KT1 != 0) {
-          if (mbar_wait_bounded(pub_u, npub & 1u, p.wait_ns))
-            publish_release(reinterpret_cast<unsigned int*>(&p.counters1[i0b / p.KT1]));
-          else
-            atomicExch(p.status, 5);
-        }
-      }
+    // publish this CTA's partial of it once the consumers have written it.
+    if (lane == 0 && i0 < i1 && i0 % KT != 0) {
+      if (mbar_wait_bounded(pub_u, 0, p.wait_ns))
+        publish_release(reinterpret_cast<unsigned int*>(&p.counters[i0 / KT]));
+      else
+        atomicExch(p.status, 5);
     }
     return;
   }
@@ -581,67 +532,6 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         ++issued;
         if (++slot == S) slot = 0;
       }
-      if constexpr (MLP) {
-        // Phase 1: its weights follow at once, as slots free up; its activations exist only
-        // once every CTA has passed the grid barrier, so their copies wait for it.  Stages
-        // requested before then are pending (weights only).  The barrier cannot pass before
-        // this CTA's consumers have used every phase-0 stage, by which time the producer has
-        // filled the ring with pending stages: it waits for the barrier only then (or after
-        // its last stage), without polling on the way.
-        KTi = (int)p.KT1;
-        i1 = i1b;
-        pos = i0b;
-        kt = (int)(i0b % p.KT1);
-        int64_t ppos = pos;  // first pending stage
-        int pkt = kt, pslot = slot, npend = 0;
-        bool passed = false, failed = false;
-        auto issue_pending = [&]() {
-          for (; npend > 0; --npend) {
-            const int n = stage_len(ppos, pkt);
-            const uint32_t dst = ring_u + pslot * STAGE;
-            bulk_g2s(dst + WBYTES, p.Ap1 + (int64_t)pkt * M * 64, (uint32_t)(n * M * 128),
-                     full_u + 8 * pslot, pol_a);
-            bulk_g2s(dst + SCALES_OFF, p.ascale1 + (int64_t)pkt * kAScaleStride,
-                     (uint32_t)(n * kAScaleStride * 4), full_u + 8 * pslot, pol_a);
-            ppos += n;
-            pkt += n;
-            if (pkt == KTi) pkt = 0;
-            if (++pslot == S) pslot = 0;
-          }
-        };
-        auto pass = [&]() -> bool {
-          // grid barrier: every CTA has announced its phase-0 writes
-          if (!wait_count(p.gbar, (unsigned int)G, p.wait_ns)) return false;
-          fence_proxy_async_all();  // the activations were written through the generic proxy
-          passed = true;
-          issue_pending();
-          return true;
-        };
-        while (pos < i1) {
-          if (!passed && npend == S && !pass()) {
-            failed = true;
-            break;
-          }
-          if (issued >= S &&
-              !mbar_wait_bounded(empty_u + 8 * slot, (uint32_t)((issued / S - 1) & 1), p.wait_ns)) {
-            failed = true;
-            break;
-          }
-          const int n = stage_len(pos, kt);
-          const uint32_t dst = ring_u + slot * STAGE;
-          mbar_expect_tx(full_u + 8 * slot, n * per_tile);
-          bulk_g2s(dst, p.tiles1 + pos * TB, (uint32_t)(n * TB), full_u + 8 * slot, pol);
-          ++npend;
-          if (passed) issue_pending();
-          pos += n;
-          kt += n;
-          if (kt == KTi) kt = 0;
-          ++issued;
-          if (++slot == S) slot = 0;
-        }
-        if (!failed && !passed && npend > 0 && !pass()) failed = true;
-        if (failed) atomicExch(p.status, 5);
-      }
     }
     return;
   }
@@ -720,37 +610,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   int64_t pos = i0;
   int kt = kt_first, slot = 0;
   uint32_t par = 0;
-  int64_t rt = i0 / KT;  // row tile of the current segment
-  // the GEMM of the current phase (fused MLP: phase 1 is the down projection)
-  int silu_on = p.silu;
-  __nv_bfloat16* Cout = p.C;
-  int64_t ldc = p.ldc, split = p.seg_split, Nrows = p.N;
-  uint32_t layout = p.layout;
-  float* partials = p.partials;
-  int* counters = p.counters;
-  // fused MLP: silu(gate) * up of the current tile as bf16 bits [16][64], for the conversion
-  uint16_t* s_act = reinterpret_cast<uint16_t*>(smem + decode_mlp_act_offset(S, STAGE, MT));
-#pragma unroll 1
-  for (int ph = 0; ph < (MLP ? 2 : 1); ++ph) {
-  if (MLP && ph == 1) {
-    KT = p.KT1;
-    KTi = (int)KT;
-    I = I1;
-    i0 = i0b;
-    i1 = i1b;
-    pos = i0;
-    kt = (int)(i0 % KT);
-    rt = i0 / KT;
-    silu_on = 0;
-    Cout = p.C1;
-    ldc = p.ldc1;
-    split = Nrows = p.N1;
-    layout = kLayoutRows;
-    partials = p.partials1;
-    counters = p.counters1;
-    f0 = p.hdr1->factor[0];
-    f1 = p.hdr1->factor[1];
-  }
+  const int64_t rt_first = i0 / KT;
+  int64_t rt = rt_first;  // row tile of the current segment
   while (pos < i1) {
     const int n = stage_len(pos, kt);
     if constexpr (GRP) {
@@ -887,15 +748,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       }
     consumer_sync(CT);
     const int nout = Mc * 128;
-    // SiLU-and-multiply output j of token m of this paired tile (fused MLP: also staged as
-    // bf16 bits for the conversion below, 0 past the intermediate size)
-    auto silu_out = [&](int m, int j, float gs, float us) {
-      const int64_t i = rt * 64 + j;
-      const __nv_bfloat16 v = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
-      if (i < split && (!MLP || Cout)) Cout[(int64_t)m * ldc + i] = v;
-      if constexpr (MLP) s_act[m * 64 + j] = i < split ? __bfloat16_as_ushort(v) : (uint16_t)0;
-    };
-    if (complete && silu_on) {
+    if (complete && p.silu) {
       // paired tile: rows j < 64 are gate rows, rows 64 + j the matching up rows
       for (int idx = threadIdx.x; idx < M * 64; idx += CT) {
         const int m = idx >> 6, j = idx & 63;
@@ -905,7 +758,9 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           gs += slots[(q * 4 + (j >> 5)) * SLOT + m * kSlotPad + (j & 31)];
           us += slots[(q * 4 + 2 + (j >> 5)) * SLOT + m * kSlotPad + (j & 31)];
         }
-        silu_out(m, j, gs, us);
+        const int64_t i = rt * 64 + j;
+        if (i < p.seg_split)
+          p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
       }
     } else if (!reducer) {  // a reducer adds its slots when the other partials are in
       for (int idx = threadIdx.x; idx < nout; idx += CT) {
@@ -918,18 +773,18 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           // the row within the expert, and the output row of the problem's token m
           const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
                                    : rt * kTileRows + row;
-          const int64_t n = packed_to_row(layout, prow, Nrows, split);
+          const int64_t n = packed_to_row(p.layout, prow, p.N, p.seg_split);
           const int64_t crow = GRP ? (int64_t)grow[m] : (int64_t)m;
           if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
             unsigned long long key = 0;
-            if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < split ? f0 : f1)), n);
+            if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
             greedy_fold(key, s_gkey, m);
           } else if (n >= 0) {
-            const float f = n < split ? f0 : f1;
-            Cout[crow * ldc + n] = __float2bfloat16_rn(sum * f);
+            const float f = n < p.seg_split ? f0 : f1;
+            p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
         } else if (!reducer) {
-          partials[((size_t)c * 2 * MT + m) * 128 + row] = sum;
+          p.partials[((size_t)c * 2 * MT + m) * 128 + row] = sum;
         }
       }
     }
@@ -940,7 +795,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     }
     if (reducer) {
       if (threadIdx.x == 0) {
-        unsigned int* ctr = reinterpret_cast<unsigned int*>(&counters[rt]);
+        unsigned int* ctr = reinterpret_cast<unsigned int*>(&p.counters[rt]);
         const bool got = wait_count(ctr, (unsigned int)(s_ncon - 1), p.wait_ns);
         if (got) *ctr = 0;  // every contributor has arrived: reset for the next call
         else atomicExch(p.status, 5);
@@ -963,7 +818,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const int64_t cc = c_lo + b0 + q;
-              v[q] = (b0 + q < ncon) ? __ldcg(&partials[(size_t)cc * 2 * MT * 128 + off]) : 0.0f;
+              v[q] = (b0 + q < ncon) ? __ldcg(&p.partials[(size_t)cc * 2 * MT * 128 + off]) : 0.0f;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -971,66 +826,29 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           }
           return sum;
         };
-        if (silu_on) {
+        if (p.silu) {
           for (int idx = threadIdx.x; idx < M * 64; idx += CT) {
             const int m = idx >> 6, j = idx & 63;
-            silu_out(m, j, tile_sum(m, j), tile_sum(m, 64 + j));
+            const float gs = tile_sum(m, j), us = tile_sum(m, 64 + j);
+            const int64_t i = rt * 64 + j;
+            if (i < p.seg_split)
+              p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
           }
         }
-        for (int idx = threadIdx.x; idx < (silu_on ? 0 : nout); idx += CT) {
+        for (int idx = threadIdx.x; idx < (p.silu ? 0 : nout); idx += CT) {
           const int m = idx >> 7, row = idx & 127;
           const float sum = tile_sum(m, row);
           const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
                                    : rt * kTileRows + row;
-          const int64_t n = packed_to_row(layout, prow, Nrows, split);
+          const int64_t n = packed_to_row(p.layout, prow, p.N, p.seg_split);
           const int64_t crow = GRP ? (int64_t)grow[m] : (int64_t)m;
           if (p.g_idx) {
             unsigned long long key = 0;
-            if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < split ? f0 : f1)), n);
+            if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
             greedy_fold(key, s_gkey, m);
           } else if (n >= 0) {
-            const float f = n < split ? f0 : f1;
-            Cout[crow * ldc + n] = __float2bfloat16_rn(sum * f);
-          }
-        }
-      }
-    }
-    if constexpr (MLP) {
-      if (ph == 0 && (complete || reducer)) {
-        // this tile's 64 outputs per token are k tile rt of phase 1: convert them as the
-        // activation pre-pass does (per token, one power of two from the largest magnitude)
-        consumer_sync(CT);
-        if (threadIdx.x < 128) {
-          const int m = threadIdx.x >> 3, gi = threadIdx.x & 7;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (m < M) v = *reinterpret_cast<const uint4*>(s_act + m * 64 + gi * 8);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          int mx = 0;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            mx = max(mx, (int)(w[q] & 0x7FFFu));
-            mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
-          }
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          if (m < M) {
-            int pe = 0;
-            if (mx > 0 && mx <= 0x7F80) {
-              pe = ((mx >> 7) - 127) - 14;
-              pe = pe < -120 ? -120 : (pe > 113 ? 113 : pe);
-            }
-            const float down = ldexpf(1.0f, -pe);
-            uint32_t o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float lo = __uint_as_float(w[q] << 16) * down;
-              const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
-              __half2 h = __floats2half2_rn(lo, hi);
-              o[q] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(p.Ap1 + ((rt * M + m) * 64 + ((gi ^ (m & 7)) * 8))) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-            if (gi == 0) p.ascale1[rt * kAScaleStride + m] = ldexpf(1.0f, pe);
+            const float f = n < p.seg_split ? f0 : f1;
+            p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
         }
       }
@@ -1038,16 +856,6 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     consumer_sync(CT);  // slots are rewritten by the next segment
     ++rt;
   }
-  if constexpr (MLP) {
-    if (ph == 0) {
-      // phase 0 done in this CTA: its converted activations go to phase 1's TMA copies
-      // (async proxy) in every CTA once all have arrived
-      fence_proxy_async_all();
-      consumer_sync(CT);
-      if (threadIdx.x == 0) publish_release(p.gbar);  // this CTA's arrival at the barrier
-    }
-  }
-  }  // phases
   if (!ok && lane == 0) atomicExch(p.status, 5);
   if (p.g_idx) {
     // One global atomic per token per CTA; the last CTA to finish turns the keys into
@@ -1082,11 +890,11 @@ static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
   return e;
 }
 
-template <int FMT, int MT, int KS, bool GRP = false, bool RA = false, bool MLP = false>
+template <int FMT, int MT, int KS, bool GRP = false, bool RA = false>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   static int done[64] = {0};
-  const size_t smem = decode_smem_bytes(FMT, GRP ? 16 : L.M, KS, L.stages, RA ? L.KT : 0, MLP);
-  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP, RA, MLP>, (int)smem, done);
+  const size_t smem = decode_smem_bytes(FMT, GRP ? 16 : L.M, KS, L.stages, RA ? L.KT : 0);
+  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP, RA>, (int)smem, done);
   if (e != cudaSuccess) return e;
   DecodeParams p;
   p.tiles = reinterpret_cast<const uint8_t*>(L.packed) + kHeaderBytes;
@@ -1119,19 +927,6 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
   p.lda = L.lda;
   p.K = L.K;
-  if (MLP) {
-    p.tiles1 = reinterpret_cast<const uint8_t*>(L.down_packed) + kHeaderBytes;
-    p.hdr1 = reinterpret_cast<const PackedHeader*>(L.down_packed);
-    p.N1 = L.N1;
-    p.KT1 = L.KT1;
-    p.ldc1 = L.ldc1;
-    p.C1 = reinterpret_cast<__nv_bfloat16*>(L.C1);
-    p.partials1 = L.partials1;
-    p.counters1 = L.counters1;
-    p.Ap1 = reinterpret_cast<__half*>(L.Ap1);
-    p.ascale1 = L.ascale1;
-    p.gbar = L.gbar;
-  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
@@ -1143,7 +938,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP, RA, MLP>, p);
+  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP, RA>, p);
 }
 
 // ------------------------------------------------------------- grouped pre-pass
@@ -1341,38 +1136,6 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) 
     if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 8>(L, s) : launch_t<FMT_NV, 16, 8>(L, s);
     else e = (mt == 8) ? launch_t<FMT_MX, 8, 8>(L, s) : launch_t<FMT_MX, 16, 8>(L, s);
   }
-  if (launches) *launches = 2;
-  return e;
-}
-
-cudaError_t launch_decode_mlp(const DecodeLaunch& L, cudaStream_t s, int* launches) {
-  if (L.w4a4 || L.resident || !L.down_packed || L.ks != 8 ||
-      L.counters1 != L.counters + L.RT ||
-      L.gbar != reinterpret_cast<unsigned int*>(L.counters1 + L.RT1))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaSuccess;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)L.M, (unsigned)((L.KT + kPrepTiles - 1) / kPrepTiles));
-    cfg.blockDim = dim3(kPrepThreads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // zeroes both GEMMs' split-K counters and the grid-barrier counter after them
-    e = cudaLaunchKernelEx(&cfg, k_prep_a, reinterpret_cast<const __nv_bfloat16*>(L.A), L.lda,
-                           L.K, L.KT, L.M, reinterpret_cast<__half*>(L.Ap), L.ascale, L.counters,
-                           L.RT + L.RT1 + 1);
-    if (e != cudaSuccess) return e;
-  }
-  if (L.fmt == FMT_NV)
-    e = decode_mt(L.M) == 8 ? launch_t<FMT_NV, 8, 8, false, false, true>(L, s)
-                            : launch_t<FMT_NV, 16, 8, false, false, true>(L, s);
-  else
-    e = decode_mt(L.M) == 8 ? launch_t<FMT_MX, 8, 8, false, false, true>(L, s)
-                            : launch_t<FMT_MX, 16, 8, false, false, true>(L, s);
   if (launches) *launches = 2;
   return e;
 }

@@ -51,18 +51,6 @@ struct DecodeLaunch {
   int w4a4 = 0;
   float alpha = 1.0f;
   int resident = 0;  // resident-activation mode (decode_resident_ok; not with w4a4 / grouped)
-  // fused MLP (launch_decode_mlp): `packed` is the paired gate_up and C its silu(gate) * up
-  // output [M][seg_split] (may be null); the down projection (N1 x K1, K1 = seg_split)
-  // follows in the same launch and writes C1 [M][ldc1]
-  const void* down_packed = nullptr;
-  int64_t N1 = 0, RT1 = 0, KT1 = 0;
-  void* C1 = nullptr;
-  int64_t ldc1 = 0;
-  float* partials1 = nullptr;  // [grid*2][MT][128]
-  int* counters1 = nullptr;    // [RT1], directly after counters[RT] (zeroed together)
-  void* Ap1 = nullptr;         // f16 [KT1][M][64], written by the first GEMM's epilogues
-  float* ascale1 = nullptr;    // [KT1][16]
-  unsigned int* gbar = nullptr;  // grid-barrier counter: counters1 + RT1 (zeroed by the pre-pass)
 };
 int decode_mt(int M);  // 8 or 16
 // Resident-activation decode (small M * K): the decode kernel converts A into shared memory
@@ -77,16 +65,12 @@ __host__ __device__ inline size_t decode_resident_bytes(int M, int64_t KT) {
 }
 bool decode_resident_ok(int M, int64_t KT, int64_t RT);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
-// Fused MLP decode: the activation pre-pass, then one kernel running the paired gate_up with
-// the SiLU-and-multiply epilogue and the down projection behind a grid-wide barrier.
-cudaError_t launch_decode_mlp(const DecodeLaunch& L, cudaStream_t s, int* launches);
 // Grouped decode: a pre-pass groups the (token, slot) pairs of topk_ids [M][topk] by
 // expert and converts their activations, then the decode kernel runs every problem.
 cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids, int npairs,
                                   int topk, int E, cudaStream_t s, int* launches);
 constexpr int kGroupTableInts = 1 + 3 * 128 + 128 * 16;  // see the decode kernel
-size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt = 0,
-                         bool mlp = false);
+size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt = 0);
 
 // Prefill tile GEMM (tensor cores), any M.
 struct PrefillLaunch {

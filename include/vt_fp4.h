@@ -176,32 +176,6 @@ vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_f
                                      void* C, int64_t ldc, void* workspace, size_t ws_bytes,
                                      vt_stream_t s);
 
-/* Fused MLP decode: C = down( silu(gate) * up ) for M <= 16 tokens in one GEMM kernel (plus
- * the activation pre-pass), the dense MLP of the pages' decode step -- "MXFP4 decode-graph +
- * gate_up FUSION default-ON" (PR #54), "Attribution" (the glue between the MLP's GEMMs is
- * a measured cost) and "re-verify 27B NVFP4" (PR #178), "Attribution" (the FP4 MLP GEMMs
- * are the decode step's lever).  The result equals vt_fp4_w4a16_gemm_silu_mul followed by
- * vt_fp4_w4a16_gemm on its output, bit for bit; the kernel streams the down weights while
- * the gate_up GEMM finishes, with a grid-wide barrier (bounded wait) between the two.
- *   A        (device) bf16 [M][lda], 16-byte aligned, lda % 8 == 0, lda >= K of gate_up.
- *   gate_up  a paired weight (vt_fp4_prepack_gate_up_paired) with intermediate size I.
- *   down     a plain weight (vt_fp4_prepack) of the same format with K == I.
- *   act      (device, optional: NULL) bf16 [M][ld_act], ld_act >= I: silu(gate) * up.
- *   C        (device) bf16 [M][ldc], ldc >= N of down; 4-byte aligned, ldc and ld_act even.
- *   workspace vt_fp4_mlp_workspace_bytes(gate_up, down) bytes, 256-byte aligned, zeroed
- *            once by the caller; it must not be in use by another call at the same time.
- *   opts     NULL or: grid (at most the SM count: every CTA must be resident at once),
- *            stages, wait_limit_us, withhold_weights as for vt_fp4_w4a16_gemm_ex; warps
- *            must be 0 or 8 and force_path 0.
- * Errors: M outside [0, 16], a weight that is grouped or of the wrong layout, formats that
- * differ, down's K != I -> VT_ERR_INVALID_ARG; misalignment -> VT_ERR_MISALIGNED; a wait
- * that runs out -> VT_ERR_TIMEOUT in the workspace status word (vt_fp4_workspace_status). */
-vt_status vt_fp4_mlp_workspace_bytes(vt_fp4_handle gate_up, vt_fp4_handle down, size_t* bytes);
-vt_status vt_fp4_w4a16_mlp(const void* A, int64_t M, int64_t lda, vt_fp4_handle gate_up,
-                           vt_fp4_handle down, void* act, int64_t ld_act, void* C, int64_t ldc,
-                           void* workspace, size_t ws_bytes, vt_stream_t s,
-                           const vt_fp4_gemm_opts* opts);
-
 /* Mixture-of-experts (grouped) weights: E experts of the same N x K, prepacked one after
  * another as E independent packed weights (each with its own global scale, or MXFP4 scale
  * window).  Source: "keep the ModelOpt NVFP4 lm_head packed" (PR #263), "Why this row

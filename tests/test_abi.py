@@ -98,14 +98,6 @@ def test_gemm_rejects_null_handle_and_negative_m(L):
     assert L.vt_fp4_destroy(None) == 0
 
 
-def test_fused_mlp_rejects_null_handles_without_a_gpu(L):
-    fake = ctypes.c_void_p(0x1000)
-    size = ctypes.c_size_t(0)
-    assert L.vt_fp4_mlp_workspace_bytes(None, None, ctypes.byref(size)) == 1
-    assert L.vt_fp4_w4a16_mlp(fake, 1, 64, None, None, None, 0, fake, 64, fake, 1 << 20, None,
-                              None) == 1
-
-
 def test_quantize_rejects_bad_shapes(L):
     fake = ctypes.c_void_p(0x1000)
     assert L.vt_fp4_quantize(fake, 4, 24, 0, fake, fake, fake, fake, None) == 1
