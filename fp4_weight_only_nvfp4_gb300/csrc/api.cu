@@ -492,8 +492,11 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
     return fail(VT_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, L.total);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   const int ks = 8;
+  // token tile of the decode kernel: 8 rows when M <= 8 (an expert then has at most M pairs
+  // unless a token names it twice; such extra pairs are left out), else 16
+  const int mrows = decode_mt((int)M);
   int stages = 6;
-  while (stages > 2 && decode_smem_bytes(W->fmt, 16, ks, stages) > 226 * 1024) --stages;
+  while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages) > 226 * 1024) --stages;
   const int64_t pmax = npairs < W->E ? npairs : W->E;
   const int64_t items = pmax * W->RT * W->KT;  // an upper bound: the pre-pass finds P
   int64_t grid = sm_count();
@@ -510,7 +513,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   D.seg_split = W->seg_split;
   D.A = A;
   D.lda = lda;
-  D.M = 16;
+  D.M = mrows;
   D.C = C;
   D.ldc = ldc;
   D.status = reinterpret_cast<int*>(ws + L.status);
@@ -532,7 +535,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   W->info.path = 3;
   W->info.grid = D.grid;
   W->info.warps_per_cta = 18;
-  W->info.m_tile = 16;
+  W->info.m_tile = mrows;
   W->info.items = items;
   W->info.launches = launches;
   W->info.calls += 1;

@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   // it first (the weights to stream depend on the routing)
   if constexpr (GRP) pdl_wait();
   const int S = p.stages;
-  const int M = GRP ? 16 : p.M;  // rows of the stage's activation area
+  const int M = GRP ? MT : p.M;  // rows of the stage's activation area
   // stage: weights | activation slices (M rows of 128 B per k tile) | activation scales;
   // resident mode: weights only
   const int SCALES_OFF = WBYTES + KS * M * 128;
@@ -893,7 +893,7 @@ static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
 template <int FMT, int MT, int KS, bool GRP = false, bool RA = false>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   static int done[64] = {0};
-  const size_t smem = decode_smem_bytes(FMT, GRP ? 16 : L.M, KS, L.stages, RA ? L.KT : 0);
+  const size_t smem = decode_smem_bytes(FMT, GRP ? MT : L.M, KS, L.stages, RA ? L.KT : 0);
   cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP, RA>, (int)smem, done);
   if (e != cudaSuccess) return e;
   DecodeParams p;
@@ -949,10 +949,13 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
 // activations of problem b's tokens for k tiles 8y .. 8y+7 exactly as k_prep_a does, into
 // A'[rowsum_b * KT + kt * count_b + s][64] (granules XOR-swizzled by s & 7) with scales
 // ascale[(b * KT + kt) * 16 + s]; block (0, 0) also writes the group table.  A pair whose
-// expert id is out of range sets status 6 and is left out (its output row is not written).
+// expert id is out of range, or that would be the (cap+1)-th or later pair of its expert (the
+// decode kernel's token tile holds `cap` rows; only a token naming one expert several times
+// can get there, since M <= cap), sets status 6 and is left out (its output row is not
+// written).
 __global__ void __launch_bounds__(kPrepThreads) k_group_prep(
     const __nv_bfloat16* __restrict__ A, int64_t lda, int64_t K, int64_t KT,
-    const int32_t* __restrict__ topk_ids, int npairs, int topk, int E,
+    const int32_t* __restrict__ topk_ids, int npairs, int topk, int E, int cap,
     __half* __restrict__ Ap, float* __restrict__ ascale, int* __restrict__ gtab,
     int* __restrict__ status, int* __restrict__ counters, int64_t ncounters) {
   pdl_launch_dependents();
@@ -988,7 +991,9 @@ __global__ void __launch_bounds__(kPrepThreads) k_group_prep(
     int pidx = 0;
     for (int j = 0; j < npairs; ++j)
       if (s_first[j] && s_e[j] < e) ++pidx;
-    s_prob[i] = e >= 0 ? pidx : -1;
+    const bool over = e >= 0 && s_slot[i] >= cap;  // the expert's token tile is full
+    if (over && blockIdx.x == 0 && blockIdx.y == 0) atomicExch(status, 6);
+    s_prob[i] = (e >= 0 && !over) ? pidx : -1;
   }
   __syncthreads();
   if (tid == 0) {
@@ -1079,13 +1084,19 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, k_group_prep, reinterpret_cast<const __nv_bfloat16*>(L.A),
-                           L.lda, L.K, L.KT, topk_ids, npairs, topk, E,
+                           L.lda, L.K, L.KT, topk_ids, npairs, topk, E, decode_mt(L.M),
                            reinterpret_cast<__half*>(L.Ap), L.ascale, const_cast<int*>(L.gtab),
                            L.status, L.counters, (int64_t)(pmax < kGtMaxProblems ? pmax : kGtMaxProblems) * L.RT);
     if (e != cudaSuccess) return e;
   }
-  if (L.ks == 4) e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 16, 4, true>(L, s) : launch_t<FMT_MX, 16, 4, true>(L, s);
-  else e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 16, 8, true>(L, s) : launch_t<FMT_MX, 16, 8, true>(L, s);
+  // token tile: 8 rows when no expert can have more than 8 pairs (M <= 8), else 16
+  const bool m8 = decode_mt(L.M) == 8;
+  if (L.ks == 4)
+    e = (L.fmt == FMT_NV) ? (m8 ? launch_t<FMT_NV, 8, 4, true>(L, s) : launch_t<FMT_NV, 16, 4, true>(L, s))
+                          : (m8 ? launch_t<FMT_MX, 8, 4, true>(L, s) : launch_t<FMT_MX, 16, 4, true>(L, s));
+  else
+    e = (L.fmt == FMT_NV) ? (m8 ? launch_t<FMT_NV, 8, 8, true>(L, s) : launch_t<FMT_NV, 16, 8, true>(L, s))
+                          : (m8 ? launch_t<FMT_MX, 8, 8, true>(L, s) : launch_t<FMT_MX, 16, 8, true>(L, s));
   if (launches) *launches = 2;
   return e;
 }

@@ -206,7 +206,9 @@ vt_status vt_fp4_moe_workspace_bytes(vt_fp4_handle W, int64_t M_max, int64_t top
  * decode kernel runs every expert's problem.
  *   topk_ids (device) int32 [M][topk], 1 <= topk <= 8; C (device) bf16 [M*topk][ldc].
  * A pair whose expert id is outside [0, E) is skipped (its C row is not written) and the
- * workspace status word reads 6. */
+ * workspace status word reads 6.  Each token's ids should be distinct: an expert serves at
+ * most 8 pairs when M <= 8 (16 when M > 8), so pairs beyond that -- possible only when a
+ * token names an expert more than once -- are skipped the same way (status 6). */
 vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
                                 const int32_t* topk_ids, int64_t topk, void* C, int64_t ldc,
                                 void* workspace, size_t ws_bytes, vt_stream_t s);

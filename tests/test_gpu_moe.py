@@ -1,7 +1,8 @@
 """GPU: the mixture-of-experts (grouped) decode GEMM.  Every output row (token m, slot j)
 is a plain GEMM row of expert topk_ids[m, j], so the oracle is the plain oracle GEMM per
 expert; the grouped prepack round-trips bit-exactly; results do not depend on the order of
-the routing; an out-of-range expert id is reported and skipped."""
+the routing; an out-of-range expert id, or a pair beyond its expert's token tile, is
+reported and skipped."""
 import numpy as np
 import pytest
 import torch
@@ -105,3 +106,24 @@ def test_moe_out_of_range_expert_is_reported_and_skipped():
     assert np.all(got[2] == 5.0)  # the skipped pair's row is untouched
     ref = _oracle(fmt, Ab, srcs, np.array([[0, 2], [1, 1]], np.int32), N)
     check_rows(got[[0, 1, 3]], ref[[0, 1, 3]], what="valid pairs")
+
+
+def test_moe_pairs_beyond_an_experts_token_tile_are_skipped():
+    """Every token names expert 3 in both slots: with M = 5 (token tile of 8 rows) expert 3
+    gets 10 pairs; the first 8 in pair order are computed, the last two (token 4) are
+    skipped with status 6 and their rows left untouched."""
+    fmt, E, N, K = vt.MXFP4, 4, 256, 512
+    srcs, W = _experts(fmt, E, N, K, 9)
+    M, topk = 5, 2
+    ids = np.full((M, topk), 3, np.int32)
+    Ab = make_acts(synth.tensor_id(89, 9, synth.ROLE_A), M, K)
+    ws = W.moe_workspace(M, topk)
+    C = torch.full((M * topk, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    vt.w4a16_gemm_moe(bf16_dev(Ab), W, to_dev(ids), out=C, workspace=ws)
+    torch.cuda.synchronize()
+    assert W.stats()["m_tile"] == 8
+    assert vt.workspace_status(ws) == 6
+    got = C.float().cpu().numpy()
+    assert np.all(got[8:] == 5.0)
+    ref = _oracle(fmt, Ab, srcs, ids, N)
+    check_rows(got[:8], ref[:8], what="pairs within the token tile")
