@@ -953,7 +953,25 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
 // decode kernel's token tile holds `cap` rows; only a token naming one expert several times
 // can get there, since M <= cap), sets status 6 and is left out (its output row is not
 // written).
-__global__ void __launch_bounds__(kPrepThreads) k_group_prep(
+constexpr int kGroupThreads = 128;  // one (token, slot) pair per thread: M * topk <= 128
+
+// Block-wide inclusive scan (sum or max) over the 128 threads' values.
+template <bool MAX>
+__device__ __forceinline__ int block_scan128(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = MAX ? max(v, u) : v + u;
+  }
+  if (lane == 31) s_warp[w] = v;
+  __syncthreads();
+  for (int q = 0; q < w; ++q) v = MAX ? max(v, s_warp[q]) : v + s_warp[q];
+  __syncthreads();
+  return v;
+}
+
+__global__ void __launch_bounds__(kGroupThreads) k_group_prep(
     const __nv_bfloat16* __restrict__ A, int64_t lda, int64_t K, int64_t KT,
     const int32_t* __restrict__ topk_ids, int npairs, int topk, int E, int cap,
     __half* __restrict__ Ap, float* __restrict__ ascale, int* __restrict__ gtab,
@@ -961,80 +979,76 @@ __global__ void __launch_bounds__(kPrepThreads) k_group_prep(
   pdl_launch_dependents();
   pdl_wait();
   zero_counters(counters, ncounters);
-  __shared__ int s_e[kGtMaxProblems], s_prob[kGtMaxProblems], s_slot[kGtMaxProblems];
-  __shared__ int s_first[kGtMaxProblems], s_cnt[kGtMaxProblems], s_rsum[kGtMaxProblems];
-  __shared__ int s_pexp[kGtMaxProblems], s_P;
+  __shared__ uint32_t s_key[kGroupThreads];
+  __shared__ int s_warp[kGroupThreads / 32];
+  __shared__ int s_P, s_cnt, s_rsum, s_pair[16];
   const int tid = threadIdx.x;
-  for (int i = tid; i < npairs; i += kPrepThreads) {
-    int e = topk_ids[i];
-    if (e < 0 || e >= E) {
-      if (blockIdx.x == 0 && blockIdx.y == 0) atomicExch(status, 6);
-      e = -1;
-    }
-    s_e[i] = e;
+  const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
+  // Sort the pairs by (expert, pair index); an invalid id sorts last.
+  uint32_t key = 0xFFFFFFFFu;
+  if (tid < npairs) {
+    const int e = topk_ids[tid];
+    if (e >= 0 && e < E) key = ((uint32_t)e << 8) | (uint32_t)tid;
+    else if (lead) atomicExch(status, 6);
   }
+  s_key[tid] = key;
   __syncthreads();
-  for (int i = tid; i < npairs; i += kPrepThreads) {
-    const int e = s_e[i];
-    int first = 1, slot = 0;
-    for (int j = 0; j < i; ++j)
-      if (s_e[j] == e) {
-        first = 0;
-        ++slot;
+  for (int k = 2; k <= kGroupThreads; k <<= 1) {  // bitonic sort, ascending
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int o = tid ^ j;
+      if (o > tid) {
+        const uint32_t x = s_key[tid], y = s_key[o];
+        if ((x > y) == ((tid & k) == 0)) {
+          s_key[tid] = y;
+          s_key[o] = x;
+        }
       }
-    s_first[i] = first && e >= 0;
-    s_slot[i] = slot;
-  }
-  __syncthreads();
-  for (int i = tid; i < npairs; i += kPrepThreads) {
-    const int e = s_e[i];
-    int pidx = 0;
-    for (int j = 0; j < npairs; ++j)
-      if (s_first[j] && s_e[j] < e) ++pidx;
-    const bool over = e >= 0 && s_slot[i] >= cap;  // the expert's token tile is full
-    if (over && blockIdx.x == 0 && blockIdx.y == 0) atomicExch(status, 6);
-    s_prob[i] = (e >= 0 && !over) ? pidx : -1;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int P = 0;
-    for (int j = 0; j < npairs; ++j) P += s_first[j];
-    for (int q = 0; q < P; ++q) s_cnt[q] = 0;
-    for (int j = 0; j < npairs; ++j)
-      if (s_prob[j] >= 0) {
-        ++s_cnt[s_prob[j]];
-        s_pexp[s_prob[j]] = s_e[j];
-      }
-    int r = 0;
-    for (int q = 0; q < P; ++q) {
-      s_rsum[q] = r;
-      r += s_cnt[q];
+      __syncthreads();
     }
-    s_P = P;
+  }
+  // Sorted position tid: its expert's run starts at `first`; its slot in the run is
+  // tid - first; a pair at slot >= cap does not fit the decode kernel's token tile.
+  key = s_key[tid];
+  const bool valid = key != 0xFFFFFFFFu;
+  const int e = (int)(key >> 8), pair = (int)(key & 0xFFu);
+  const bool head = valid && (tid == 0 || (s_key[tid - 1] >> 8) != key >> 8);
+  const int first = block_scan128<true>(head ? tid : 0, s_warp);
+  const int slot = tid - first;
+  const bool kept = valid && slot < cap;
+  if (valid && !kept && lead) atomicExch(status, 6);
+  const int prob = block_scan128<false>(head ? 1 : 0, s_warp) - 1;  // problem index
+  const int kept_incl = block_scan128<false>(kept ? 1 : 0, s_warp);
+  const bool last = kept && (tid + 1 == kGroupThreads || !(s_key[tid + 1] != 0xFFFFFFFFu &&
+                                                         (s_key[tid + 1] >> 8) == key >> 8 &&
+                                                         slot + 1 < cap));
+  if (tid == kGroupThreads - 1) s_P = prob + 1;  // heads among the valid pairs
+  if (lead && kept) {
+    gtab[kGtPair + prob * 16 + slot] = pair;
+    if (head) {
+      gtab[kGtExpert + prob] = e;
+      gtab[kGtRowsum + prob] = kept_incl - 1;
+    }
+    if (last) gtab[kGtCount + prob] = slot + 1;
+  }
+  const int b = blockIdx.x;
+  if (kept && prob == b) {
+    s_pair[slot] = pair;
+    if (head) s_rsum = kept_incl - 1;
+    if (last) s_cnt = slot + 1;
   }
   __syncthreads();
   const int P = s_P;
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
-    for (int q = tid; q < P; q += kPrepThreads) {
-      gtab[kGtExpert + q] = s_pexp[q];
-      gtab[kGtCount + q] = s_cnt[q];
-      gtab[kGtRowsum + q] = s_rsum[q];
-    }
-    for (int i = tid; i < npairs; i += kPrepThreads)
-      if (s_prob[i] >= 0) gtab[kGtPair + s_prob[i] * 16 + s_slot[i]] = i;
-    if (tid == 0) gtab[kGtP] = P;
-  }
-  const int b = blockIdx.x;
+  if (lead && tid == 0) gtab[kGtP] = P;
   if (b >= P) return;
-  const int cnt = s_cnt[b], rsum = s_rsum[b];
-  const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + (tid >> 3);
+  // Convert this problem's tokens for k tiles 8y .. 8y+7 as k_prep_a does: rows
+  // rowsum * KT + kt * count + s, granules XOR-swizzled by s & 7; threads 0-63 take the even
+  // slots, 64-127 the odd ones.
+  const int cnt = s_cnt, rsum = s_rsum;
+  const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + ((tid & 63) >> 3);
   const int gi = tid & 7;
   const int64_t k0 = kt * 64 + gi * 8;
-  for (int sx = 0; sx < cnt; ++sx) {
-    int pair = 0;
-    for (int j = 0; j < npairs; ++j)
-      if (s_prob[j] == b && s_slot[j] == sx) pair = j;
-    const int64_t m = pair / topk;
+  for (int sx = tid >> 6; sx < cnt; sx += 2) {
+    const int64_t m = s_pair[sx] / topk;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -1076,7 +1090,7 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(pmax > 0 ? pmax : 1),
                        (unsigned)((L.KT + kPrepTiles - 1) / kPrepTiles));
-    cfg.blockDim = dim3(kPrepThreads);
+    cfg.blockDim = dim3(kGroupThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
