@@ -979,33 +979,38 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
   pdl_launch_dependents();
   pdl_wait();
   zero_counters(counters, ncounters);
-  __shared__ uint32_t s_key[kGroupThreads];
+  __shared__ uint32_t s_in[kGroupThreads], s_key[kGroupThreads];
   __shared__ int s_warp[kGroupThreads / 32];
   __shared__ int s_P, s_cnt, s_rsum, s_pair[16];
+  __shared__ __align__(16) uint4 s_a[16 * kPrepTiles * 8];  // A rows' granules of this block's k tiles
   const int tid = threadIdx.x;
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
-  // Sort the pairs by (expert, pair index); an invalid id sorts last.
+  const int M = npairs / topk;
+  // The activations of every token for this block's k tiles, requested before the grouping
+  // (which token rows the block converts is known only after it).
+  for (int i = tid; i < M * kPrepTiles * 8; i += kGroupThreads) {
+    const int m = i / (kPrepTiles * 8), r = i - m * (kPrepTiles * 8);
+    const int64_t k0 = ((int64_t)blockIdx.y * kPrepTiles + (r >> 3)) * 64 + (r & 7) * 8;
+    s_a[i] = k0 < K ? __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0)) : make_uint4(0, 0, 0, 0);
+  }
+  // Sort the pairs by (expert, pair index) -- an invalid id sorts last -- by rank: the
+  // number of smaller keys, ties (the invalid ones) broken by position.
   uint32_t key = 0xFFFFFFFFu;
   if (tid < npairs) {
     const int e = topk_ids[tid];
     if (e >= 0 && e < E) key = ((uint32_t)e << 8) | (uint32_t)tid;
     else if (lead) atomicExch(status, 6);
   }
-  s_key[tid] = key;
+  s_in[tid] = key;
   __syncthreads();
-  for (int k = 2; k <= kGroupThreads; k <<= 1) {  // bitonic sort, ascending
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const int o = tid ^ j;
-      if (o > tid) {
-        const uint32_t x = s_key[tid], y = s_key[o];
-        if ((x > y) == ((tid & k) == 0)) {
-          s_key[tid] = y;
-          s_key[o] = x;
-        }
-      }
-      __syncthreads();
-    }
+  int rank = 0;
+#pragma unroll 8
+  for (int j = 0; j < kGroupThreads; ++j) {
+    const uint32_t x = s_in[j];
+    rank += (x < key) | ((x == key) & (j < tid));
   }
+  s_key[rank] = key;
+  __syncthreads();
   // Sorted position tid: its expert's run starts at `first`; its slot in the run is
   // tid - first; a pair at slot >= cap does not fit the decode kernel's token tile.
   key = s_key[tid];
@@ -1046,11 +1051,9 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
   const int cnt = s_cnt, rsum = s_rsum;
   const int64_t kt = (int64_t)blockIdx.y * kPrepTiles + ((tid & 63) >> 3);
   const int gi = tid & 7;
-  const int64_t k0 = kt * 64 + gi * 8;
   for (int sx = tid >> 6; sx < cnt; sx += 2) {
-    const int64_t m = s_pair[sx] / topk;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
+    const int m = s_pair[sx] / topk;
+    const uint4 v = s_a[m * (kPrepTiles * 8) + (tid & 63)];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     int mx = 0;
 #pragma unroll
