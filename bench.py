@@ -786,7 +786,7 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0):
     reps = 1
     if frac >= 1.0 and dt < 0.5 * target_s:
         # the whole step is quicker than the target: run it repeatedly
-        reps = max(1, min(64, int(target_s / max(dt, 1e-3))))
+        reps = max(1, min(4096, int(target_s / max(dt, 1e-3))))
         for _ in range(reps - 1):
             b2, d2 = run(frac)
             nbytes += b2
@@ -906,6 +906,8 @@ def main():
                        calls_per_step=r["calls_per_step"]),
         "roofline": {"bound": "tensor" if prefill else "hbm",
                      "kernel": ("k_prefill (+ k_prep_rows, one GEMM call)" if prefill else
+                                "k_decode, grouped (+ k_group_prep; one MoE call)"
+                                if w.kind == "moe" else
                                 "k_decode (+ k_prep_a where a pre-pass converts the "
                                 "activations; one GEMM call)"),
                      "achieved": round(r["achieved"], 1), "peak": peak, "unit": w.unit,
