@@ -609,107 +609,38 @@ def run_gpu(args, rank: int, world: int):
     }
 
 
-def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
+class _Slots:
+    """Per-call slots carved out of one pinned host buffer and one device buffer (256-byte
+    aligned), so that a step moves all its inputs, or all its outputs, with one copy."""
+
+    def __init__(self, sizes, dev):
+        import torch
+        self.off, tot = [], 0
+        for b in sizes:
+            self.off.append(tot)
+            tot += (b + 255) // 256 * 256
+        self.nbytes = tot
+        self.host = torch.zeros(max(tot, 256), dtype=torch.uint8).pin_memory()
+        self.dev = torch.zeros(max(tot, 256), dtype=torch.uint8, device=dev)
+
+    def view(self, i, shape, dtype, host=False):
+        import torch
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        buf = self.host if host else self.dev
+        return buf[self.off[i]:self.off[i] + n].view(dtype).view(shape)
+
+    def to_dev(self):
+        if self.nbytes:
+            self.dev[:self.nbytes].copy_(self.host[:self.nbytes], non_blocking=True)
+
+    def to_host(self):
+        if self.nbytes:
+            self.host[:self.nbytes].copy_(self.dev[:self.nbytes], non_blocking=True)
+
+
+def _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, h2d, d2h):
+    """Warm-up, one CUDA graph of the step (copy in, every call, copy out), timed replays."""
     import torch
-    import fp4_weight_only_nvfp4_gb300 as vt
-    hA, dA, hC, dC = {}, {}, {}, {}
-    for M in w.Ms:
-        for p in w.projs:
-            hA[(M, p.K)] = torch.randn((M, p.K)).to(torch.bfloat16).pin_memory()
-            dA[(M, p.K)] = torch.empty((M, p.K), dtype=torch.bfloat16, device=dev)
-            hC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16).pin_memory()
-            dC[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
-    greedy = w.kind == "greedy"
-    silu = w.kind == "mlp_silu"
-    a4 = w.extra.get("w4a4")
-    hT = {M: torch.empty(M, dtype=torch.int32).pin_memory() for M in w.Ms}
-    if silu:  # the MLP chain: host input of gate_up in, host output of down out
-        I_mlp = max(p.I for p in w.projs if p.fused)
-        dAct = {M: torch.empty((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms}
-        h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls if w.projs[pi].fused)
-        d2h = sum(M * w.projs[pi].N * 2 for _, _, pi, M in calls if not w.projs[pi].fused)
-    else:
-        h2d = sum(M * w.projs[pi].K * 2 for _, _, pi, M in calls)
-        d2h = sum(M * (4 if greedy else w.projs[pi].N * 2) for _, _, pi, M in calls)
-
-    def issue():
-        for c, layer, pi, M in calls:
-            p = w.projs[pi]
-            if silu:
-                if p.fused:
-                    dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
-                    vt.w4a16_gemm_silu_mul(dA[(M, p.K)], sets[c][layer][pi], out=dAct[M],
-                                           workspace=ws, stream=stream)
-                else:
-                    vt.w4a16_gemm(dAct[M], sets[c][layer][pi], out=dC[(M, p.N)], workspace=ws,
-                                  stream=stream)
-                    hC[(M, p.N)].copy_(dC[(M, p.N)], non_blocking=True)
-                continue
-            dA[(M, p.K)].copy_(hA[(M, p.K)], non_blocking=True)
-            if greedy:
-                tok, _ = vt.w4a16_gemm_greedy(dA[(M, p.K)], sets[c][layer][pi], workspace=ws,
-                                              stream=stream, want_value=False)
-                hT[M].copy_(tok, non_blocking=True)
-                continue
-            if a4 is not None:
-                vt.w4a4_gemm(dA[(M, p.K)], sets[c][layer][pi], a4, out=dC[(M, p.N)],
-                             workspace=ws, stream=stream)
-            else:
-                vt.w4a16_gemm(dA[(M, p.K)], sets[c][layer][pi], out=dC[(M, p.N)],
-                              workspace=ws, stream=stream)
-            hC[(M, p.N)].copy_(dC[(M, p.N)], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            issue()
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            issue()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            graph.replay()
-    stream.synchronize()
-    if dist:
-        dist.barrier()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        t1.record(stream)
-    stream.synchronize()
-    ms = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms, dist, dev)
-    ms_step = ms / args.steps
-    return {"value": round(job_rate(w, step_bytes, world, ms_step * 1e-3), 2), "unit": w.unit,
-            "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-
-
-def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
-    """The MoE step end to end: host activations and routing in, host expert outputs out."""
-    import torch
-    import fp4_weight_only_nvfp4_gb300 as vt
-    p, topk = w.projs[0], w.extra["topk"]
-    hA = {M: torch.randn((M, p.K)).to(torch.bfloat16).pin_memory() for M in w.Ms}
-    dA = {M: torch.empty((M, p.K), dtype=torch.bfloat16, device=dev) for M in w.Ms}
-    hR = {k: v.cpu().pin_memory() for k, v in route.items()}
-    dR = {k: torch.empty_like(v) for k, v in route.items()}
-    hC = {M: torch.empty((M * topk, p.N), dtype=torch.bfloat16).pin_memory() for M in w.Ms}
-    dC = {M: torch.empty((M * topk, p.N), dtype=torch.bfloat16, device=dev) for M in w.Ms}
-    h2d = sum(M * p.K * 2 + M * topk * 4 for _, _, _, M in calls)
-    d2h = sum(M * topk * p.N * 2 for _, _, _, M in calls)
-
-    def issue():
-        for c, layer, pi, M in calls:
-            dA[M].copy_(hA[M], non_blocking=True)
-            dR[(c, M)].copy_(hR[(c, M)], non_blocking=True)
-            vt.w4a16_gemm_moe(dA[M], sets[c][layer][pi], dR[(c, M)], out=dC[M], workspace=ws,
-                              stream=stream)
-            hC[M].copy_(dC[M], non_blocking=True)
-
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             issue()
@@ -732,7 +663,87 @@ def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, 
     stream.synchronize()
     ms_step = max_over_ranks(t0.elapsed_time(t1), dist, dev) / args.steps
     return {"value": round(job_rate(w, step_bytes, world, ms_step * 1e-3), 2), "unit": w.unit,
-            "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies_per_step": 2}
+
+
+def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
+    """The step end to end through the public API: every call's activations from pinned host
+    memory (one host-to-device copy of the step's inputs), the calls, and every call's
+    result back to pinned host memory (one device-to-host copy), all inside the timed
+    region."""
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    greedy = w.kind == "greedy"
+    silu = w.kind in ("mlp_silu",)
+    a4 = w.extra.get("w4a4")
+    # MLP chain: the host input feeds gate_up, down's output goes back; act stays on device
+    host_in = [not (silu and not w.projs[pi].fused) for _, _, pi, _ in calls]
+    host_out = [not (silu and w.projs[pi].fused) for _, _, pi, _ in calls]
+    IN = _Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
+                 for i, (_, _, pi, M) in enumerate(calls)], dev)
+    OUT = _Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
+                  for i, (_, _, pi, M) in enumerate(calls)], dev)
+    for i, (_, _, pi, M) in enumerate(calls):
+        if host_in[i]:
+            IN.view(i, (M, w.projs[pi].K), torch.bfloat16, host=True).copy_(
+                torch.randn((M, w.projs[pi].K)).to(torch.bfloat16))
+    I_mlp = max((p.I for p in w.projs if p.fused), default=0)
+    dAct = {M: torch.empty((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms} if silu else {}
+
+    def issue():
+        IN.to_dev()
+        for i, (c, layer, pi, M) in enumerate(calls):
+            p, W = w.projs[pi], sets[c][layer][pi]
+            if silu:
+                if p.fused:
+                    vt.w4a16_gemm_silu_mul(IN.view(i, (M, p.K), torch.bfloat16), W, out=dAct[M],
+                                           workspace=ws, stream=stream)
+                else:
+                    vt.w4a16_gemm(dAct[M], W, out=OUT.view(i, (M, p.N), torch.bfloat16),
+                                  workspace=ws, stream=stream)
+                continue
+            A = IN.view(i, (M, p.K), torch.bfloat16)
+            if greedy:
+                vt.w4a16_gemm_greedy(A, W, workspace=ws, stream=stream, want_value=False,
+                                     token=OUT.view(i, (M,), torch.int32))
+            elif a4 is not None:
+                vt.w4a4_gemm(A, W, a4, out=OUT.view(i, (M, p.N), torch.bfloat16), workspace=ws,
+                             stream=stream)
+            else:
+                vt.w4a16_gemm(A, W, out=OUT.view(i, (M, p.N), torch.bfloat16), workspace=ws,
+                              stream=stream)
+        OUT.to_host()
+
+    return _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, IN.nbytes, OUT.nbytes)
+
+
+def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
+    """The MoE step end to end: every call's activations and routing from pinned host memory
+    (one copy in), the calls, every call's expert outputs back to the host (one copy out)."""
+    import torch
+    import fp4_weight_only_nvfp4_gb300 as vt
+    p, topk = w.projs[0], w.extra["topk"]
+    sizes = []
+    for _, _, _, M in calls:
+        sizes += [M * p.K * 2, M * topk * 4]
+    IN = _Slots(sizes, dev)
+    OUT = _Slots([M * topk * p.N * 2 for _, _, _, M in calls], dev)
+    for i, (c, _, _, M) in enumerate(calls):
+        IN.view(2 * i, (M, p.K), torch.bfloat16, host=True).copy_(
+            torch.randn((M, p.K)).to(torch.bfloat16))
+        IN.view(2 * i + 1, (M, topk), torch.int32, host=True).copy_(route[(c, M)].cpu())
+
+    def issue():
+        IN.to_dev()
+        for i, (c, layer, pi, M) in enumerate(calls):
+            vt.w4a16_gemm_moe(IN.view(2 * i, (M, p.K), torch.bfloat16), sets[c][layer][pi],
+                              IN.view(2 * i + 1, (M, topk), torch.int32),
+                              out=OUT.view(i, (M * topk, p.N), torch.bfloat16), workspace=ws,
+                              stream=stream)
+        OUT.to_host()
+
+    return _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, IN.nbytes, OUT.nbytes)
 
 
 # ---------------------------------------------------------------- CPU (oracle) leg

@@ -274,14 +274,18 @@ def w4a16_gemm_silu_mul(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | No
 
 
 def w4a16_gemm_greedy(A: torch.Tensor, W: PackedWeight, workspace: torch.Tensor | None = None,
-                      stream=None, want_value: bool = True):
+                      stream=None, want_value: bool = True, token: torch.Tensor | None = None):
     """Greedy head (M <= 16): per token, the index (int32 [M]) of the largest bf16 output of
     A . W^T, ties to the lowest index, and that value (fp32 [M]) -- without writing the
-    outputs.  See vt_fp4_w4a16_gemm_greedy in include/vt_fp4.h."""
+    outputs.  ``token``: an optional int32 [M] output tensor.  See vt_fp4_w4a16_gemm_greedy
+    in include/vt_fp4.h."""
     if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
         raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
     M = A.shape[0]
-    token = torch.empty(M, dtype=torch.int32, device=A.device)
+    if token is None:
+        token = torch.empty(M, dtype=torch.int32, device=A.device)
+    elif token.dtype != torch.int32 or token.shape != (M,) or not token.is_contiguous():
+        raise ValueError("token must be a contiguous int32 [M] tensor")
     value = torch.empty(M, dtype=torch.float32, device=A.device) if want_value else None
     if workspace is None:
         workspace = W.new_workspace(M)
