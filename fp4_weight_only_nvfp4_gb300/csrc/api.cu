@@ -329,8 +329,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
                 (long long)lda, (long long)ldc);
   if (!aligned(A, 16) || lda % 8)
     return fail(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda %% 8 == 0");
-  if (!g_idx && (!aligned(C, 4) || ldc % 2))
-    return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
+  if (!g_idx && !aligned(C, 2)) return fail(VT_ERR_MISALIGNED, "C must be 2-byte aligned");
   if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   const int force = opts ? opts->force_path : 0;
   if (force < 0 || force > 3) return fail(VT_ERR_INVALID_ARG, "force_path must be 0..3");
@@ -482,7 +481,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
     return fail(VT_ERR_INVALID_ARG, "lda must be >= K and ldc >= N");
   if (!aligned(A, 16) || lda % 8)
     return fail(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda %% 8 == 0");
-  if (!aligned(C, 4) || ldc % 2) return fail(VT_ERR_MISALIGNED, "C must be 4-byte aligned, ldc even");
+  if (!aligned(C, 2)) return fail(VT_ERR_MISALIGNED, "C must be 2-byte aligned");
   if (!aligned(workspace, 256)) return fail(VT_ERR_MISALIGNED, "workspace must be 256-byte aligned");
   if (!aligned(topk_ids, 4)) return fail(VT_ERR_MISALIGNED, "topk_ids must be 4-byte aligned");
   if (W->K > 110000) return fail(VT_ERR_UNSUPPORTED, "K > 110000 is not supported");

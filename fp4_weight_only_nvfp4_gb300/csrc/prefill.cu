@@ -164,6 +164,7 @@ struct PrefillParams {
   __nv_bfloat16* C;
   int* status;
   int vec_store;     // C 16-byte aligned and ldc % 8 == 0
+  int pair_store;    // C 4-byte aligned and ldc even: two outputs per 32-bit store
   uint64_t wait_ns;  // limit of every bounded wait
   int withhold;      // test hook: issue no copies (the waits then run out)
   uint32_t layout;   // packed row order (kLayoutRows / kLayoutPaired)
@@ -329,9 +330,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             sc[r] = 0;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_empty + 8 * ip);
-        if (++ip == kPStages) { ip = 0; pp ^= 1u; }
         // convert: row g words in k order, row g+8 likewise (8 x f16x2 each)
         uint32_t og[2][8], o8[2][8];
 #pragma unroll
@@ -355,6 +353,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             o8[r][2 * q + 1] = *reinterpret_cast<uint32_t*>(&h3);
           }
         }
+        // The packed stage is released only now that every lane has used the values it
+        // loaded: an arrive right after issuing the shared-memory loads let the next copy
+        // into the stage overwrite data some loads had not read yet (one warp's 32 weight
+        // rows of a k tile wrong, seen with MXFP4 tiles when a CTA ran many tiles).
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_empty + 8 * ip);
+        if (++ip == kPStages) { ip = 0; pp ^= 1u; }
         if (!(ok = pf_wait(b_empty + 8 * ib, pb ^ 1u, abort, p.wait_ns))) break;
         const uint32_t bt = sB + ib * kBBytes;
 #pragma unroll
@@ -419,8 +424,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int64_t i = i0 + 2 * e;
-              if (i + 1 < p.seg_split) *reinterpret_cast<uint32_t*>(crow + i) = o[e];
-              else if (i < p.seg_split) *reinterpret_cast<uint16_t*>(crow + i) = (uint16_t)(o[e] & 0xFFFFu);
+              if (p.pair_store && i + 1 < p.seg_split) {
+                *reinterpret_cast<uint32_t*>(crow + i) = o[e];
+              } else {
+                if (i < p.seg_split) *reinterpret_cast<uint16_t*>(crow + i) = (uint16_t)(o[e] & 0xFFFFu);
+                if (i + 1 < p.seg_split) *reinterpret_cast<uint16_t*>(crow + i + 1) = (uint16_t)(o[e] >> 16);
+              }
             }
           }
         }
@@ -461,11 +470,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int64_t n = n0 + 2 * i;
-            if (n + 1 < p.N) {
+            if (p.pair_store && n + 1 < p.N) {
               *reinterpret_cast<uint32_t*>(crow + n) = o[i];
-            } else if (n < p.N) {
-              const uint16_t lo = (uint16_t)(o[i] & 0xFFFFu);
-              *reinterpret_cast<uint16_t*>(crow + n) = lo;
+            } else {
+              if (n < p.N) *reinterpret_cast<uint16_t*>(crow + n) = (uint16_t)(o[i] & 0xFFFFu);
+              if (n + 1 < p.N) *reinterpret_cast<uint16_t*>(crow + n + 1) = (uint16_t)(o[i] >> 16);
             }
           }
         }
@@ -681,6 +690,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   pp.C = reinterpret_cast<__nv_bfloat16*>(L.C);
   pp.status = L.status;
   pp.vec_store = ((uintptr_t)L.C % 16 == 0) && (L.ldc % 8 == 0);
+  pp.pair_store = ((uintptr_t)L.C % 4 == 0) && (L.ldc % 2 == 0);
   pp.wait_ns = L.wait_ns ? L.wait_ns : 2000000000ull;
   pp.withhold = L.withhold;
   pp.layout = L.layout;

@@ -148,7 +148,7 @@ vt_status vt_fp4_workspace_bytes(vt_fp4_handle W, int64_t M_max, size_t* bytes);
 
 /* C = A . W^T in bf16 with fp32 accumulation.
  *   A  (device) bf16 [M][lda], 16-byte aligned, lda >= K, lda % 8 == 0.
- *   C  (device) bf16 [M][ldc], 4-byte aligned, ldc >= N, ldc % 2 == 0.
+ *   C  (device) bf16 [M][ldc], 2-byte aligned, ldc >= N.
  *   M  tokens; M == 0 is a no-op.  M <= 16 runs the decode kernel, larger M the
  *      tensor-core tile kernel.
  *   workspace (device) >= vt_fp4_workspace_bytes(W, M), 256-byte aligned, zeroed once.
@@ -169,7 +169,7 @@ vt_status vt_fp4_w4a16_gemm_ex(const void* A, int64_t M, int64_t lda, vt_fp4_han
  * gate row i and up row i times their globals, silu(x) = x / (1 + e^-x) in fp32 -- the
  * gate_up GEMM and the SiLU-and-multiply step in one call, without writing the [M][2I]
  * intermediate.  Any M >= 0 (the decode path for M <= 16, the tile path above).
- *   C  (device) bf16 [M][ldc], ldc >= I, 4-byte aligned, ldc even.
+ *   C  (device) bf16 [M][ldc], ldc >= I, 2-byte aligned.
  * Other arguments as for vt_fp4_w4a16_gemm.  A weight not prepacked paired is rejected
  * with VT_ERR_INVALID_ARG. */
 vt_status vt_fp4_w4a16_gemm_silu_mul(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,

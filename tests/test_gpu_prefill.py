@@ -79,16 +79,20 @@ def test_prefill_fused_gate_up_equals_split(fmt):
 @pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
 def test_prefill_deterministic_and_grid_independent(fmt):
     """Each output tile is summed by one CTA in a fixed k order, so the bits do not depend
-    on the number of CTAs."""
+    on the number of CTAs.  Repeated: a CTA that runs many tiles reuses every ring stage
+    many times, so a hand-off race between the kernel's roles shows up as changed bits
+    (one such race, in the release of the packed-weight stages, changed about a quarter of
+    the MXFP4 runs with few CTAs)."""
     N, K, M = 1280, 1536, 260
     W, codes, scales, G = _packed(fmt, N, K, synth.tensor_id(73, fmt, 1))
     Ab = make_acts(synth.tensor_id(73, fmt, 2), M, K)
     A = bf16_dev(Ab)
     ws = W.new_workspace(M)
     first = bf16_host_bits(vt.w4a16_gemm(A, W, workspace=ws))
-    for opts in (None, {"grid": 1}, {"grid": 7}, {"grid": 1000}):
-        again = bf16_host_bits(vt.w4a16_gemm(A, W, workspace=ws, opts=opts))
-        assert np.array_equal(first, again), opts
+    for rep in range(8):
+        for opts in (None, {"grid": 1}, {"grid": 2}, {"grid": 7}, {"grid": 1000}):
+            again = bf16_host_bits(vt.w4a16_gemm(A, W, workspace=ws, opts=opts))
+            assert np.array_equal(first, again), (rep, opts)
     ref, _ = oracle.gemm(fmt, Ab, codes, scales, G, N)
     check_rows((first.astype(np.uint32) << 16).view(np.float32), ref, what="deterministic")
     assert vt.workspace_status(ws) == 0
