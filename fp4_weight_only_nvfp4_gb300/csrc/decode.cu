@@ -1106,7 +1106,8 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids
                            L.status, L.counters, (int64_t)(pmax < kGtMaxProblems ? pmax : kGtMaxProblems) * L.RT);
     if (e != cudaSuccess) return e;
   }
-  // token tile: 8 rows when no expert can have more than 8 pairs (M <= 8), else 16
+  // token tile: 8 rows when M <= 8 (an expert then gets at most 8 pairs; extra pairs from a
+  // token naming one expert twice are skipped by the pre-pass), else 16
   const bool m8 = decode_mt(L.M) == 8;
   if (L.ks == 4)
     e = (L.fmt == FMT_NV) ? (m8 ? launch_t<FMT_NV, 8, 4, true>(L, s) : launch_t<FMT_NV, 16, 4, true>(L, s))
