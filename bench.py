@@ -416,6 +416,15 @@ def run_gpu(args, rank: int, world: int):
     else:
         step_bytes = sum(_work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
     n_calls = len(calls)
+    # A step smaller than twice the L2 would find its weights still in L2 on the next replay:
+    # such a workload rotates over `rot` graphs, step j on the copies shifted by j steps'
+    # worth, so that every timed step reads weights no recent step has read.
+    cps = len({c for c, _, _, _ in calls})
+    rot = 1
+    if not moe and w.kind != "prefill" and step_bytes < 2 * L2_BYTES:
+        rot = max(1, min(copies // cps, int(np.ceil(2 * L2_BYTES / step_bytes))))
+    steps_calls = [[((c + j * cps) % copies, layer, pi, M) for c, layer, pi, M in calls]
+                   for j in range(rot)]
 
     greedy = w.kind == "greedy"
     silu = w.kind == "mlp_silu"
@@ -454,8 +463,8 @@ def run_gpu(args, rank: int, world: int):
         if unfused:  # the unfused greedy step: logits out, then a separate argmax
             torch.argmax(C[(M, p.N)], dim=1)
 
-    def issue(timing_events=None, unfused=False):
-        for i, (c, layer, pi, M) in enumerate(calls):
+    def issue(timing_events=None, unfused=False, j=0):
+        for i, (c, layer, pi, M) in enumerate(steps_calls[j]):
             if timing_events is not None:
                 timing_events[i][0].record(stream)
             one_call(c, layer, pi, M, unfused)
@@ -477,14 +486,25 @@ def run_gpu(args, rank: int, world: int):
     stream.synchronize()
 
     # the timed step: one CUDA graph of all the step's calls, back to back (consecutive
-    # calls overlap through programmatic dependent launch)
-    graph = torch.cuda.CUDAGraph()
+    # calls overlap through programmatic dependent launch); `rot` graphs replayed in turn
+    # when the step alone does not exceed the L2
+    graphs = []
     with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            issue(None)
+        for j in range(rot):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue(None, j=j)
+            graphs.append(g)
         for _ in range(max(3, args.warmup)):
-            graph.replay()
+            for g in graphs:
+                g.replay()
     stream.synchronize()
+    turn = {"next": 0}  # the graph the next step replays
+
+    def replay_step():
+        graphs[turn["next"]].replay()
+        turn["last"] = turn["next"]
+        turn["next"] = (turn["next"] + 1) % rot
 
     dist = None
     if world > 1:
@@ -499,7 +519,7 @@ def run_gpu(args, rank: int, world: int):
             t_end = time.perf_counter() + seconds
             while time.perf_counter() < t_end:
                 for _ in range(8):
-                    graph.replay()
+                    replay_step()
                 stream.synchronize()
 
     sampler = ClockSampler(local)
@@ -513,7 +533,7 @@ def run_gpu(args, rank: int, world: int):
     with torch.cuda.stream(stream):  # replay() launches on the current stream
         t0.record(stream)
         for _ in range(args.steps):
-            graph.replay()
+            replay_step()
         t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -526,29 +546,31 @@ def run_gpu(args, rank: int, world: int):
     ms_step = ms_total / args.steps
     value = job_rate(w, step_bytes, world, ms_step * 1e-3)
     # the outputs of the timed graph, checked before anything else runs on them
-    check = self_check(w, sets, calls, A, C, w.extra.get("w4a4"))
+    check = self_check(w, sets, steps_calls[turn["last"]], A, C, w.extra.get("w4a4"))
 
     # per-call durations: a second graph with an event record node around every call (the
     # event nodes break the overlap between calls, so these durations are slightly larger
     # than the calls' share of the timed step)
+    # (over every rotated step, so that the calls read cold weights here too)
+    all_calls = [x for sc in steps_calls for x in sc]
     try:
-        ev = [(torch.cuda.Event(enable_timing=True, external=True),
-               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_calls)]
+        ev = [[(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_calls)]
+              for _ in range(rot)]
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g2, stream=stream):
-                issue(ev)
+                for j in range(rot):
+                    issue(ev[j], j=j)
             for _ in range(3):
                 g2.replay()
         stream.synchronize()
-        durs = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n_calls)]
+        durs = [e[0].elapsed_time(e[1]) for evj in ev for e in evj]
     except (TypeError, RuntimeError):
         torch.cuda.synchronize()
         durs = []
-        for i in range(n_calls):
+        for c, layer, pi, M in all_calls:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            c, layer, pi, M = calls[i]
-            p = w.projs[pi]
             e0.record(stream)
             one_call(c, layer, pi, M)
             e1.record(stream)
@@ -556,7 +578,7 @@ def run_gpu(args, rank: int, world: int):
             durs.append(e0.elapsed_time(e1))
     per_call = []
     agg = {}
-    for i, (c, layer, pi, M) in enumerate(calls):
+    for i, (c, layer, pi, M) in enumerate(all_calls):
         p = w.projs[pi]
         key = (p.name, M)
         b = moe_bytes[(c, M)] if moe else _work(w, p.N, p.K, M)
@@ -568,7 +590,7 @@ def run_gpu(args, rank: int, world: int):
         us = ms * 1e3 / n
         per_call.append({"proj": name, "M": M, "us_per_call": round(us, 3),
                          w.unit.replace("/", "p"): round(_rate(w, b / n, us * 1e-6), 1)})
-    kernel_ms = sum(durs)
+    kernel_ms = sum(durs) / rot
     unfused = None
     if greedy or silu:
         # the same step with the logits written and a separate argmax per call
@@ -598,13 +620,14 @@ def run_gpu(args, rank: int, world: int):
 
     # end to end: pinned host activations in, host logits out, every call
     e2e = (run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route)
-           if moe else run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist))
+           if moe else run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world,
+                               dist))
     ws_status = vt.workspace_status(ws, stream)
     return {
         "value": value, "ms_per_step": ms_step, "step_bytes": step_bytes, "clocks": clocks,
         "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "copies": copies,
-        "calls_per_step": n_calls, "ws_status": ws_status, "unfused": unfused,
+        "calls_per_step": n_calls, "rotation": rot, "ws_status": ws_status, "unfused": unfused,
         "self_check": check,
     }
 
@@ -638,27 +661,33 @@ class _Slots:
             self.host[:self.nbytes].copy_(self.dev[:self.nbytes], non_blocking=True)
 
 
-def _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, h2d, d2h):
-    """Warm-up, one CUDA graph of the step (copy in, every call, copy out), timed replays."""
+def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h):
+    """Warm-up, one CUDA graph per rotated step (copy in, every call, copy out), timed
+    replays in turn."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
-            issue()
+            for issue in issues:
+                issue()
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    graphs = []
     with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            issue()
+        for issue in issues:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue()
+            graphs.append(g)
         for _ in range(3):
-            graph.replay()
+            for g in graphs:
+                g.replay()
     stream.synchronize()
     if dist:
         dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
+        for st in range(args.steps):
+            graphs[st % len(graphs)].replay()
         t1.record(stream)
     stream.synchronize()
     ms_step = max_over_ranks(t0.elapsed_time(t1), dist, dev) / args.steps
@@ -667,55 +696,60 @@ def _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, h2d, d2h):
             "copies_per_step": 2}
 
 
-def run_e2e(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist):
+def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist):
     """The step end to end through the public API: every call's activations from pinned host
     memory (one host-to-device copy of the step's inputs), the calls, and every call's
     result back to pinned host memory (one device-to-host copy), all inside the timed
-    region."""
+    region.  steps_calls: the rotated steps (one, unless a step alone fits the L2)."""
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
     greedy = w.kind == "greedy"
     silu = w.kind in ("mlp_silu",)
     a4 = w.extra.get("w4a4")
-    # MLP chain: the host input feeds gate_up, down's output goes back; act stays on device
-    host_in = [not (silu and not w.projs[pi].fused) for _, _, pi, _ in calls]
-    host_out = [not (silu and w.projs[pi].fused) for _, _, pi, _ in calls]
-    IN = _Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
-                 for i, (_, _, pi, M) in enumerate(calls)], dev)
-    OUT = _Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
-                  for i, (_, _, pi, M) in enumerate(calls)], dev)
-    for i, (_, _, pi, M) in enumerate(calls):
-        if host_in[i]:
-            IN.view(i, (M, w.projs[pi].K), torch.bfloat16, host=True).copy_(
-                torch.randn((M, w.projs[pi].K)).to(torch.bfloat16))
     I_mlp = max((p.I for p in w.projs if p.fused), default=0)
     dAct = {M: torch.empty((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms} if silu else {}
 
-    def issue():
-        IN.to_dev()
-        for i, (c, layer, pi, M) in enumerate(calls):
-            p, W = w.projs[pi], sets[c][layer][pi]
-            if silu:
-                if p.fused:
-                    vt.w4a16_gemm_silu_mul(IN.view(i, (M, p.K), torch.bfloat16), W, out=dAct[M],
-                                           workspace=ws, stream=stream)
-                else:
-                    vt.w4a16_gemm(dAct[M], W, out=OUT.view(i, (M, p.N), torch.bfloat16),
-                                  workspace=ws, stream=stream)
-                continue
-            A = IN.view(i, (M, p.K), torch.bfloat16)
-            if greedy:
-                vt.w4a16_gemm_greedy(A, W, workspace=ws, stream=stream, want_value=False,
-                                     token=OUT.view(i, (M,), torch.int32))
-            elif a4 is not None:
-                vt.w4a4_gemm(A, W, a4, out=OUT.view(i, (M, p.N), torch.bfloat16), workspace=ws,
-                             stream=stream)
-            else:
-                vt.w4a16_gemm(A, W, out=OUT.view(i, (M, p.N), torch.bfloat16), workspace=ws,
-                              stream=stream)
-        OUT.to_host()
+    def make_step(calls):
+        # MLP chain: the host input feeds gate_up, down's output goes back; act stays on device
+        host_in = [not (silu and not w.projs[pi].fused) for _, _, pi, _ in calls]
+        host_out = [not (silu and w.projs[pi].fused) for _, _, pi, _ in calls]
+        IN = _Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
+                     for i, (_, _, pi, M) in enumerate(calls)], dev)
+        OUT = _Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
+                      for i, (_, _, pi, M) in enumerate(calls)], dev)
+        for i, (_, _, pi, M) in enumerate(calls):
+            if host_in[i]:
+                IN.view(i, (M, w.projs[pi].K), torch.bfloat16, host=True).copy_(
+                    torch.randn((M, w.projs[pi].K)).to(torch.bfloat16))
 
-    return _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, IN.nbytes, OUT.nbytes)
+        def issue():
+            IN.to_dev()
+            for i, (c, layer, pi, M) in enumerate(calls):
+                p, W = w.projs[pi], sets[c][layer][pi]
+                if silu:
+                    if p.fused:
+                        vt.w4a16_gemm_silu_mul(IN.view(i, (M, p.K), torch.bfloat16), W,
+                                               out=dAct[M], workspace=ws, stream=stream)
+                    else:
+                        vt.w4a16_gemm(dAct[M], W, out=OUT.view(i, (M, p.N), torch.bfloat16),
+                                      workspace=ws, stream=stream)
+                    continue
+                A = IN.view(i, (M, p.K), torch.bfloat16)
+                if greedy:
+                    vt.w4a16_gemm_greedy(A, W, workspace=ws, stream=stream, want_value=False,
+                                         token=OUT.view(i, (M,), torch.int32))
+                elif a4 is not None:
+                    vt.w4a4_gemm(A, W, a4, out=OUT.view(i, (M, p.N), torch.bfloat16),
+                                 workspace=ws, stream=stream)
+                else:
+                    vt.w4a16_gemm(A, W, out=OUT.view(i, (M, p.N), torch.bfloat16),
+                                  workspace=ws, stream=stream)
+            OUT.to_host()
+        return issue, IN.nbytes, OUT.nbytes
+
+    steps = [make_step(sc) for sc in steps_calls]
+    return _time_e2e(args, w, [st[0] for st in steps], stream, dev, step_bytes, world, dist,
+                     steps[0][1], steps[0][2])
 
 
 def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
@@ -743,7 +777,7 @@ def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, 
                               stream=stream)
         OUT.to_host()
 
-    return _time_e2e(args, w, issue, stream, dev, step_bytes, world, dist, IN.nbytes, OUT.nbytes)
+    return _time_e2e(args, w, [issue], stream, dev, step_bytes, world, dist, IN.nbytes, OUT.nbytes)
 
 
 # ---------------------------------------------------------------- CPU (oracle) leg
@@ -913,7 +947,9 @@ def main():
                        l2=(f"{r['copies']} weight copies rotate (one per M); activations and "
                            f"weight tiles are reused through L2 by design" if prefill else
                            f"inputs larger than L2: {r['copies']} weight copies rotate, "
-                           f"{r['step_bytes'] / 1e6:.1f} MB streamed per step"),
+                           f"{r['step_bytes'] / 1e6:.1f} MB streamed per step" +
+                           (f"; the step fits the L2, so {r['rotation']} graphs, each on "
+                            f"other copies, are replayed in turn" if r['rotation'] > 1 else "")),
                        calls_per_step=r["calls_per_step"]),
         "roofline": {"bound": "tensor" if prefill else "hbm",
                      "kernel": ("k_prefill (+ k_prep_rows, one GEMM call)" if prefill else
