@@ -661,7 +661,7 @@ class _Slots:
             self.host[:self.nbytes].copy_(self.dev[:self.nbytes], non_blocking=True)
 
 
-def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h):
+def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h, copies=2):
     """Warm-up, one CUDA graph per rotated step (copy in, every call, copy out), timed
     replays in turn."""
     import torch
@@ -693,7 +693,7 @@ def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h):
     ms_step = max_over_ranks(t0.elapsed_time(t1), dist, dev) / args.steps
     return {"value": round(job_rate(w, step_bytes, world, ms_step * 1e-3), 2), "unit": w.unit,
             "ms_per_step": round(ms_step, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "copies_per_step": 2}
+            "copies_per_step": copies}
 
 
 def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist):
@@ -708,6 +708,9 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
     a4 = w.extra.get("w4a4")
     I_mlp = max((p.I for p in w.projs if p.fused), default=0)
     dAct = {M: torch.empty((M, I_mlp), dtype=torch.bfloat16, device=dev) for M in w.Ms} if silu else {}
+    # prefill outputs are large (tens to hundreds of MB): each call's result goes back on a
+    # second stream while the next call computes; decode results (KB) go back in one copy
+    side = torch.cuda.Stream(device=dev) if w.kind == "prefill" else None
 
     def make_step(calls):
         # MLP chain: the host input feeds gate_up, down's output goes back; act stays on device
@@ -744,12 +747,21 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
                 else:
                     vt.w4a16_gemm(A, W, out=OUT.view(i, (M, p.N), torch.bfloat16),
                                   workspace=ws, stream=stream)
-            OUT.to_host()
+                if side is not None:
+                    side.wait_stream(stream)
+                    with torch.cuda.stream(side):
+                        OUT.view(i, (M, p.N), torch.bfloat16, host=True).copy_(
+                            OUT.view(i, (M, p.N), torch.bfloat16), non_blocking=True)
+            if side is not None:
+                stream.wait_stream(side)
+            else:
+                OUT.to_host()
         return issue, IN.nbytes, OUT.nbytes
 
     steps = [make_step(sc) for sc in steps_calls]
     return _time_e2e(args, w, [st[0] for st in steps], stream, dev, step_bytes, world, dist,
-                     steps[0][1], steps[0][2])
+                     steps[0][1], steps[0][2],
+                     copies=1 + (len(steps_calls[0]) if side is not None else 1))
 
 
 def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
