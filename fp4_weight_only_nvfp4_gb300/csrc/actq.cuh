@@ -13,6 +13,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "common.cuh"  // act_maxmag8: a granule's largest magnitude (>= 0x7F80: inf or NaN)
+
 namespace vt {
 
 // Nearest point of the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code,
@@ -98,18 +100,6 @@ __device__ __forceinline__ uint32_t aq_mx_code(float x, float inv) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Largest bf16 magnitude pattern (sign cleared) among the 8 values of a 16-byte granule;
-// patterns >= 0x7F80 are inf or NaN.
-__device__ __forceinline__ int bf16_maxmag8(const uint32_t w[4]) {
-  int mx = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    mx = max(mx, (int)(w[q] & 0x7FFFu));
-    mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
-  }
-  return mx;
-}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);

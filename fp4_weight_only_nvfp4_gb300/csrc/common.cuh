@@ -235,6 +235,44 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// ---------------------------------------------------- activation conversion (bf16 -> f16)
+// A tile of bf16 activations becomes f16 values A * 2^-p with one power of two p per tile:
+// p = (exponent of the largest magnitude) - 14, clamped to [-120, 113], so that every value
+// lands below 2^15 and values down to about 2^-31 of the largest one keep all their bits (the
+// f16 subnormals end at 2^-24); p = 0 for an all-zero tile or one holding a NaN (infinities
+// and NaNs pass through as such).
+
+// Largest bf16 magnitude pattern (sign cleared) among the 8 values of a 16-byte granule.
+__device__ __forceinline__ int act_maxmag8(const uint32_t w[4]) {
+  int mx = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    mx = max(mx, (int)(w[q] & 0x7FFFu));
+    mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
+  }
+  return mx;
+}
+
+// The tile's power of two from its largest magnitude pattern.
+__device__ __forceinline__ int act_pow2(int mx) {
+  if (mx <= 0 || mx > 0x7F80) return 0;
+  const int p = ((mx >> 7) - 127) - 14;  // exponent of the largest magnitude (subnormals: -127)
+  return p < -120 ? -120 : (p > 113 ? 113 : p);
+}
+
+// One granule times 2^-p, rounded to f16, as four f16x2 words.
+__device__ __forceinline__ uint4 act_granule_f16(const uint32_t w[4], int p) {
+  const float down = ldexpf(1.0f, -p);
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * down,
+                                        __uint_as_float(w[q] & 0xFFFF0000u) * down);
+    o[q] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ int4 ld_global_nc_v4(const void* p) {
   int4 v;
   asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"

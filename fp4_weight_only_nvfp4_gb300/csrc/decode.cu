@@ -107,32 +107,13 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep_a(const __nv_bfloat16* __
   uint4 v = make_uint4(0, 0, 0, 0);
   if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  int mx = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    mx = max(mx, (int)(w[q] & 0x7FFFu));
-    mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
-  }
+  int mx = act_maxmag8(w);
 #pragma unroll
   for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (kt >= KT) return;
-  int p = 0;
-  if (mx > 0 && mx <= 0x7F80) {
-    const int e = (mx >> 7) - 127;  // exponent of the largest magnitude (subnormals: -127)
-    p = e - 14;
-    p = p < -120 ? -120 : (p > 113 ? 113 : p);
-  }
-  const float down = ldexpf(1.0f, -p);
-  uint32_t o[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float lo = __uint_as_float(w[q] << 16) * down;
-    const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
-    __half2 h = __floats2half2_rn(lo, hi);
-    o[q] = *reinterpret_cast<uint32_t*>(&h);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8)));
-  *dst = make_uint4(o[0], o[1], o[2], o[3]);
+  const int p = act_pow2(mx);
+  *reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8))) =
+      act_granule_f16(w, p);
   if (gi == 0) ascale[kt * kAScaleStride + m] = ldexpf(1.0f, p);
 }
 
@@ -159,7 +140,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep_a4(const __nv_bfloat16* _
   if (kt < KT && k0 < K) v = __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0));
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   // the group's largest magnitude: 2 granules (NVFP4) or 4 (MXFP4) in adjacent lanes
-  int mg = bf16_maxmag8(w);
+  int mg = act_maxmag8(w);
   mg = max(mg, __shfl_xor_sync(0xffffffffu, mg, 1));
   if constexpr (FMT == FMT_MX) mg = max(mg, __shfl_xor_sync(0xffffffffu, mg, 2));
   const int mt = max(min(mg, 0x7F7F), __shfl_xor_sync(0xffffffffu, min(mg, 0x7F7F), 4));
@@ -557,32 +538,14 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       uint4 v = make_uint4(0, 0, 0, 0);
       if (valid && k0 < p.K) v = __ldg(reinterpret_cast<const uint4*>(A + m * p.lda + k0));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      int mx = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        mx = max(mx, (int)(w[q] & 0x7FFFu));
-        mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
-      }
+      int mx = act_maxmag8(w);
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       if (valid) {
-        int pe = 0;
-        if (mx > 0 && mx <= 0x7F80) {
-          const int e = (mx >> 7) - 127;
-          pe = e - 14;
-          pe = pe < -120 ? -120 : (pe > 113 ? 113 : pe);
-        }
-        const float down = ldexpf(1.0f, -pe);
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(w[q] << 16) * down;
-          const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
-          __half2 h = __floats2half2_rn(lo, hi);
-          o[q] = *reinterpret_cast<uint32_t*>(&h);
-        }
+        const int pe = act_pow2(mx);
+        const uint4 o = act_granule_f16(w, pe);
         st_shared_v4(res_u + (uint32_t)(((ktr * M + m) * 64 + ((gi ^ (m & 7)) * 8)) * 2),
-                     o[0], o[1], o[2], o[3]);
+                     o.x, o.y, o.z, o.w);
         if (gi == 0) st_shared_f32(rscale_u + (uint32_t)((ktr * kResScaleStride + m) * 4), ldexpf(1.0f, pe));
       }
     }
@@ -1055,32 +1018,13 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
     const int m = s_pair[sx] / topk;
     const uint4 v = s_a[m * (kPrepTiles * 8) + (tid & 63)];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    int mx = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mx = max(mx, (int)(w[q] & 0x7FFFu));
-      mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
-    }
+    int mx = act_maxmag8(w);
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (kt >= KT) continue;
-    int pe = 0;
-    if (mx > 0 && mx <= 0x7F80) {
-      pe = ((mx >> 7) - 127) - 14;
-      pe = pe < -120 ? -120 : (pe > 113 ? 113 : pe);
-    }
-    const float down = ldexpf(1.0f, -pe);
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(w[q] << 16) * down;
-      const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
-      __half2 h = __floats2half2_rn(lo, hi);
-      o[q] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(
-        Ap + ((rsum * KT + kt * cnt + sx) * 64 + ((gi ^ (sx & 7)) * 8)));
-    *dst = make_uint4(o[0], o[1], o[2], o[3]);
+    const int pe = act_pow2(mx);
+    *reinterpret_cast<uint4*>(Ap + ((rsum * KT + kt * cnt + sx) * 64 + ((gi ^ (sx & 7)) * 8))) =
+        act_granule_f16(w, pe);
     if (gi == 0) ascale[((int64_t)b * KT + kt) * kAScaleStride + sx] = ldexpf(1.0f, pe);
   }
 }

@@ -512,11 +512,7 @@ __global__ void __launch_bounds__(kRowThreads) k_prep_rows(const __nv_bfloat16* 
   for (int64_t i = threadIdx.x; i < ng; i += kRowThreads) {
     const uint4 v = __ldg(row + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mx = max(mx, (int)(w[q] & 0x7FFFu));
-      mx = max(mx, (int)((w[q] >> 16) & 0x7FFFu));
-    }
+    mx = max(mx, act_maxmag8(w));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -525,26 +521,12 @@ __global__ void __launch_bounds__(kRowThreads) k_prep_rows(const __nv_bfloat16* 
   mx = 0;
 #pragma unroll
   for (int i = 0; i < kRowThreads / 32; ++i) mx = max(mx, s_max[i]);
-  int p = 0;
-  if (mx > 0 && mx <= 0x7F80) {
-    const int e = (mx >> 7) - 127;
-    p = e - 14;
-    p = p < -120 ? -120 : (p > 113 ? 113 : p);
-  }
-  const float down = ldexpf(1.0f, -p);
+  const int p = act_pow2(mx);
   uint4* dst = reinterpret_cast<uint4*>(Ap + m * ldp);
   for (int64_t i = threadIdx.x; i < ng; i += kRowThreads) {
     const uint4 v = __ldg(row + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(w[q] << 16) * down;
-      const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * down;
-      __half2 h = __floats2half2_rn(lo, hi);
-      o[q] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[i] = act_granule_f16(w, p);
   }
   if (threadIdx.x == 0) rowscale[m] = ldexpf(1.0f, p);
 }
@@ -571,7 +553,7 @@ __global__ void __launch_bounds__(kRowThreads) k_prep_rows4(const __nv_bfloat16*
     for (int64_t i = threadIdx.x; i < K / 8; i += kRowThreads) {
       const uint4 v = __ldg(row + i);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      mx = max(mx, min(bf16_maxmag8(w), 0x7F7F));
+      mx = max(mx, min(act_maxmag8(w), 0x7F7F));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -593,7 +575,7 @@ __global__ void __launch_bounds__(kRowThreads) k_prep_rows4(const __nv_bfloat16*
       w[v][1] = x.y;
       w[v][2] = x.z;
       w[v][3] = x.w;
-      mg = max(mg, bf16_maxmag8(w[v]));
+      mg = max(mg, act_maxmag8(w[v]));
     }
     const bool bad = mg >= 0x7F80;
     const float amax = __uint_as_float((uint32_t)(bad ? 0 : mg) << 16);

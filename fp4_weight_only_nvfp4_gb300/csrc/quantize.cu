@@ -187,7 +187,7 @@ __global__ void k_qa(const uint16_t* __restrict__ A, int64_t M, int64_t lda, int
     w[v][1] = x.y;
     w[v][2] = x.z;
     w[v][3] = x.w;
-    mx = max(mx, bf16_maxmag8(w[v]));
+    mx = max(mx, act_maxmag8(w[v]));
   }
   const bool bad = mx >= 0x7F80;
   const float amax = __uint_as_float((uint32_t)(bad ? 0 : mx) << 16);
