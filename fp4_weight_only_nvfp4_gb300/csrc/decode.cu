@@ -47,6 +47,10 @@ constexpr int kPrefetchStages = VT_DECODE_PREFETCH;  // stages requested before 
 #define VT_RESIDENT_PREFETCH 2
 #endif
 constexpr int kResidentPrefetch = VT_RESIDENT_PREFETCH;  // resident mode: stages before A is in
+#ifndef VT_GROUPED_PREFETCH
+#define VT_GROUPED_PREFETCH 2
+#endif
+constexpr int kGroupedPrefetch = VT_GROUPED_PREFETCH;  // grouped mode: stages before the pre-pass ends
 
 int decode_mt(int M) { return M <= 8 ? 8 : 16; }
 
@@ -190,6 +194,8 @@ struct DecodeParams {
   int64_t lda, K;
   const uint8_t* gbase;        // expert e's packed weight at gbase + e * expert_bytes
   int64_t expert_bytes, RT;    // bytes per expert; 128-row tiles per expert
+  const int32_t* topk_ids;     // grouped mode: the routing, grouped again by the kernel itself
+  int npairs, E;
 };
 
 // SiLU(x) = x / (1 + e^-x) in fp32 (e^-x overflowing to infinity gives -0 for large -x).
@@ -271,6 +277,84 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
+// ---------------------------------------------------------------- routing grouping
+// Mixture-of-experts decode groups the (token m, slot j) pairs of topk_ids[M][topk] into
+// problems, one per expert in use, in increasing expert order, with each problem's pairs in
+// increasing pair order (m * topk + j), so that the grouping, and every output bit, does not
+// depend on the routing's order.  The first 128 threads of a block compute it, one pair per
+// thread: a rank sort of the keys (expert << 8 | pair; an id outside [0, E) sorts last),
+// then scans for each pair's problem, its slot in the problem and the problem's first row.
+// A pair at slot >= cap (the decode kernel's token tile; only a token naming one expert
+// several times can get there, since M <= cap) is not kept.  Both the activation pre-pass
+// and the grouped decode kernel compute it, from the same ids, to the same result.
+constexpr int kGroupThreads = 128;  // one pair per thread: M * topk <= 128
+
+// Barrier over the block's first 128 threads: named barrier BAR (0 = the whole block, when it
+// has exactly 128 threads).
+template <int BAR>
+__device__ __forceinline__ void group_sync() {
+  asm volatile("bar.sync %0, 128;" ::"n"(BAR) : "memory");
+}
+
+// Inclusive scan (sum or max) over the 128 threads' values.
+template <int BAR, bool MAX>
+__device__ __forceinline__ int group_scan(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = MAX ? max(v, u) : v + u;
+  }
+  if (lane == 31) s_warp[w] = v;
+  group_sync<BAR>();
+  for (int q = 0; q < w; ++q) v = MAX ? max(v, s_warp[q]) : v + s_warp[q];
+  group_sync<BAR>();
+  return v;
+}
+
+__device__ __forceinline__ uint32_t pair_key(int e, int i, int E) {
+  return (e >= 0 && e < E) ? (((uint32_t)e << 8) | (uint32_t)i) : 0xFFFFFFFFu;
+}
+
+// Thread t's result describes sorted position t: its pair, expert, problem, slot, whether it
+// is kept, heads its problem (then rsum = the problem's first row) or is its problem's last
+// kept pair; prob + 1 at t = 127 is the number of problems.
+struct PairPlace {
+  int e, pair, prob, slot, rsum;
+  bool valid, kept, head, last;
+};
+
+template <int BAR>
+__device__ __forceinline__ PairPlace group_pairs(uint32_t key, int cap, uint32_t* s_in,
+                                                 uint32_t* s_key, int* s_warp) {
+  const int tid = threadIdx.x;
+  s_in[tid] = key;
+  group_sync<BAR>();
+  int rank = 0;  // smaller keys, ties (the invalid ones) broken by position
+#pragma unroll 8
+  for (int j = 0; j < kGroupThreads; ++j) {
+    const uint32_t x = s_in[j];
+    rank += (x < key) | ((x == key) & (j < tid));
+  }
+  s_key[rank] = key;
+  group_sync<BAR>();
+  PairPlace q;
+  key = s_key[tid];
+  q.valid = key != 0xFFFFFFFFu;
+  q.e = (int)(key >> 8);
+  q.pair = (int)(key & 0xFFu);
+  q.head = q.valid && (tid == 0 || (s_key[tid - 1] >> 8) != key >> 8);
+  const int first = group_scan<BAR, true>(q.head ? tid : 0, s_warp);
+  q.slot = tid - first;
+  q.kept = q.valid && q.slot < cap;
+  q.prob = group_scan<BAR, false>(q.head ? 1 : 0, s_warp) - 1;
+  q.rsum = group_scan<BAR, false>(q.kept ? 1 : 0, s_warp) - 1;  // kept pairs before this one
+  q.last = q.kept && (tid + 1 == kGroupThreads || !(s_key[tid + 1] != 0xFFFFFFFFu &&
+                                                   (s_key[tid + 1] >> 8) == key >> 8 &&
+                                                   q.slot + 1 < cap));
+  return q;
+}
+
 // CTA layout: 16 consumer warps, one producer warp and one publisher warp.  A stage holds
 // up to KS consecutive k tiles of one 128-row tile (one TMA bulk copy of the weights, one
 // of the matching activation slices, one of their scales); consumer warp w owns the
@@ -306,9 +390,28 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   // for this grid to finish before it touches anything this grid reads or writes.
   pdl_launch_dependents();
 
-  // grouped mode: the number of problems comes from the pre-pass, so every role waits for
-  // it first (the weights to stream depend on the routing)
-  if constexpr (GRP) pdl_wait();
+  // Grouped mode: the weights to stream depend on the routing, so the block's first 128
+  // threads group the pairs first, from topk_ids (complete: the pre-pass lets this kernel
+  // launch only after its own wait), as the pre-pass does; the producer can then request
+  // weights while the pre-pass still converts the activations.
+  __shared__ uint32_t s_rin[GRP ? kGroupThreads : 1], s_rkey[GRP ? kGroupThreads : 1];
+  __shared__ int s_rwarp[4], s_rP;
+  __shared__ int s_rexp[GRP ? kGtMaxProblems : 1], s_rcnt[GRP ? kGtMaxProblems : 1];
+  __shared__ int s_rrsum[GRP ? kGtMaxProblems : 1];
+  if constexpr (GRP) {
+    if (threadIdx.x < kGroupThreads) {
+      const int tid = threadIdx.x;
+      const uint32_t key = tid < p.npairs ? pair_key(__ldcg(p.topk_ids + tid), tid, p.E) : 0xFFFFFFFFu;
+      const PairPlace q = group_pairs<2>(key, MT, s_rin, s_rkey, s_rwarp);
+      if (q.kept && q.head) {
+        s_rexp[q.prob] = q.e;
+        s_rrsum[q.prob] = q.rsum;
+      }
+      if (q.last) s_rcnt[q.prob] = q.slot + 1;
+      if (tid == kGroupThreads - 1) s_rP = q.prob + 1;
+    }
+    __syncthreads();
+  }
   const int S = p.stages;
   const int M = GRP ? MT : p.M;  // rows of the stage's activation area
   // stage: weights | activation slices (M rows of 128 B per k tile) | activation scales;
@@ -317,7 +420,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   const int STAGE = RA ? WBYTES : SCALES_OFF + KS * kAScaleStride * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t G = gridDim.x, c = blockIdx.x, KT = p.KT;
-  const int64_t I = GRP ? (int64_t)p.gtab[kGtP] * p.RT * KT : p.items;
+  const int64_t I = GRP ? (int64_t)s_rP * p.RT * KT : p.items;
   const int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
 
   float* slots = reinterpret_cast<float*>(smem + (size_t)S * STAGE);
@@ -369,7 +472,9 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   if constexpr (GRP) {
     if (warp == CW) {
       // --------------------------------------------------------- producer (grouped)
-      // virtual row tile rt = problem * RT + rt_l; the weights of expert e = expert[problem]
+      // virtual row tile rt = problem * RT + rt_l; the weights of expert e = expert[problem].
+      // As in the dense producer, the first stages' weights are requested before the
+      // activation pre-pass has finished and their activation copies once it has.
       if (lane == 0 && !p.withhold) {
         const uint64_t pol = l2_evict_first_policy();
         const uint64_t pol_a = l2_evict_last_policy();
@@ -380,11 +485,31 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         int64_t rtl = rt - (int64_t)prob * p.RT;
         int e = 0, cnt = 0, rsum = 0;
         if (pos < i1) {
-          e = p.gtab[kGtExpert + prob];
-          cnt = p.gtab[kGtCount + prob];
-          rsum = p.gtab[kGtRowsum + prob];
+          e = s_rexp[prob];
+          cnt = s_rcnt[prob];
+          rsum = s_rrsum[prob];
         }
+        // the activation slices and scales of a stage (pre-pass layout of problem pr)
+        auto act_copies = [&](int sl, int n, int ktv, int pr, int cn, int rs) {
+          const uint32_t dst = ring_u + sl * STAGE;
+          bulk_g2s(dst + WBYTES, p.Ap + ((int64_t)rs * KT + (int64_t)ktv * cn) * 64,
+                   (uint32_t)(n * cn * 128), full_u + 8 * sl, pol_a);
+          bulk_g2s(dst + SCALES_OFF, p.ascale + ((int64_t)pr * KT + ktv) * kAScaleStride,
+                   (uint32_t)(n * kAScaleStride * 4), full_u + 8 * sl, pol_a);
+        };
+        const int PF = S < kGroupedPrefetch ? S : kGroupedPrefetch;
+        int pf_n[kGroupedPrefetch], pf_kt[kGroupedPrefetch], pf_pr[kGroupedPrefetch];
+        int pf_cnt[kGroupedPrefetch], pf_rs[kGroupedPrefetch];
+        bool waited = false;
+        auto finish_prefetch = [&]() {
+          pdl_wait();
+          fence_proxy_async_all();
+          waited = true;
+          for (int s2 = 0; s2 < issued && s2 < PF; ++s2)
+            act_copies(s2, pf_n[s2], pf_kt[s2], pf_pr[s2], pf_cnt[s2], pf_rs[s2]);
+        };
         while (pos < i1) {
+          if (!waited && issued == PF) finish_prefetch();
           if (issued >= S && !mbar_wait_bounded(empty_u + 8 * slot, par ^ 1u, p.wait_ns)) {
             atomicExch(p.status, 5);
             break;
@@ -394,10 +519,15 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           mbar_expect_tx(full_u + 8 * slot, (uint32_t)(n * (TB + cnt * 128 + kAScaleStride * 4)));
           bulk_g2s(dst, p.gbase + e * p.expert_bytes + kHeaderBytes + (rtl * KT + kt) * TB,
                    (uint32_t)(n * TB), full_u + 8 * slot, pol);
-          bulk_g2s(dst + WBYTES, p.Ap + ((int64_t)rsum * KT + (int64_t)kt * cnt) * 64,
-                   (uint32_t)(n * cnt * 128), full_u + 8 * slot, pol_a);
-          bulk_g2s(dst + SCALES_OFF, p.ascale + ((int64_t)prob * KT + kt) * kAScaleStride,
-                   (uint32_t)(n * kAScaleStride * 4), full_u + 8 * slot, pol_a);
+          if (waited) {
+            act_copies(slot, n, kt, prob, cnt, rsum);
+          } else {  // slot == issued here
+            pf_n[issued] = n;
+            pf_kt[issued] = kt;
+            pf_pr[issued] = prob;
+            pf_cnt[issued] = cnt;
+            pf_rs[issued] = rsum;
+          }
           ++issued;
           pos += n;
           kt += n;
@@ -406,9 +536,9 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
             if (++rtl == p.RT && pos < i1) {
               rtl = 0;
               ++prob;
-              e = p.gtab[kGtExpert + prob];
-              cnt = p.gtab[kGtCount + prob];
-              rsum = p.gtab[kGtRowsum + prob];
+              e = s_rexp[prob];
+              cnt = s_rcnt[prob];
+              rsum = s_rrsum[prob];
             }
           }
           if (++slot == S) {
@@ -416,6 +546,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
             par ^= 1u;
           }
         }
+        if (!waited) finish_prefetch();
       }
       return;
     }
@@ -518,7 +649,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   }
 
   // ---------------------------------------------------------------- consumers
-  if constexpr (!GRP) pdl_wait();
+  pdl_wait();
   if constexpr (RA) {
     // The activation conversion of the pre-pass, done here into shared memory: A[m][k]
     // (bf16) -> A'[kt][m][64] (f16) = A * 2^-p with one power of two p per (token m, 64-wide
@@ -581,10 +712,10 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       const int pr = (int)(rt / p.RT);
       if (pr != gprob) {
         gprob = pr;
-        Mc = p.gtab[kGtCount + pr];
-        grow = p.gtab + kGtPair + pr * 16;
+        Mc = s_rcnt[pr];
+        grow = p.gtab + kGtPair + pr * 16;  // written by the pre-pass (complete: waited above)
         const PackedHeader* he = reinterpret_cast<const PackedHeader*>(
-            p.gbase + p.gtab[kGtExpert + pr] * p.expert_bytes);
+            p.gbase + (int64_t)s_rexp[pr] * p.expert_bytes);
         f0 = f1 = he->factor[0];
       }
     }
@@ -890,6 +1021,9 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
   p.lda = L.lda;
   p.K = L.K;
+  p.topk_ids = L.topk_ids;
+  p.npairs = L.npairs;
+  p.E = L.E;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
@@ -916,31 +1050,15 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
 // decode kernel's token tile holds `cap` rows; only a token naming one expert several times
 // can get there, since M <= cap), sets status 6 and is left out (its output row is not
 // written).
-constexpr int kGroupThreads = 128;  // one (token, slot) pair per thread: M * topk <= 128
-
-// Block-wide inclusive scan (sum or max) over the 128 threads' values.
-template <bool MAX>
-__device__ __forceinline__ int block_scan128(int v, int* s_warp) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v = MAX ? max(v, u) : v + u;
-  }
-  if (lane == 31) s_warp[w] = v;
-  __syncthreads();
-  for (int q = 0; q < w; ++q) v = MAX ? max(v, s_warp[q]) : v + s_warp[q];
-  __syncthreads();
-  return v;
-}
-
 __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
     const __nv_bfloat16* __restrict__ A, int64_t lda, int64_t K, int64_t KT,
     const int32_t* __restrict__ topk_ids, int npairs, int topk, int E, int cap,
     __half* __restrict__ Ap, float* __restrict__ ascale, int* __restrict__ gtab,
     int* __restrict__ status, int* __restrict__ counters, int64_t ncounters) {
-  pdl_launch_dependents();
+  // The grouped decode kernel reads topk_ids itself as soon as it starts: it may launch only
+  // once whatever wrote them has finished, that is after this wait.
   pdl_wait();
+  pdl_launch_dependents();
   zero_counters(counters, ncounters);
   __shared__ uint32_t s_in[kGroupThreads], s_key[kGroupThreads];
   __shared__ int s_warp[kGroupThreads / 32];
@@ -956,52 +1074,29 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
     const int64_t k0 = ((int64_t)blockIdx.y * kPrepTiles + (r >> 3)) * 64 + (r & 7) * 8;
     s_a[i] = k0 < K ? __ldg(reinterpret_cast<const uint4*>(A + m * lda + k0)) : make_uint4(0, 0, 0, 0);
   }
-  // Sort the pairs by (expert, pair index) -- an invalid id sorts last -- by rank: the
-  // number of smaller keys, ties (the invalid ones) broken by position.
-  uint32_t key = 0xFFFFFFFFu;
-  if (tid < npairs) {
-    const int e = topk_ids[tid];
-    if (e >= 0 && e < E) key = ((uint32_t)e << 8) | (uint32_t)tid;
-    else if (lead) atomicExch(status, 6);
-  }
-  s_in[tid] = key;
-  __syncthreads();
-  int rank = 0;
-#pragma unroll 8
-  for (int j = 0; j < kGroupThreads; ++j) {
-    const uint32_t x = s_in[j];
-    rank += (x < key) | ((x == key) & (j < tid));
-  }
-  s_key[rank] = key;
-  __syncthreads();
-  // Sorted position tid: its expert's run starts at `first`; its slot in the run is
-  // tid - first; a pair at slot >= cap does not fit the decode kernel's token tile.
-  key = s_key[tid];
-  const bool valid = key != 0xFFFFFFFFu;
-  const int e = (int)(key >> 8), pair = (int)(key & 0xFFu);
-  const bool head = valid && (tid == 0 || (s_key[tid - 1] >> 8) != key >> 8);
-  const int first = block_scan128<true>(head ? tid : 0, s_warp);
-  const int slot = tid - first;
-  const bool kept = valid && slot < cap;
-  if (valid && !kept && lead) atomicExch(status, 6);
-  const int prob = block_scan128<false>(head ? 1 : 0, s_warp) - 1;  // problem index
-  const int kept_incl = block_scan128<false>(kept ? 1 : 0, s_warp);
-  const bool last = kept && (tid + 1 == kGroupThreads || !(s_key[tid + 1] != 0xFFFFFFFFu &&
-                                                         (s_key[tid + 1] >> 8) == key >> 8 &&
-                                                         slot + 1 < cap));
+  // the grouping (see group_pairs); an invalid id or a pair beyond its expert's token tile
+  // is reported (status 6) and left out
+  int id = -1;
+  if (tid < npairs) id = __ldcg(topk_ids + tid);
+  const uint32_t key0 = tid < npairs ? pair_key(id, tid, E) : 0xFFFFFFFFu;
+  if (tid < npairs && key0 == 0xFFFFFFFFu && lead) atomicExch(status, 6);
+  const PairPlace q = group_pairs<0>(key0, cap, s_in, s_key, s_warp);
+  if (q.valid && !q.kept && lead) atomicExch(status, 6);
+  const int prob = q.prob, slot = q.slot, pair = q.pair;
+  const bool kept = q.kept, head = q.head, last = q.last;
   if (tid == kGroupThreads - 1) s_P = prob + 1;  // heads among the valid pairs
   if (lead && kept) {
     gtab[kGtPair + prob * 16 + slot] = pair;
     if (head) {
-      gtab[kGtExpert + prob] = e;
-      gtab[kGtRowsum + prob] = kept_incl - 1;
+      gtab[kGtExpert + prob] = q.e;
+      gtab[kGtRowsum + prob] = q.rsum;
     }
     if (last) gtab[kGtCount + prob] = slot + 1;
   }
   const int b = blockIdx.x;
   if (kept && prob == b) {
     s_pair[slot] = pair;
-    if (head) s_rsum = kept_incl - 1;
+    if (head) s_rsum = q.rsum;
     if (last) s_cnt = slot + 1;
   }
   __syncthreads();
@@ -1029,8 +1124,13 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
   }
 }
 
-cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids, int npairs,
+cudaError_t launch_decode_grouped(const DecodeLaunch& L0, const int32_t* topk_ids, int npairs,
                                   int topk, int E, cudaStream_t s, int* launches) {
+  if (npairs > kGroupThreads) return cudaErrorInvalidValue;
+  DecodeLaunch L = L0;
+  L.topk_ids = topk_ids;
+  L.npairs = npairs;
+  L.E = E;
   cudaError_t e = cudaSuccess;
   {
     const int pmax = npairs < E ? npairs : E;

@@ -46,6 +46,8 @@ struct DecodeLaunch {
   // grouped (mixture-of-experts) mode: packed = expert 0's packed weight
   const int* gtab = nullptr;  // group table in the workspace
   int64_t expert_bytes = 0;   // bytes per expert's packed weight
+  const int32_t* topk_ids = nullptr;  // the routing [npairs] (the kernel groups it again)
+  int npairs = 0, E = 0;
   // W4A4: the pre-pass quantises the activations to the weight's block format (alpha:
   // NVFP4 activation global)
   int w4a4 = 0;
