@@ -6,8 +6,11 @@
 Prints ONE JSON line (rank 0).  A step is one pass of the hot path over one batch of each
 size M of the workload: for every M, every projection of the workload is called once (the
 decode MLP of the default workload: fused gate_up then down), each call on its own copy of
-the weights so that the bytes streamed per step exceed the L2 cache.  `value` is algorithmic
-HBM bytes per second (packed codes + scales + global + bf16 activations), whole job.
+the weights so that the bytes streamed per step exceed the L2 cache; a step that alone fits
+the L2 rotates over graphs on other copies.  The step is one CUDA graph; `value` is
+algorithmic HBM bytes per second (packed codes + scales + global + bf16 activations), whole
+job.  `e2e` times the same step with every call's activations copied in from pinned host
+memory and every result copied back, inside the timed region.
 
 N > 1 runs independent replicas (one process per GPU, launched by torchrun): the layer does
 not exchange data between GPUs, so there is no collective on the data path.
