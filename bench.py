@@ -815,10 +815,11 @@ def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, 
 
 
 # ---------------------------------------------------------------- CPU (oracle) leg
-def run_oracle_sample(w: Workload, target_s: float = 12.0):
+def run_oracle_sample(w: Workload, target_s: float = 12.0, nthreads: int | None = None):
     """The oracle, as it stands, on a bounded sample of the workload: every (projection, M)
     call of a step, restricted to a fixed fraction of the output columns.  Returns
-    (GB/s of algorithmic bytes, seconds, threads, description)."""
+    (GB/s of algorithmic bytes, seconds, threads, description); ``nthreads`` (default: every
+    host core) is the oracle's thread count."""
     import oracle
     import synth
 
@@ -854,7 +855,7 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0):
             if a4 is not None:
                 oracle.gemm_w4a4(w.fmt, Ab, a4, c, s, G, n)
             else:
-                oracle.gemm(w.fmt, Ab, c, s, G, n)
+                oracle.gemm(w.fmt, Ab, c, s, G, n, nthreads=nthreads)
             nbytes += _work(w, n, p.K, M)
         return nbytes, time.perf_counter() - t
 
@@ -873,7 +874,7 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0):
     desc = (f"every (projection, M) call of one step of {w.name} on the first "
             f"{frac * 100:.3g}% of each projection's output columns"
             + (f", {reps} times" if reps > 1 else ""))
-    return _rate(w, nbytes, dt), dt, oracle.threads(), desc
+    return _rate(w, nbytes, dt), dt, nthreads or oracle.threads(), desc
 
 
 # ------------------------------------------------------------------------ main
@@ -1008,6 +1009,11 @@ def main():
         gbps, dt, threads, desc = run_oracle_sample(w)
         line["cpu_baseline"] = {"value": round(gbps, 4), "unit": w.unit, "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+        if w.wid in (1, 2) and w.extra.get("w4a4") is None:
+            # the oracle on one core too, for the single GEMM and the MLP decode
+            g1, d1, _, desc1 = run_oracle_sample(w, target_s=4.0, nthreads=1)
+            line["cpu_baseline"]["single_thread"] = {"value": round(g1, 4), "cores": 1,
+                                                     "sample": desc1, "seconds": round(d1, 2)}
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

@@ -166,10 +166,12 @@ def dequant(fmt: int, codes, scales, G: float, N: int, K: int) -> np.ndarray:
     return out
 
 
-def gemm(fmt: int, A, codes, scales, G: float, N: int, cols=None, want_f64: bool = False):
+def gemm(fmt: int, A, codes, scales, G: float, N: int, cols=None, want_f64: bool = False,
+         nthreads: int | None = None):
     """y = A . W^T.  A: bf16 bits [M, K].  Returns (y fp32 [M, n], y_bf16 bits [M, n]) and,
     if ``want_f64``, the fp64-accumulated sums as a third element.  ``cols`` restricts the
-    output to those columns n (in the given order)."""
+    output to those columns n (in the given order); ``nthreads`` (default: every core) splits
+    the output columns between threads, which changes no result bit."""
     A, ap = _c(A, np.uint16)
     codes, cp = _c(codes, np.uint8)
     scales, sp = _c(scales, np.uint8)
@@ -183,7 +185,8 @@ def gemm(fmt: int, A, codes, scales, G: float, N: int, cols=None, want_f64: bool
     ybf = np.empty((M, ncols), np.uint16)
     y64 = np.empty((M, ncols), np.float64) if want_f64 else None
     rc = _load().orc_gemm(fmt, ap, M, K, cp, sp, G, N, colp, ncols, y.ctypes.data,
-                          y64.ctypes.data if want_f64 else None, ybf.ctypes.data, threads())
+                          y64.ctypes.data if want_f64 else None, ybf.ctypes.data,
+                          nthreads or threads())
     if rc:
         raise ValueError("orc_gemm rejected the input")
     return (y, ybf, y64) if want_f64 else (y, ybf)
