@@ -718,24 +718,30 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
     # step's inputs, the calls, one copy of all its results (measured: 2612 against 2183 GB/s
     # on config 2 per-call; the prefill step 695 against 644 TFLOP/s with outputs alone
     # overlapped).
+    # A decode step without rotation keeps two sets of input slots: while a step computes on
+    # one, its input copy for the next step fills the other, the way a serving loop stages the
+    # next batch (still one host-to-device copy per timed step).
     piped = w.kind == "prefill"
-    side_in = torch.cuda.Stream(device=dev) if piped else None
+    double = not piped and len(steps_calls) == 1
+    side_in = torch.cuda.Stream(device=dev) if (piped or double) else None
     side_out = torch.cuda.Stream(device=dev) if piped else None
 
     def make_step(calls):
         # MLP chain: the host input feeds gate_up, down's output goes back; act stays on device
         host_in = [not (silu and not w.projs[pi].fused) for _, _, pi, _ in calls]
         host_out = [not (silu and w.projs[pi].fused) for _, _, pi, _ in calls]
-        IN = _Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
-                     for i, (_, _, pi, M) in enumerate(calls)], dev)
+        INS = [_Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
+                       for i, (_, _, pi, M) in enumerate(calls)], dev) for _ in range(2 if double else 1)]
         OUT = _Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
                       for i, (_, _, pi, M) in enumerate(calls)], dev)
-        for i, (_, _, pi, M) in enumerate(calls):
-            if host_in[i]:
-                IN.view(i, (M, w.projs[pi].K), torch.bfloat16, host=True).copy_(
-                    torch.randn((M, w.projs[pi].K)).to(torch.bfloat16))
+        for IN in INS:
+            for i, (_, _, pi, M) in enumerate(calls):
+                if host_in[i]:
+                    IN.view(i, (M, w.projs[pi].K), torch.bfloat16, host=True).copy_(
+                        torch.randn((M, w.projs[pi].K)).to(torch.bfloat16))
 
-        def issue():
+        def issue(par=0):
+            IN = INS[par]
             ready = []
             if piped:
                 side_in.wait_stream(stream)
@@ -748,6 +754,10 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
                         ev = torch.cuda.Event()
                         ev.record(side_in)
                         ready.append(ev)
+            elif double:  # this step's inputs came in during the previous step
+                side_in.wait_stream(stream)
+                with torch.cuda.stream(side_in):
+                    INS[1 - par].to_dev()
             else:
                 IN.to_dev()
             for i, (c, layer, pi, M) in enumerate(calls):
@@ -779,11 +789,14 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
                 stream.wait_stream(side_out)
             else:
                 OUT.to_host()
-        return issue, IN.nbytes, OUT.nbytes, (sum(host_in) + sum(host_out)) if piped else 2
+                if double:
+                    stream.wait_stream(side_in)
+        issues = [issue] if not double else [lambda: issue(0), lambda: issue(1)]
+        return issues, INS[0].nbytes, OUT.nbytes, (sum(host_in) + sum(host_out)) if piped else 2
 
     steps = [make_step(sc) for sc in steps_calls]
-    return _time_e2e(args, w, [st[0] for st in steps], stream, dev, step_bytes, world, dist,
-                     steps[0][1], steps[0][2], copies=steps[0][3])
+    return _time_e2e(args, w, [f for st in steps for f in st[0]], stream, dev, step_bytes, world,
+                     dist, steps[0][1], steps[0][2], copies=steps[0][3])
 
 
 def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
