@@ -306,6 +306,19 @@ def _calls(w: Workload, sets):
     return calls
 
 
+def _rotated_steps(w: Workload, calls, copies: int, step_bytes: float):
+    """A step smaller than twice the L2 would find its weights still in L2 on the next
+    replay: such a workload rotates over several graphs, step j on the copies shifted by j
+    steps' worth, so that every timed step reads weights no recent step has read.  Returns
+    the calls of each rotated step (one step when no rotation is needed)."""
+    cps = len({c for c, _, _, _ in calls})
+    rot = 1
+    if w.kind not in ("moe", "prefill") and step_bytes < 2 * L2_BYTES:
+        rot = max(1, min(copies // cps, int(np.ceil(2 * L2_BYTES / step_bytes))))
+    return [[((c + j * cps) % copies, layer, pi, M) for c, layer, pi, M in calls]
+            for j in range(rot)]
+
+
 def _dequant_act(A, fmt: int, alpha: float):
     """The W4A4 arm's quantised activations as values, from the library's activation
     quantiser (codes and scales) decoded here with PyTorch."""
@@ -419,15 +432,8 @@ def run_gpu(args, rank: int, world: int):
     else:
         step_bytes = sum(_work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
     n_calls = len(calls)
-    # A step smaller than twice the L2 would find its weights still in L2 on the next replay:
-    # such a workload rotates over `rot` graphs, step j on the copies shifted by j steps'
-    # worth, so that every timed step reads weights no recent step has read.
-    cps = len({c for c, _, _, _ in calls})
-    rot = 1
-    if not moe and w.kind != "prefill" and step_bytes < 2 * L2_BYTES:
-        rot = max(1, min(copies // cps, int(np.ceil(2 * L2_BYTES / step_bytes))))
-    steps_calls = [[((c + j * cps) % copies, layer, pi, M) for c, layer, pi, M in calls]
-                   for j in range(rot)]
+    steps_calls = _rotated_steps(w, calls, copies, step_bytes)
+    rot = len(steps_calls)
 
     greedy = w.kind == "greedy"
     silu = w.kind == "mlp_silu"

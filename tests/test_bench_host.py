@@ -1,0 +1,37 @@
+"""CPU: the benchmark's host-side step construction.  Every timed step must read weights no
+recent step has read (the L2 rule): a step that alone exceeds twice the L2 uses one weight
+copy per call of a size M, and a step that fits the L2 rotates over enough graphs, each on
+other copies, that the bytes between two reads of one copy exceed twice the L2."""
+import bench
+
+
+def _steps(name):
+    w = bench.WORKLOADS[name]
+    copies = bench._copies_needed(w)
+    sets = [[[None] * len(w.projs)] * w.layers] * copies
+    calls = bench._calls(w, sets)
+    step_bytes = sum(bench._work(w, w.projs[pi].N, w.projs[pi].K, M) for _, _, pi, M in calls)
+    return w, copies, calls, step_bytes, bench._rotated_steps(w, calls, copies, step_bytes)
+
+
+def test_large_steps_are_not_rotated():
+    for name in ("mxfp4_mlp_12288x4096", "nvfp4_lm_head_248320x2560", "nvfp4_layer_sweep_5120"):
+        w, copies, calls, step_bytes, steps = _steps(name)
+        assert len(steps) == 1 and steps[0] == calls
+        assert step_bytes > 2 * bench.L2_BYTES, name
+        per_copy = sum(bench._algo_bytes(w.fmt, p.N, p.K, 0) for p in w.projs) * w.layers
+        if per_copy < 2 * bench.L2_BYTES:
+            # a copy smaller than twice the L2: every M of the step streams its own copy
+            by_m = {}
+            for c, _, _, M in calls:
+                by_m.setdefault(M, set()).add(c)
+            assert len({frozenset(v) for v in by_m.values()}) == len(w.Ms), name
+
+
+def test_small_step_rotates_over_cold_copies():
+    w, copies, calls, step_bytes, steps = _steps("nvfp4_gemm_2048x1024")
+    assert step_bytes < bench.L2_BYTES
+    assert len(steps) * step_bytes >= 2 * bench.L2_BYTES
+    used = [c for st in steps for c, _, _, _ in st]
+    assert len(set(used)) == len(used)  # no copy read twice within one rotation
+    assert all(0 <= c < copies for c in used)
