@@ -494,8 +494,8 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   // token tile of the decode kernel: 8 rows when M <= 8 (an expert then has at most M pairs
   // unless a token names it twice; such extra pairs are left out), else 16
   const int mrows = decode_mt((int)M);
-  int stages = 6;
-  while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages) > 226 * 1024) --stages;
+  int stages = 6;  // the grouped kernel also holds ~3 KB of static shared memory (the grouping)
+  while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages) > 223 * 1024) --stages;
   const int64_t pmax = npairs < W->E ? npairs : W->E;
   const int64_t items = pmax * W->RT * W->KT;  // an upper bound: the pre-pass finds P
   int64_t grid = sm_count();
