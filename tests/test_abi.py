@@ -122,6 +122,39 @@ def test_w4a4_rejects_bad_arguments_without_a_gpu(L):
     assert L.vt_fp4_w4a4_gemm(fake, 4, 64, None, 1.0, fake, 64, fake, 1 << 20, None) == 1
 
 
+def test_grouped_and_epilogue_entry_points_reject_without_a_gpu(L):
+    """The mixture-of-experts, greedy and SiLU-and-multiply entry points check their counts,
+    pointers and alignment before any CUDA call."""
+    fake = ctypes.c_void_p(0x1000)
+    nb = ctypes.c_size_t(0)
+    gb = L.vt_fp4_prepack_grouped_bytes
+    for E in (0, -1, 65537):
+        assert gb(0, E, 64, 64, ctypes.byref(nb)) == _lib.VT_ERR_INVALID_ARG
+    assert gb(0, 4, 64, 24, ctypes.byref(nb)) == _lib.VT_ERR_INVALID_ARG   # K % 16
+    assert gb(0, 4, 64, 64, None) == _lib.VT_ERR_INVALID_ARG
+    assert gb(1, 3, 130, 96, ctypes.byref(nb)) == 0
+    assert nb.value == 3 * vt.prepack_bytes(vt.MXFP4, 130, 96)  # E whole experts back to back
+    h = ctypes.c_void_p(0x1234)
+    pg = L.vt_fp4_prepack_grouped
+    assert pg(fake, fake, fake, 0, 2, 64, 64, fake, 1 << 20, None, None) == 1  # no out pointer
+    assert pg(None, fake, fake, 0, 2, 64, 64, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    assert h.value in (None, 0)  # cleared before any check fails
+    assert pg(fake, fake, None, 0, 2, 64, 64, fake, 1 << 20, None, ctypes.byref(h)) == 1
+    assert pg(fake, fake, fake, 0, 2, 64, 64, fake, 100, None, ctypes.byref(h)) == 1
+    assert L.vt_fp4_moe_workspace_bytes(None, 4, 2, ctypes.byref(nb)) == 1
+    assert L.vt_fp4_w4a16_gemm_moe(fake, 4, 64, None, fake, 2, fake, 64, fake, 1 << 20,
+                                   None) == 1
+    g = L.vt_fp4_w4a16_gemm_greedy
+    assert g(fake, 4, 64, None, None, None, fake, 1 << 20, None) == 1       # no token buffer
+    assert g(fake, 17, 64, None, fake, None, fake, 1 << 20, None) == _lib.VT_ERR_UNSUPPORTED
+    assert g(fake, 4, 64, None, ctypes.c_void_p(0x1002), None, fake, 1 << 20,
+             None) == _lib.VT_ERR_MISALIGNED
+    assert g(fake, 4, 64, None, fake, ctypes.c_void_p(0x1001), fake, 1 << 20,
+             None) == _lib.VT_ERR_MISALIGNED
+    assert L.vt_fp4_w4a16_gemm_silu_mul(fake, 4, 64, None, fake, 64, fake, 1 << 20, None) == 1
+    assert L.vt_fp4_last_error()
+
+
 def test_algorithmic_bytes_reproduce_the_pages_figures():
     """tests/golden/footprint_pages.txt: the packed head is 0.6660 GiB, its bf16 expansion
     2.3683 GiB, the avoidable traffic 1.702 GiB."""
