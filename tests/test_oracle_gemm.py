@@ -152,3 +152,25 @@ def test_empty_batch():
     scales = np.full((4, 2), 0x38, np.uint8)
     y, ybf = oracle.gemm(oracle.NVFP4, np.zeros((0, 32), np.uint16), codes, scales, 1.0, 4)
     assert y.shape == (0, 4)
+
+
+@pytest.mark.parametrize("fmt", [oracle.NVFP4, oracle.MXFP4])
+def test_thread_count_changes_no_bit(fmt):
+    """The oracle splits output columns (and weight rows) between threads; every output is
+    still one sequential sum, so the thread count must not show in any bit."""
+    M, N, K = 3, 37, 256
+    Wb = synth.normal_bf16(0, 95 + fmt, 0.02, N, K)
+    A = synth.normal_bf16(0, 96 + fmt, 1.0, M, K)
+    q1 = oracle.quantize_nvfp4(Wb, nthreads=1) if fmt == oracle.NVFP4 else \
+        oracle.quantize_mxfp4(Wb, nthreads=1)
+    q5 = oracle.quantize_nvfp4(Wb, nthreads=5) if fmt == oracle.NVFP4 else \
+        oracle.quantize_mxfp4(Wb, nthreads=5)
+    for a, b in zip(q1, q5):
+        assert np.array_equal(a, b)
+    codes, scales = q1[:2]
+    G = q1[2] if fmt == oracle.NVFP4 else 1.0
+    ref = oracle.gemm(fmt, A, codes, scales, G, N, want_f64=True, nthreads=1)
+    for t in (2, 5, 64):
+        got = oracle.gemm(fmt, A, codes, scales, G, N, want_f64=True, nthreads=t)
+        for a, b in zip(ref, got):
+            assert np.array_equal(a, b), t
