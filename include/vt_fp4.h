@@ -53,13 +53,16 @@ typedef enum {
 
 typedef struct vt_fp4_weight_s* vt_fp4_handle;
 
-/* What the last vt_fp4_w4a16_gemm on a handle launched (host-side record). */
+/* What the last GEMM call on a handle launched (host-side record). */
 typedef struct {
-  int path;           /* 0 none yet, 1 decode (M <= 16), 2 prefill tile path */
+  int path;           /* 0 none yet, 1 decode (M <= 16), 2 prefill tile path,
+                         3 grouped mixture-of-experts decode */
   int grid;           /* CTAs of the main kernel */
   int warps_per_cta;  /* warps per CTA of the main kernel */
-  int m_tile;         /* decode: tokens per MMA column block (8 or 16); prefill: 128 */
-  int64_t items;      /* decode: (row tile, k tile) work items; prefill: output tiles */
+  int m_tile;         /* decode and grouped: tokens per MMA column block (8 or 16);
+                         prefill: 128 */
+  int64_t items;      /* decode: (row tile, k tile) work items; grouped: an upper bound on
+                         them (the routing is read on the device); prefill: output tiles */
   int64_t launches;   /* kernels enqueued by that call */
   int64_t calls;      /* GEMM calls made on this handle so far */
 } vt_fp4_launch_info;
