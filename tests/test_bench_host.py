@@ -35,3 +35,26 @@ def test_small_step_rotates_over_cold_copies():
     used = [c for st in steps for c, _, _, _ in st]
     assert len(set(used)) == len(used)  # no copy read twice within one rotation
     assert all(0 <= c < copies for c in used)
+
+
+def test_traffic_is_dropped_once_the_kernel_source_changes(tmp_path, monkeypatch):
+    """The DRAM traffic of a committed capture is reported only while the captured kernel's
+    source is unchanged; decode traffic is scaled to the step's average launch."""
+    import hashlib
+    import json
+    import os
+    w = bench.WORKLOADS["mxfp4_mlp_12288x4096"]
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    os.makedirs(tmp_path / "profiles")
+    rec = {w.name: {"kernel": "k", "source": "k.cu",
+                    "source_sha256_16": hashlib.sha256(b"kernel v1\n").hexdigest()[:16],
+                    "captured_launch": "one launch", "dram_bytes": 110,
+                    "algorithmic_bytes": 100, "summary": "profiles/k.md"}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    t = bench._profiled_traffic(w, step_work=4000.0, calls=4)
+    assert t["bytes_per_launch"] == 1100 and t["dram_over_algorithmic"] == 1.1
+    src.write_text("kernel v2\n")
+    assert bench._profiled_traffic(w, step_work=4000.0, calls=4) is None
+    assert bench._profiled_traffic(bench.WORKLOADS["nvfp4_gemm_2048x1024"], 1.0, 1) is None
