@@ -58,3 +58,26 @@ def test_traffic_is_dropped_once_the_kernel_source_changes(tmp_path, monkeypatch
     src.write_text("kernel v2\n")
     assert bench._profiled_traffic(w, step_work=4000.0, calls=4) is None
     assert bench._profiled_traffic(bench.WORKLOADS["nvfp4_gemm_2048x1024"], 1.0, 1) is None
+
+
+def test_clock_sampler_reads_median_clock_and_throttle_reasons(tmp_path, monkeypatch):
+    """The clocks record of the JSON line, from a stand-in nvidia-smi that prints three
+    samples: the median SM clock, the highest maximum clock and every reason seen Active."""
+    import os
+    import stat
+    import time
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '0, 1900, 2070, 900.1, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '0, 2010, 2070, 1001.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '0, [N/A], 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '0, 1950, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "exec sleep 30\n")
+    fake.chmod(fake.stat().st_mode | stat.S_IEXEC)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    s.start()
+    time.sleep(1.0)
+    rec = s.stop()
+    assert rec["sm_mhz"] == 1950 and rec["sm_max_mhz"] == 2070
+    assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] == 4
