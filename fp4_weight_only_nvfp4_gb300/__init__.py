@@ -18,8 +18,9 @@ NVFP4, MXFP4 = 0, 1
 GROUP = {NVFP4: 16, MXFP4: 32}
 
 __all__ = ["NVFP4", "MXFP4", "GROUP", "PackedWeight", "w4a16_gemm", "w4a16_gemm_noalloc",
-           "quantize", "prepack_bytes",
-           "workspace_status", "VtError", "algorithmic_bytes"]
+           "w4a16_gemm_greedy", "w4a16_gemm_silu_mul", "w4a16_gemm_moe", "w4a4_gemm",
+           "quantize_act", "quantize", "prepack_bytes", "workspace_status", "VtError",
+           "algorithmic_bytes"]
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -112,6 +113,9 @@ class PackedWeight:
         (vt_fp4_prepack_grouped)."""
         if codes.shape != (E, N, K // 2) or scales.shape != (E, N, K // GROUP[fmt]):
             raise ValueError("codes [E, N, K/2] and scales [E, N, K/g] expected")
+        _check_src(codes, scales, E * N, K, fmt)
+        if len(globals_) != E:
+            raise ValueError("one global per expert expected")
         out = ctypes.c_size_t(0)
         check(lib().vt_fp4_prepack_grouped_bytes(fmt, E, N, K, ctypes.byref(out)),
               "vt_fp4_prepack_grouped_bytes")
@@ -173,6 +177,32 @@ def _check_src(codes, scales, N, K, fmt):
         raise ValueError("codes/scales sizes do not match N and K")
 
 
+def _check_A(A: torch.Tensor, W: "PackedWeight"):
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+
+
+def _check_out(out: torch.Tensor, rows: int, cols: int, name: str = "out"):
+    """The kernels write rows x cols bf16 values at the given row stride: a smaller or
+    differently typed tensor would be written past its end."""
+    if out.dtype != torch.bfloat16 or out.dim() != 2 or tuple(out.shape) != (rows, cols) \
+            or out.stride(1) != 1:
+        raise ValueError(f"{name} must be a bf16 [{rows}, {cols}] tensor with unit inner stride")
+
+
+def _check_device(W: "PackedWeight", **tensors):
+    """Every tensor handed to the kernels must live on the weight's GPU: a host tensor or
+    another device's memory would reach the kernels as a wild address."""
+    dev = W.packed.device
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda or t.device != dev:
+            raise ValueError(f"{name} must be a CUDA tensor on {dev} (got {t.device})")
+        if name == "workspace" and (t.dtype != torch.uint8 or not t.is_contiguous()):
+            raise ValueError("workspace must be a contiguous uint8 tensor")
+
+
 def _opts(opts: dict | None):
     if not opts:
         return None
@@ -185,11 +215,12 @@ def w4a16_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
                workspace: torch.Tensor | None = None, stream=None,
                opts: dict | None = None) -> torch.Tensor:
     """out[M, N] (bf16) = A[M, K] (bf16) . W^T, fp32 accumulation, on the library's kernels."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    _check_A(A, W)
+    _check_device(W, A=A, out=out, workspace=workspace)
     M = A.shape[0]
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M, W.N)
     if workspace is None:
         workspace = W.new_workspace(M)
     o = _opts(opts)
@@ -205,11 +236,12 @@ def w4a4_gemm(A: torch.Tensor, W: PackedWeight, input_scale: float = 1.0,
               stream=None, opts: dict | None = None) -> torch.Tensor:
     """The W4A4 arm: out[M, N] (bf16) = Q(A) . W^T with the activations quantised to W's
     block format (NVFP4 with the activation global ``input_scale``; MXFP4: 1.0)."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    _check_A(A, W)
+    _check_device(W, A=A, out=out, workspace=workspace)
     M = A.shape[0]
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M, W.N)
     if workspace is None:
         workspace = W.new_workspace(M)
     o = _opts(opts)
@@ -239,14 +271,15 @@ def w4a16_gemm_moe(A: torch.Tensor, W: PackedWeight, topk_ids: torch.Tensor,
                    stream=None) -> torch.Tensor:
     """Mixture-of-experts decode GEMM: out[m * topk + j] = A[m] . W_e^T with
     e = topk_ids[m, j] (see vt_fp4_w4a16_gemm_moe in include/vt_fp4.h)."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    _check_A(A, W)
     if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2 or topk_ids.shape[0] != A.shape[0]:
         raise ValueError("topk_ids must be an int32 [M, topk] tensor")
+    _check_device(W, A=A, topk_ids=topk_ids, out=out, workspace=workspace)
     M, topk = topk_ids.shape
     topk_ids = topk_ids.contiguous()
     if out is None:
         out = torch.empty((M * topk, W.N), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M * topk, W.N)
     if workspace is None:
         workspace = W.moe_workspace(max(M, 1), topk)
     check(lib().vt_fp4_w4a16_gemm_moe(_ptr(A), M, A.stride(0), W.handle, _ptr(topk_ids), topk,
@@ -260,11 +293,12 @@ def w4a16_gemm_silu_mul(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | No
                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """out[M, I] (bf16) = silu(gate) * up of a paired gate_up weight, in one call (see
     vt_fp4_w4a16_gemm_silu_mul in include/vt_fp4.h)."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    _check_A(A, W)
+    _check_device(W, A=A, out=out, workspace=workspace)
     M = A.shape[0]
     if out is None:
         out = torch.empty((M, W.N // 2), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M, W.N // 2)
     if workspace is None:
         workspace = W.new_workspace(M)
     check(lib().vt_fp4_w4a16_gemm_silu_mul(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
@@ -279,8 +313,8 @@ def w4a16_gemm_greedy(A: torch.Tensor, W: PackedWeight, workspace: torch.Tensor 
     A . W^T, ties to the lowest index, and that value (fp32 [M]) -- without writing the
     outputs.  ``token``: an optional int32 [M] output tensor.  See vt_fp4_w4a16_gemm_greedy
     in include/vt_fp4.h."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    _check_A(A, W)
+    _check_device(W, A=A, token=token, workspace=workspace)
     M = A.shape[0]
     if token is None:
         token = torch.empty(M, dtype=torch.int32, device=A.device)
@@ -300,11 +334,12 @@ def w4a16_gemm_noalloc(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | Non
     """The decode GEMM (M <= 16) on the library's fixed scratch area instead of a caller
     workspace, for callers that cannot allocate device memory (see vt_fp4_w4a16_gemm_noalloc
     in include/vt_fp4.h).  Calls must not overlap on the GPU."""
-    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
-        raise ValueError("A must be a bf16 [M, K] tensor with unit inner stride")
+    _check_A(A, W)
+    _check_device(W, A=A, out=out)
     M = A.shape[0]
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M, W.N)
     check(lib().vt_fp4_w4a16_gemm_noalloc(_ptr(A), M, A.stride(0), W.handle, _ptr(out),
                                           out.stride(0), _stream(stream)),
           "vt_fp4_w4a16_gemm_noalloc")
@@ -312,6 +347,10 @@ def w4a16_gemm_noalloc(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | Non
 
 
 def workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """The workspace's status word (0, or the code a kernel recorded there); synchronises
+    the stream."""
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
     st = ctypes.c_int(0)
     check(lib().vt_fp4_workspace_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
           "vt_fp4_workspace_status")
