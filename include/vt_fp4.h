@@ -250,8 +250,9 @@ vt_status vt_fp4_w4a16_gemm_greedy(const void* A, int64_t M, int64_t lda, vt_fp4
 vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
                                     void* C, int64_t ldc, vt_stream_t s);
 
-/* Reads the workspace status word (synchronises `s`): *status = VT_OK, or VT_ERR_TIMEOUT
- * if a bounded device-side wait gave up during an earlier call; the word is then cleared.
+/* Reads the workspace status word (synchronises `s`): *status = VT_OK, VT_ERR_TIMEOUT if
+ * a bounded device-side wait gave up during an earlier call, or 6 if a grouped call
+ * skipped pairs (vt_fp4_w4a16_gemm_moe); the word is then cleared.
  * After VT_ERR_TIMEOUT zero the whole workspace again before reusing it: a call that gave up
  * may leave split-K arrival counts behind. */
 vt_status vt_fp4_workspace_status(void* workspace, vt_stream_t s, int* status);
