@@ -10,6 +10,7 @@
 // A magnitude that rounds to zero is code 0 (+0).  The kernels are built without fast-math
 // (IEEE division, denormals kept), which these decisions rely on.
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -135,6 +136,21 @@ __device__ __forceinline__ uint4 aq_mx_granule(const uint32_t w[4], int e, int p
     o[q] = bad ? 0x7E007E00u : pack_half2(aq_e2m1_val(c0) * up, aq_e2m1_val(c1) * up);
   }
   if (codes) *codes = bad ? 0u : cw;
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One granule of an MXFP4 group with exponent e -> c * 2^e as bf16: exact (at most two
+// significant bits, |c 2^e| >= 2^-128 for e >= -127; bf16 has fp32's exponent range, so a
+// value beyond it is inf in both).  For the tiles of a wide MXFP4 weight (bf16 x bf16).
+__device__ __forceinline__ uint4 aq_mx_granule_bf16(const uint32_t w[4], int e, bool bad) {
+  const float inv = ldexpf(1.0f, -e), up = ldexpf(1.0f, e);
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t c0 = aq_mx_code(bf16_lo(w[q]), inv), c1 = aq_mx_code(bf16_hi(w[q]), inv);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(aq_e2m1_val(c0) * up, aq_e2m1_val(c1) * up);
+    o[q] = bad ? 0x7FC07FC0u : *reinterpret_cast<const uint32_t*>(&h);
+  }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 

@@ -23,7 +23,9 @@ namespace vt {
 //   scales NVFP4 [4 row-block pairs jp][32 lanes][2 j][2 B] (512 B): E4M3 bytes of rows
 //          16j+g and 16j+g+8 (j = 2jp + j&1) for group 4kt+t (the 16 k lane t covers).
 //   scales MXFP4 [4 jp][8 g][2 h][2 j][2 B] (256 B): rows 16j+g, 16j+g+8, group 2kt+h;
-//          the bytes are re-encoded as the high byte of an f16 power of two (see prepack).
+//          the bytes are re-encoded as the high byte of an f16 power of two (see prepack),
+//          or kept as raw E8M0 bytes when the weight's scales span more exponents than
+//          that encoding holds (header field `wide`).
 //   so the four scale bytes lane (g, t) needs for a row-block pair form one 32-bit word.
 constexpr int kHeaderBytes = 256;
 constexpr int kTileRows = 128;
@@ -56,7 +58,11 @@ struct PackedHeader {
   float factor[2];     // epilogue multiplier per segment (NVFP4 global, MXFP4 2^(emax-140))
   int32_t emax[2];     // MXFP4: largest finite E8M0 byte per segment
   uint32_t layout;     // kLayoutRows or kLayoutPaired
-  uint32_t pad[51];
+  int32_t emin[2];     // MXFP4: smallest finite E8M0 byte per segment
+  uint32_t wide;       // MXFP4: 1 when a segment's finite scale bytes span more than the
+                       // 30 exponents the f16 re-encoding holds; the tiles then keep the raw
+                       // E8M0 bytes and the kernels apply each group scale exactly (factor 1)
+  uint32_t pad[48];
 };
 static_assert(sizeof(PackedHeader) == kHeaderBytes, "header size");
 constexpr uint32_t kMagic = 0x34465456u;  // "VTF4"
@@ -198,6 +204,13 @@ __device__ __forceinline__ uint32_t mxenc2_to_f16x2(uint32_t two_bytes) {
   return __byte_perm(two_bytes, 0u, 0x1404);
 }
 
+// E8M0 byte -> its value 2^(e - 127) as an fp32 (exact: 2^-127 is an fp32 subnormal);
+// 0xFF -> NaN.  The OCP Microscaling definition of the MXFP4 scale.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
+  return e == 0xFFu ? __uint_as_float(0x7FC00000u)
+                    : (e == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23));
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
@@ -222,6 +235,12 @@ __device__ __forceinline__ int4 ld_shared_v4(uint32_t addr) {
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
 

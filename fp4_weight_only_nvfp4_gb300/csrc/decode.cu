@@ -20,6 +20,8 @@
 // (see k_decode), which adds the others' partials in CTA order.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "actq.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -688,6 +690,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   }
   const int jp = warp & 3, kq = warp >> 2;  // row blocks 2jp, 2jp+1; k tiles kq, kq+4
   float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
+  // wide MXFP4 weight: raw E8M0 bytes in the tiles, each group's exact scale applied in fp32
+  bool wide = FMT == FMT_MX && p.hdr->wide != 0;
   // grouped mode: the current problem's token count, output rows and expert factor
   int Mc = M, gprob = -1;
   const int* grow = nullptr;
@@ -700,6 +704,12 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[b][u][r] = 0.0f;
 
+  // The stage loop, compiled twice for plain MXFP4 weights at the 8-token tile: once for the
+  // narrow scale encoding and once for wide weights (WIDE), so that each copy gets its own
+  // register allocation.  The grouped kernel, whose experts may differ, and the 16-token tile
+  // (where two copies in one kernel cost more registers than one) decide inside one copy.
+  auto consume = [&](auto wide_tag) -> bool {
+  constexpr bool WIDE = decltype(wide_tag)::value;
   bool ok = true;
   int64_t pos = i0;
   int kt = kt_first, slot = 0;
@@ -717,90 +727,146 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         const PackedHeader* he = reinterpret_cast<const PackedHeader*>(
             p.gbase + (int64_t)s_rexp[pr] * p.expert_bytes);
         f0 = f1 = he->factor[0];
+        wide = FMT == FMT_MX && he->wide != 0;
       }
     }
     if (ok) ok = mbar_wait_bounded(full_u + 8 * slot, par, p.wait_ns);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       const uint32_t sbase = ring_u + slot * STAGE;
+      // one k tile of this warp's work; W: the exact path of a wide MXFP4 weight
+      auto ktile = [&](int kh, auto w_tag) {
+        constexpr bool W = decltype(w_tag)::value;
+        const uint32_t tb = sbase + kh * TB;
+        const uint32_t ab = RA ? res_u + (uint32_t)((kt + kh) * M * 128)
+                               : sbase + WBYTES + kh * Mc * 128;
+        // activation fragments (B operand) of token block u: token rows g (+8), physical
+        // k 16t .. 16t+15
+        auto load_b = [&](int u, uint32_t (&bf)[4][2]) {
+          const int m = g + 8 * u;
+          if (m < Mc) {
+            const uint32_t rowa = ab + m * 128;
+            const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (m & 7)) << 4));
+            const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (m & 7)) << 4));
+            bf[0][0] = v0.x; bf[0][1] = v0.y;
+            bf[1][0] = v0.z; bf[1][1] = v0.w;
+            bf[2][0] = v1.x; bf[2][1] = v1.y;
+            bf[3][0] = v1.z; bf[3][1] = v1.w;
+          } else {
 #pragma unroll
-      for (int kh = kq; kh < KS; kh += 4) {
-        if (kh < n) {
-          const uint32_t tb = sbase + kh * TB;
-          const uint32_t ab = RA ? res_u + (uint32_t)((kt + kh) * M * 128)
-                                 : sbase + WBYTES + kh * Mc * 128;
-          // activation fragments (B operand): token rows g (+8), physical k 16t .. 16t+15
-          uint32_t bfr[NJ][4][2];
-#pragma unroll
-          for (int u = 0; u < NJ; ++u) {
-            const int m = g + 8 * u;
-            if (m < Mc) {
-              const uint32_t rowa = ab + m * 128;
-              const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (m & 7)) << 4));
-              const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (m & 7)) << 4));
-              bfr[u][0][0] = v0.x; bfr[u][0][1] = v0.y;
-              bfr[u][1][0] = v0.z; bfr[u][1][1] = v0.w;
-              bfr[u][2][0] = v1.x; bfr[u][2][1] = v1.y;
-              bfr[u][3][0] = v1.z; bfr[u][3][1] = v1.w;
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) bfr[u][q][0] = bfr[u][q][1] = 0u;
-            }
+            for (int q = 0; q < 4; ++q) bf[q][0] = bf[q][1] = 0u;
           }
-          // activation scales of this k tile for the tokens of this lane's accumulators
-          float as[NJ][2];
-#pragma unroll
-          for (int u = 0; u < NJ; ++u) {
-            const uint32_t sa =
-                RA ? rscale_u + (uint32_t)(((kt + kh) * kResScaleStride + 2 * t + 8 * u) * 4)
-                   : sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
-                         : "=f"(as[u][0]), "=f"(as[u][1])
-                         : "r"(sa));
-          }
-          uint32_t sc4;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc4) : "r"(tb + soff));
+        };
+        // activation scales of this k tile for the tokens of this lane's accumulators
+        auto load_as = [&](int u, float (&a)[2]) {
+          const uint32_t sa =
+              RA ? rscale_u + (uint32_t)(((kt + kh) * kResScaleStride + 2 * t + 8 * u) * 4)
+                 : sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[0]), "=f"(a[1]) : "r"(sa));
+        };
+        if constexpr (W) {
+          // Exact MXFP4 over the whole E8M0 range: lane t's k lie in group t >> 1 of the
+          // k tile, so one MMA takes the lanes of group 0 (the others' weights zeroed) and
+          // a second those of group 1; each group's fp32 sums are multiplied by the token's
+          // activation scale and then by the group's exact scale 2^(e - 127).  The weights
+          // enter the MMA as the E2M1 values themselves (exact in f16).  One row block and
+          // one token block at a time, to keep few registers live.
+          const uint2 sc8 = ld_shared_v2(tb + kCodeBytes + jp * 64 + g * 8);
+          const uint32_t gm = (t < 2) ? 0xFFFFFFFFu : 0u;
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             const int j = 2 * jp + b;
             const int4 wv = ld_shared_v4(tb + j * 512 + lane * 16);
-            const uint32_t two = b ? (sc4 >> 16) : (sc4 & 0xFFFFu);
-            const uint32_t sc = (FMT == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
-            const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc);
-            const __half2 sg = __low2half2(sc2), sg8 = __high2half2(sc2);
+            // scale bytes: group h, row g (low byte) and row g + 8 (high byte) of block j
+            const uint32_t s0 = sc8.x >> (16 * b), s1 = sc8.y >> (16 * b);
+            const float fg0 = e8m0_to_f32(s0 & 0xFFu), fg80 = e8m0_to_f32((s0 >> 8) & 0xFFu);
+            const float fg1 = e8m0_to_f32(s1 & 0xFFu), fg81 = e8m0_to_f32((s1 >> 8) & 0xFFu);
             const uint32_t words[4] = {(uint32_t)wv.x, (uint32_t)wv.y, (uint32_t)wv.z,
                                        (uint32_t)wv.w};
-            float tmp[NJ][4];
-#pragma unroll
-            for (int u = 0; u < NJ; ++u)
-#pragma unroll
-              for (int r = 0; r < 4; ++r) tmp[u][r] = 0.0f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t r0, r1, r2, r3;
-              e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
-              __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&r0), sg);
-              __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&r1), sg8);
-              __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&r2), sg);
-              __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&r3), sg8);
-              const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0);
-              const uint32_t a1 = *reinterpret_cast<uint32_t*>(&h1);
-              const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2);
-              const uint32_t a3 = *reinterpret_cast<uint32_t*>(&h3);
-#pragma unroll
-              for (int u = 0; u < NJ; ++u)
-                mma_f16_16816(tmp[u], a0, a1, a2, a3, bfr[u][q][0], bfr[u][q][1]);
-            }
-            // this k tile's sums back to the activations' true scale
 #pragma unroll
             for (int u = 0; u < NJ; ++u) {
-              acc[b][u][0] = fmaf(tmp[u][0], as[u][0], acc[b][u][0]);
-              acc[b][u][1] = fmaf(tmp[u][1], as[u][1], acc[b][u][1]);
-              acc[b][u][2] = fmaf(tmp[u][2], as[u][0], acc[b][u][2]);
-              acc[b][u][3] = fmaf(tmp[u][3], as[u][1], acc[b][u][3]);
+              uint32_t bf[4][2];
+              float a2[2];
+              load_b(u, bf);
+              load_as(u, a2);
+              float t0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, t1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t r0, r1, r2, r3;
+                e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
+                mma_f16_16816(t0, r0 & gm, r1 & gm, r2 & gm, r3 & gm, bf[q][0], bf[q][1]);
+                mma_f16_16816(t1, r0 & ~gm, r1 & ~gm, r2 & ~gm, r3 & ~gm, bf[q][0], bf[q][1]);
+              }
+              acc[b][u][0] = fmaf(t0[0] * a2[0], fg0, acc[b][u][0]);
+              acc[b][u][0] = fmaf(t1[0] * a2[0], fg1, acc[b][u][0]);
+              acc[b][u][1] = fmaf(t0[1] * a2[1], fg0, acc[b][u][1]);
+              acc[b][u][1] = fmaf(t1[1] * a2[1], fg1, acc[b][u][1]);
+              acc[b][u][2] = fmaf(t0[2] * a2[0], fg80, acc[b][u][2]);
+              acc[b][u][2] = fmaf(t1[2] * a2[0], fg81, acc[b][u][2]);
+              acc[b][u][3] = fmaf(t0[3] * a2[1], fg80, acc[b][u][3]);
+              acc[b][u][3] = fmaf(t1[3] * a2[1], fg81, acc[b][u][3]);
             }
           }
+          return;
         }
+        uint32_t bfr[NJ][4][2];
+        float as[NJ][2];
+#pragma unroll
+        for (int u = 0; u < NJ; ++u) {
+          load_b(u, bfr[u]);
+          load_as(u, as[u]);
+        }
+        uint32_t sc4;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc4) : "r"(tb + soff));
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int j = 2 * jp + b;
+          const int4 wv = ld_shared_v4(tb + j * 512 + lane * 16);
+          const uint32_t two = b ? (sc4 >> 16) : (sc4 & 0xFFFFu);
+          const uint32_t sc = (FMT == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
+          const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc);
+          const __half2 sg = __low2half2(sc2), sg8 = __high2half2(sc2);
+          const uint32_t words[4] = {(uint32_t)wv.x, (uint32_t)wv.y, (uint32_t)wv.z,
+                                     (uint32_t)wv.w};
+          float tmp[NJ][4];
+#pragma unroll
+          for (int u = 0; u < NJ; ++u)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) tmp[u][r] = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t r0, r1, r2, r3;
+            e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
+            __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&r0), sg);
+            __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&r1), sg8);
+            __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&r2), sg);
+            __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&r3), sg8);
+            const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0);
+            const uint32_t a1 = *reinterpret_cast<uint32_t*>(&h1);
+            const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2);
+            const uint32_t a3 = *reinterpret_cast<uint32_t*>(&h3);
+#pragma unroll
+            for (int u = 0; u < NJ; ++u)
+              mma_f16_16816(tmp[u], a0, a1, a2, a3, bfr[u][q][0], bfr[u][q][1]);
+          }
+          // this k tile's sums back to the activations' true scale
+#pragma unroll
+          for (int u = 0; u < NJ; ++u) {
+            acc[b][u][0] = fmaf(tmp[u][0], as[u][0], acc[b][u][0]);
+            acc[b][u][1] = fmaf(tmp[u][1], as[u][1], acc[b][u][1]);
+            acc[b][u][2] = fmaf(tmp[u][2], as[u][0], acc[b][u][2]);
+            acc[b][u][3] = fmaf(tmp[u][3], as[u][1], acc[b][u][3]);
+          }
+        }
+      };
+      if (FMT == FMT_MX && (WIDE || ((GRP || MT == 16) && wide))) {
+#pragma unroll 1
+        for (int kh = kq; kh < KS; kh += 4)
+          if (kh < n) ktile(kh, std::true_type{});
+      } else {
+#pragma unroll
+        for (int kh = kq; kh < KS; kh += 4)
+          if (kh < n) ktile(kh, std::false_type{});
       }
     }
     __syncwarp();
@@ -949,6 +1015,15 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     }
     consumer_sync(CT);  // slots are rewritten by the next segment
     ++rt;
+  }
+  return ok;
+  };
+  bool ok;
+  if constexpr (FMT == FMT_MX && !GRP && MT == 8) {
+    if (wide) ok = consume(std::true_type{});
+    else ok = consume(std::false_type{});
+  } else {
+    ok = consume(std::false_type{});
   }
   if (!ok && lane == 0) atomicExch(p.status, 5);
   if (p.g_idx) {

@@ -133,6 +133,9 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 // Instruction descriptor: kind::f16, A = B = f16, D = f32, both K-major, M = 128, N = 256.
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                             ((uint32_t)(kBM >> 4) << 24);
+// The same with A = B = bf16 (the operand-format fields: 0 = f16, 1 = bf16): the tiles of a
+// wide MXFP4 weight, whose exact values c * 2^(e - 127) need bf16's exponent range.
+constexpr uint32_t kIdescBF16 = kIdesc | (1u << 7) | (1u << 10);
 
 __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   uint64_t p;
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const uint32_t idesc = (FMT == FMT_MX && p.hdr->wide) ? kIdescBF16 : kIdesc;
       uint32_t ia = 0, pa = 0, ib = 0, pb = 0, ab = 0, pab = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint64_t bd = desc_sw128(sB + ib * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)  // +32 bytes per 16-element k step
-            mma_f16(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
           mma_commit(a_empty + 8 * ia);
           mma_commit(b_empty + 8 * ib);
           if (++ia == kAStages) { ia = 0; pa ^= 1u; }
@@ -310,6 +314,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // rows 16d+g and 16d+g+8 for physical k [16t, 16t+16) of the k tile (one scale each).
     const int d = warp - 2, g = lane >> 2, t = lane & 3;
     const int soff = scale_offset(FMT, d, g, t);
+    // wide MXFP4 weight: the raw E8M0 bytes give exact bf16 tiles c * 2^(e - 127)
+    const bool wide = FMT == FMT_MX && p.hdr->wide != 0;
     uint32_t ip = 0, pp = 0, ib = 0, pb = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
@@ -334,6 +340,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t og[2][8], o8[2][8];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
+          if (FMT == FMT_MX && wide) {
+            // c (exact in f16) -> fp32, times the exact group scale, -> bf16 (exact: at most
+            // two significant bits, >= 2^-128; 6 * 2^127 overflows to inf as in fp32)
+            const float wg = e8m0_to_f32(sc[r] & 0xFFu), wg8 = e8m0_to_f32((sc[r] >> 8) & 0xFFu);
+            const uint32_t words[4] = {(uint32_t)cw[r].x, (uint32_t)cw[r].y, (uint32_t)cw[r].z,
+                                       (uint32_t)cw[r].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t c4[4];
+              e2m1x8_to_f16x8(words[q], c4[0], c4[1], c4[2], c4[3]);
+              uint32_t o4[4];
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const __half2 hc = *reinterpret_cast<const __half2*>(&c4[b]);
+                const float sw = (b & 1) ? wg8 : wg;
+                const __nv_bfloat162 hb =
+                    __floats2bfloat162_rn(__low2float(hc) * sw, __high2float(hc) * sw);
+                o4[b] = *reinterpret_cast<const uint32_t*>(&hb);
+              }
+              og[r][2 * q] = o4[0];
+              og[r][2 * q + 1] = o4[2];
+              o8[r][2 * q] = o4[1];
+              o8[r][2 * q + 1] = o4[3];
+            }
+            continue;
+          }
           const uint32_t s2 = (FMT == FMT_NV) ? e4m3x2_to_f16x2(sc[r]) : mxenc2_to_f16x2(sc[r]);
           const __half2 sh = *reinterpret_cast<const __half2*>(&s2);
           const __half2 sg = __low2half2(sh), sg8 = __high2half2(sh);
@@ -497,17 +529,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 // --------------------------------------------------------------- activation pre-pass
 // A[m][k] (bf16) -> A'[m][k] = A * 2^-p (f16), p = (exponent of the row's largest
-// magnitude) - 14, clamped to [-120, 113]; rowscale[m] = 2^p.  One CTA per token row.
+// magnitude) - 14, clamped to [-120, 113]; rowscale[m] = 2^p.  One CTA per token row.  For
+// a wide MXFP4 weight (bf16 tiles) A' is A itself (bf16) and rowscale 1.
 constexpr int kRowThreads = 256;
 
 __global__ void __launch_bounds__(kRowThreads) k_prep_rows(const __nv_bfloat16* __restrict__ A,
                                                            int64_t lda, int64_t K, int64_t ldp,
                                                            __half* __restrict__ Ap,
-                                                           float* __restrict__ rowscale) {
+                                                           float* __restrict__ rowscale,
+                                                           const PackedHeader* __restrict__ hdr) {
   __shared__ int s_max[kRowThreads / 32];
   const int64_t m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(A + m * lda);
   const int64_t ng = K / 8;
+  if (hdr->fmt == FMT_MX && hdr->wide) {
+    uint4* dst = reinterpret_cast<uint4*>(Ap + m * ldp);
+    for (int64_t i = threadIdx.x; i < ng; i += kRowThreads) dst[i] = __ldg(row + i);
+    if (threadIdx.x == 0) rowscale[m] = 1.0f;
+    return;
+  }
   int mx = 0;
   for (int64_t i = threadIdx.x; i < ng; i += kRowThreads) {
     const uint4 v = __ldg(row + i);
@@ -534,19 +574,43 @@ __global__ void __launch_bounds__(kRowThreads) k_prep_rows(const __nv_bfloat16* 
 // W4A4: the activations quantised to the weight's block format (fp32 decisions, actq.cuh)
 // and written as their exact dequantised values: NVFP4 A' = c * s, rowscale = alpha; MXFP4
 // A' = c * 2^(e - p), p = (the row's largest group exponent) - 12, at least -126,
-// rowscale = 2^p.  One CTA per token row, one group per thread; a group holding an inf or
-// NaN is written as NaN.
+// rowscale = 2^p; for a wide MXFP4 weight (bf16 tiles) A' = c * 2^e in bf16, rowscale 1.
+// One CTA per token row, one group per thread; a group holding an inf or NaN is written as
+// NaN.
 template <int FMT>
 __global__ void __launch_bounds__(kRowThreads) k_prep_rows4(const __nv_bfloat16* __restrict__ A,
                                                             int64_t lda, int64_t K, int64_t ldp,
                                                             __half* __restrict__ Ap,
                                                             float* __restrict__ rowscale,
-                                                            float alpha, float alpha6) {
+                                                            float alpha, float alpha6,
+                                                            const PackedHeader* __restrict__ hdr) {
   constexpr int G = FMT == FMT_NV ? 16 : 32, NG = G / 8;
   const int64_t m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(A + m * lda);
   const int64_t ngr = K / G;
   int p = 0;
+  if (FMT == FMT_MX && hdr->wide) {
+    uint4* dst = reinterpret_cast<uint4*>(Ap + m * ldp);
+    for (int64_t grp = threadIdx.x; grp < ngr; grp += kRowThreads) {
+      uint32_t w[NG][4];
+      int mg = 0;
+#pragma unroll
+      for (int v = 0; v < NG; ++v) {
+        const uint4 x = __ldg(row + grp * NG + v);
+        w[v][0] = x.x;
+        w[v][1] = x.y;
+        w[v][2] = x.z;
+        w[v][3] = x.w;
+        mg = max(mg, act_maxmag8(w[v]));
+      }
+      const bool bad = mg >= 0x7F80;
+      const int e = aq_mx_exp(__uint_as_float((uint32_t)(bad ? 0 : mg) << 16));
+#pragma unroll
+      for (int v = 0; v < NG; ++v) dst[grp * NG + v] = aq_mx_granule_bf16(w[v], e, bad);
+    }
+    if (threadIdx.x == 0) rowscale[m] = 1.0f;
+    return;
+  }
   if constexpr (FMT == FMT_MX) {
     __shared__ int s_max[kRowThreads / 32];
     int mx = 0;
@@ -636,14 +700,15 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   // the activation pre-pass writes A' rows [0, M) with row stride Kp
   const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(L.A);
   __half* ap = reinterpret_cast<__half*>(L.Ap);
+  const PackedHeader* hdr = reinterpret_cast<const PackedHeader*>(L.packed);
   if (!L.w4a4)
-    k_prep_rows<<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale);
+    k_prep_rows<<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale, hdr);
   else if (L.fmt == FMT_NV)
     k_prep_rows4<FMT_NV><<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale,
-                                                              L.alpha, 6.0f * L.alpha);
+                                                              L.alpha, 6.0f * L.alpha, hdr);
   else
     k_prep_rows4<FMT_MX><<<(unsigned)L.M, kRowThreads, 0, s>>>(a, L.lda, L.K, Kp, ap, L.rowscale,
-                                                              L.alpha, 6.0f * L.alpha);
+                                                              L.alpha, 6.0f * L.alpha, hdr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // A' as a 2-D tensor {K, M}: reads past K or M return zeros

@@ -34,14 +34,18 @@ __global__ void k_header(PackedHeader* h, int fmt, int64_t N, int64_t K, int64_t
     h->factor[1] = f1;
     h->emax[0] = -1;
     h->emax[1] = -1;
+    h->emin[0] = 256;
+    h->emin[1] = 256;
+    h->wide = 0;
   }
 }
 
-// MXFP4: largest finite E8M0 byte of each segment.
+// MXFP4: largest and smallest finite E8M0 byte of each segment (over every group, whatever
+// its codes, so that the packed form keeps every byte recoverable).
 __global__ void k_mx_emax(SrcPair s, int64_t N, int64_t K, PackedHeader* h) {
   const int64_t gpr = K / 32;
   const int64_t total = N * gpr;
-  int local[2] = {-1, -1};
+  int hi[2] = {-1, -1}, lo[2] = {256, 256};
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     int64_t row = i / gpr, grp = i % gpr;
@@ -49,28 +53,47 @@ __global__ void k_mx_emax(SrcPair s, int64_t N, int64_t K, PackedHeader* h) {
     int64_t r;
     src_row(s, row, which, r);
     int e = s.scales[which][r * gpr + grp];
-    if (e != 0xFF) local[which] = max(local[which], e);
+    if (e != 0xFF) {
+      hi[which] = max(hi[which], e);
+      lo[which] = min(lo[which], e);
+    }
   }
   for (int w = 0; w < 2; ++w) {
-    int v = local[w];
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if ((threadIdx.x & 31) == 0 && v >= 0) atomicMax(&h->emax[w], v);
+    int v = hi[w], u = lo[w];
+    for (int o = 16; o > 0; o >>= 1) {
+      v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+      u = min(u, __shfl_xor_sync(0xffffffffu, u, o));
+    }
+    if ((threadIdx.x & 31) == 0 && v >= 0) {
+      atomicMax(&h->emax[w], v);
+      atomicMin(&h->emin[w], u);
+    }
   }
 }
 
-// MXFP4: fix the per-segment epilogue factor 2^(emax - 140) once emax is known.
+// MXFP4: choose the scale encoding once the exponent range is known.  When every segment's
+// finite scale bytes lie within the 30 exponents [emax - 29, emax], the tiles hold them as
+// f16 powers of two relative to emax (mx_encode) and the epilogue factor is 2^(emax - 140);
+// otherwise (a wider range) the tiles keep the raw bytes, the kernels multiply each group by
+// its exact scale 2^(e - 127) in fp32, and the factor is 1.
 __global__ void k_mx_factor(PackedHeader* h) {
-  if (threadIdx.x < 2) {
-    int e = h->emax[threadIdx.x];
-    if (e < 0) e = 127;  // no finite scale: any offset works
-    h->emax[threadIdx.x] = e;
-    h->factor[threadIdx.x] = ldexpf(1.0f, e - 140);
+  if (threadIdx.x == 0) {
+    bool wide = false;
+    for (int w = 0; w < 2; ++w) {
+      int e = h->emax[w];
+      if (e < 0) e = 127;  // no finite scale: any offset works
+      h->emax[w] = e;
+      if (h->emin[w] <= 255 && h->emin[w] < e - 29) wide = true;
+    }
+    h->wide = wide ? 1u : 0u;
+    for (int w = 0; w < 2; ++w) h->factor[w] = wide ? 1.0f : ldexpf(1.0f, h->emax[w] - 140);
   }
 }
 
 // E8M0 byte -> high byte of the f16 2^x, x = e - emax + 13, so that the largest scale of
 // the segment maps to 2^13 (codes up to 6 stay below the f16 limit) and scales down to
-// 2^-16 stay exact; smaller ones flush to 0; 0xFF (NaN) maps to an f16 NaN.
+// 2^-16 stay exact; 0xFF (NaN) maps to an f16 NaN.  Used only when every finite byte of the
+// weight lies in that window (k_mx_factor), so no scale is lost.
 __device__ __forceinline__ uint8_t mx_encode(int e, int emax) {
   if (e == 0xFF) return 0x7E;
   int x = e - emax + 13;
@@ -132,7 +155,7 @@ __global__ void __launch_bounds__(256) k_pack(SrcPair s, int fmt, int64_t N, int
         int64_t r;
         src_row(s, row, which, r);
         const uint8_t b = s.scales[which][r * gpr + grp];
-        v = nv ? b : mx_encode(b, h->emax[which]);
+        v = (nv || h->wide) ? b : mx_encode(b, h->emax[which]);
       }
       pair |= v << (8 * half);
     }
@@ -141,8 +164,8 @@ __global__ void __launch_bounds__(256) k_pack(SrcPair s, int fmt, int64_t N, int
   }
 }
 
-// Inverse of k_pack for the codes and (NVFP4) scale bytes.  MXFP4 scale bytes are
-// recovered from the re-encoding and the segment's emax.
+// Inverse of k_pack for the codes and scale bytes.  MXFP4 scale bytes of a narrow weight are
+// recovered from the re-encoding and the segment's emax; a wide weight keeps them raw.
 __device__ __forceinline__ int mx_decode(uint8_t enc, int emax) {
   if (enc == 0x7E) return 0xFF;
   int x;
@@ -185,7 +208,7 @@ __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, i
       const int64_t row = packed_to_row(layout, rt * kTileRows + j * 16 + g + half * 8, N, split);
       if (row >= 0 && grp < gpr) {
         const uint8_t b = (pair >> (8 * half)) & 0xFF;
-        if (nv) {
+        if (nv || h->wide) {
           scales[row * gpr + grp] = b;
         } else {
           int e = mx_decode(b, h->emax[row < split ? 0 : 1]);
@@ -197,7 +220,9 @@ __global__ void __launch_bounds__(256) k_unpack(const uint8_t* tiles, int fmt, i
 }
 
 // Dequantise through the same conversions the GEMM uses: E2M1 pair -> f16x2, scale ->
-// f16x2, one f16 multiply (exact), then fp32 multiply by the segment factor.
+// f16x2, one f16 multiply (exact), then fp32 multiply by the segment factor.  A wide MXFP4
+// weight (raw E8M0 bytes in its tiles) gives c * 2^(e - 127) by one fp32 multiply of the
+// code's value by the exact scale, as its GEMM does.
 __global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, int64_t N,
                                                  int64_t K, int64_t KT, int64_t split,
                                                  uint32_t layout, const PackedHeader* h,
@@ -210,23 +235,35 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* tiles, int fmt, 
   uint4 v = *reinterpret_cast<const uint4*>(in + j * 512 + lane * 16);
   uint32_t words[4] = {v.x, v.y, v.z, v.w};
   const uint32_t two = *reinterpret_cast<const uint16_t*>(in + scale_offset(fmt, j, g, t));
+  const bool wide = fmt == FMT_MX && h->wide;
   const uint32_t sc2 = (fmt == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
   const uint32_t s_g = bcast_lo(sc2), s_g8 = bcast_hi(sc2);
+  const float w_g = e8m0_to_f32(two & 0xFFu), w_g8 = e8m0_to_f32(two >> 8);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t r[4];
     e2m1x8_to_f16x8(words[q], r[0], r[1], r[2], r[3]);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      uint32_t p = hmul2_u32(r[b], (b & 1) ? s_g8 : s_g);
-      __half2 hp = *reinterpret_cast<__half2*>(&p);
       const int64_t row =
           packed_to_row(layout, rt * kTileRows + j * 16 + g + ((b & 1) ? 8 : 0), N, split);
       int64_t k0 = kt * kTileK + 16 * t + 4 * q + ((b >> 1) ? 2 : 0);
       if (row >= 0 && k0 < K) {
-        float f = h->factor[row < split ? 0 : 1];
-        out[row * K + k0] = __low2float(hp) * f;
-        out[row * K + k0 + 1] = __high2float(hp) * f;
+        float lo, hi;
+        if (wide) {
+          const __half2 hc = *reinterpret_cast<const __half2*>(&r[b]);
+          const float sw = (b & 1) ? w_g8 : w_g;
+          lo = __low2float(hc) * sw;
+          hi = __high2float(hc) * sw;
+        } else {
+          uint32_t p = hmul2_u32(r[b], (b & 1) ? s_g8 : s_g);
+          __half2 hp = *reinterpret_cast<__half2*>(&p);
+          float f = h->factor[row < split ? 0 : 1];
+          lo = __low2float(hp) * f;
+          hi = __high2float(hp) * f;
+        }
+        out[row * K + k0] = lo;
+        out[row * K + k0 + 1] = hi;
       }
     }
   }
