@@ -19,7 +19,7 @@ GROUP = {NVFP4: 16, MXFP4: 32}
 
 __all__ = ["NVFP4", "MXFP4", "GROUP", "PackedWeight", "w4a16_gemm", "w4a16_gemm_noalloc",
            "w4a16_gemm_greedy", "w4a16_gemm_silu_mul", "w4a16_gemm_moe", "w4a4_gemm",
-           "quantize_act", "quantize", "prepack_bytes", "workspace_status", "VtError",
+           "quantize_act", "quantize", "prepack_bytes", "workspace_status", "noalloc_status", "VtError",
            "algorithmic_bytes"]
 
 
@@ -344,6 +344,15 @@ def w4a16_gemm_noalloc(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | Non
                                           out.stride(0), _stream(stream)),
           "vt_fp4_w4a16_gemm_noalloc")
     return out
+
+
+def noalloc_status(stream=None) -> int:
+    """The no-alloc scratch area's status word on the current device (0, or VT_ERR_TIMEOUT
+    when a bounded wait of an earlier w4a16_gemm_noalloc call gave up); read and cleared,
+    synchronising the stream."""
+    st = ctypes.c_int(0)
+    check(lib().vt_fp4_noalloc_status(_stream(stream), ctypes.byref(st)), "vt_fp4_noalloc_status")
+    return st.value
 
 
 def workspace_status(workspace: torch.Tensor, stream=None) -> int:

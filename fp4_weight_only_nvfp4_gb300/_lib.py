@@ -53,6 +53,8 @@ SIGNATURES = {
     "vt_fp4_w4a16_gemm_ex": (_ST, [_P, _I64, _I64, _P, _P, _I64, _P, _SZ, _P,
                                    ctypes.POINTER(GemmOpts)]),
     "vt_fp4_w4a16_gemm_noalloc": (_ST, [_P, _I64, _I64, _P, _P, _I64, _P]),
+    "vt_fp4_noalloc_status": (_ST, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "vt_fp4_noalloc_test_hooks": (_ST, [ctypes.c_int, ctypes.c_int]),
     "vt_fp4_w4a16_gemm_greedy": (_ST, [_P, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "vt_fp4_workspace_status": (_ST, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "vt_fp4_stats": (_ST, [_P, ctypes.POINTER(LaunchInfo)]),

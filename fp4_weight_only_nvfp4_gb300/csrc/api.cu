@@ -110,19 +110,6 @@ MoeLayout moe_layout(const vt_fp4_weight_s* W, int64_t npairs) {
   return L;
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 vt_status do_prepack(const uint8_t* const codes[2], const uint8_t* const scales[2],
                      const float globals[2], int nsrc, vt_fp4_format fmt, int64_t I, int64_t K,
                      void* dst, size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out,
@@ -191,6 +178,52 @@ vt_status check_handle(vt_fp4_handle W) {
 }  // namespace
 
 vt_status vt::set_last_error(vt_status st, const char* msg) { return fail(st, "%s", msg); }
+
+int vt::sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+vt_status vt::decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_opts* opts,
+                           bool w4a4, DecodeShape* out) {
+  const int64_t items = W->RT * W->KT;
+  // k tiles per pipeline stage (8: up to 37 KB of weights per TMA copy) and ring depth
+  const int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
+  if (ks != 4 && ks != 8) return fail(VT_ERR_INVALID_ARG, "stage width must be 4 or 8 k tiles");
+  // small M * K: the decode kernel converts the activations itself (no pre-pass)
+  const bool resident = !w4a4 && !(opts && opts->force_path == 3) &&
+                        decode_resident_ok(M, W->KT, W->RT);
+  const int64_t rkt = resident ? W->KT : 0;
+  int stages = (opts && opts->stages) ? opts->stages : 0;
+  if (!stages) {  // as deep as shared memory allows, at most 6
+    stages = 6;
+    while (stages > 2 && decode_smem_bytes(W->fmt, M, ks, stages, rkt) > 226 * 1024) --stages;
+  }
+  if (stages < 2 || stages > 16) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 16]");
+  if (decode_smem_bytes(W->fmt, M, ks, stages, rkt) > 226 * 1024)
+    return fail(VT_ERR_INVALID_ARG, "stage width x stages exceed shared memory");
+  int64_t grid = (opts && opts->grid) ? opts->grid : sm_count();
+  if (!(opts && opts->grid)) {
+    const int64_t per_cta = 2 * ks;  // at least two stages of work per CTA
+    grid = grid < cdiv(items, per_cta) ? grid : cdiv(items, per_cta);
+  }
+  if (grid > items) grid = items;
+  if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
+  if (grid < 1) grid = 1;
+  out->ks = ks;
+  out->stages = stages;
+  out->grid = (int)grid;
+  out->resident = resident ? 1 : 0;
+  return VT_OK;
+}
 
 extern "C" {
 
@@ -361,40 +394,19 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     D.Ap = ws + L.ap;
     D.partials = reinterpret_cast<float*>(ws + L.partials);
     const int64_t items = W->RT * W->KT;
-    // k tiles per pipeline stage (8: up to 37 KB of weights per TMA copy) and ring depth
-    int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
-    if (ks != 4 && ks != 8) return fail(VT_ERR_INVALID_ARG, "stage width must be 4 or 8 k tiles");
     const int mt = decode_mt((int)M);
-    // small M * K: the decode kernel converts the activations itself (no pre-pass)
-    const bool resident = !w4a4 && !(opts && opts->force_path == 3) &&
-                          decode_resident_ok((int)M, W->KT, W->RT);
-    const int64_t rkt = resident ? W->KT : 0;
-    int stages = (opts && opts->stages) ? opts->stages : 0;
-    if (!stages) {  // as deep as shared memory allows, at most 6
-      stages = 6;
-      while (stages > 2 && decode_smem_bytes(W->fmt, (int)M, ks, stages, rkt) > 226 * 1024) --stages;
-    }
-    if (stages < 2 || stages > 16) return fail(VT_ERR_INVALID_ARG, "stages must be in [2, 16]");
-    if (decode_smem_bytes(W->fmt, (int)M, ks, stages, rkt) > 226 * 1024)
-      return fail(VT_ERR_INVALID_ARG, "stage width x stages exceed shared memory");
-    int64_t grid = (opts && opts->grid) ? opts->grid : sm_count();
-    if (!(opts && opts->grid)) {
-      const int64_t per_cta = 2 * ks;  // at least two stages of work per CTA
-      grid = grid < cdiv(items, per_cta) ? grid : cdiv(items, per_cta);
-    }
-    if (grid > items) grid = items;
-    if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
-    if (grid < 1) grid = 1;
-    D.grid = (int)grid;
-    D.ks = ks;
-    D.stages = stages;
+    DecodeShape sh;
+    if (vt_status st = decode_shape(W, (int)M, opts, w4a4, &sh)) return st;
+    D.grid = sh.grid;
+    D.ks = sh.ks;
+    D.stages = sh.stages;
     D.wait_ns = (opts && opts->wait_limit_us > 0) ? (uint64_t)opts->wait_limit_us * 1000ull : 0;
     D.withhold = opts ? opts->withhold_weights : 0;
     D.layout = (uint32_t)W->layout;
     D.silu = silu ? 1 : 0;
     D.w4a4 = w4a4 ? 1 : 0;
     D.alpha = alpha;
-    D.resident = resident ? 1 : 0;
+    D.resident = sh.resident;
     if (g_idx) {
       D.g_idx = g_idx;
       D.g_val = g_val;

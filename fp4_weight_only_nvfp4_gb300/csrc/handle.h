@@ -20,4 +20,17 @@ struct vt_fp4_weight_s {
 namespace vt {
 // Records the message returned by vt_fp4_last_error() for this thread; returns st.
 vt_status set_last_error(vt_status st, const char* msg);
+
+// Multiprocessors of the current device (cached per device).
+int sm_count();
+
+// Launch shape of the decode GEMM (M <= 16) on W: k tiles per pipeline stage, ring depth, CTAs
+// and whether the kernel converts the activations itself (resident mode).  `opts` may be NULL
+// (library choice); w4a4 calls always take the activation pre-pass.  Shared by every decode
+// entry point so that they launch the same shapes.
+struct DecodeShape {
+  int ks, stages, grid, resident;
+};
+vt_status decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_opts* opts, bool w4a4,
+                       DecodeShape* out);
 }  // namespace vt

@@ -4,9 +4,11 @@
 // HBM up front, a plugin inside a framework that forbids foreign allocations) or a call
 // path that must not block on, or fail in, a runtime allocation.  This entry point uses a
 // fixed scratch area that lives in this library's own device image instead of a caller
-// workspace.
+// workspace.  vt_fp4_noalloc_status reads the status word that area keeps, and
+// vt_fp4_noalloc_test_hooks lets a test make its bounded waits run out.
 #include <stdio.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -18,12 +20,15 @@ namespace {
 using namespace vt;
 
 // 4 MiB of device memory, held by every GPU that loads this library until the process
-// exits.  It holds the per-call split-K arrival counters, the activation scales, the
-// converted activations and the split-K partial sums.
+// exits.  It holds the status word, the per-call split-K arrival counters, the activation
+// scales, the converted activations and the split-K partial sums.
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// Test hooks (vt_fp4_noalloc_test_hooks): the limit of the kernels' bounded waits and the
+// weight-producer switch of vt_fp4_gemm_opts, for the calls that follow.
+std::atomic<int> g_hook_wait_us{0}, g_hook_withhold{0};
+
 inline size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -47,6 +52,8 @@ cudaError_t scratch_address(int dev, void** out) {
 
 vt_status err(vt_status st, const char* msg) { return set_last_error(st, msg); }
 
+vt_status cuda_err(cudaError_t e) { return err(VT_ERR_CUDA, cudaGetErrorString(e)); }
+
 }  // namespace
 
 extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t lda,
@@ -54,6 +61,7 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
                                                vt_stream_t s) {
   char msg[256];
   if (!W) return err(VT_ERR_INVALID_ARG, "weight handle is NULL");
+  if (W->E > 1) return err(VT_ERR_INVALID_ARG, "a grouped weight serves vt_fp4_w4a16_gemm_moe");
   if (M < 0) return err(VT_ERR_INVALID_ARG, "M must be >= 0");
   if (M == 0) return VT_OK;
   if (M > 16) return err(VT_ERR_UNSUPPORTED, "the no-alloc GEMM serves M <= 16 only");
@@ -62,21 +70,18 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   if (!aligned(A, 16) || lda % 8)
     return err(VT_ERR_MISALIGNED, "A must be 16-byte aligned with lda % 8 == 0");
   if (!aligned(C, 2)) return err(VT_ERR_MISALIGNED, "C must be 2-byte aligned");
+  if (W->K > 110000) return err(VT_ERR_UNSUPPORTED, "K > 110000 is not supported");
 
-  int dev = 0, sms = 0;
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return err(VT_ERR_CUDA, cudaGetErrorString(e));
+  if (e != cudaSuccess) return cuda_err(e);
 
-  // launch shape: the library's default decode shape
-  const int ks = 8;
-  const int64_t items = W->RT * W->KT;
-  int64_t grid = sms < cdiv(items, 2 * ks) ? sms : cdiv(items, 2 * ks);
-  if (grid > items) grid = items;
-  if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
-  if (grid < 1) grid = 1;
-  int stages = 6;
-  while (stages > 2 && decode_smem_bytes(W->fmt, (int)M, ks, stages) > 226 * 1024) --stages;
+  // launch shape: the same choice as vt_fp4_w4a16_gemm makes
+  vt_fp4_gemm_opts hooks = {};
+  hooks.wait_limit_us = g_hook_wait_us.load();
+  hooks.withhold_weights = g_hook_withhold.load();
+  DecodeShape sh;
+  if (vt_status st = decode_shape(W, (int)M, nullptr, false, &sh)) return st;
   const int mt = decode_mt((int)M);
 
   // scratch layout: status | counters [RT] | activation scales [KT][16] | activations
@@ -85,7 +90,7 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   const size_t o_ascale = up256(o_counters + (size_t)W->RT * 4);
   const size_t o_ap = up256(o_ascale + (size_t)W->KT * 16 * 4);
   const size_t o_part = up256(o_ap + (size_t)W->KT * M * 128);
-  const size_t need = up256(o_part + (size_t)grid * 2 * mt * 128 * 4);
+  const size_t need = up256(o_part + (size_t)sh.grid * 2 * mt * 128 * 4);
   if (need > kNoAllocScratchBytes) {
     snprintf(msg, sizeof(msg),
              "this weight and M need %zu bytes of scratch; the no-alloc scratch holds %zu",
@@ -94,11 +99,12 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   }
   void* base = nullptr;
   e = scratch_address(dev, &base);
-  if (e != cudaSuccess) return err(VT_ERR_CUDA, cudaGetErrorString(e));
+  if (e != cudaSuccess) return cuda_err(e);
   uint8_t* ws = static_cast<uint8_t*>(base);
-  // the status word and the arrival counters must start at zero
-  e = cudaMemsetAsync(ws, 0, o_ascale, (cudaStream_t)s);
-  if (e != cudaSuccess) return err(VT_ERR_CUDA, cudaGetErrorString(e));
+  // the arrival counters must start at zero (a call that gave up may have left counts); the
+  // status word is left alone until vt_fp4_noalloc_status reads it
+  e = cudaMemsetAsync(ws + o_counters, 0, o_ascale - o_counters, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_err(e);
 
   DecodeLaunch D;
   D.packed = W->packed;
@@ -118,21 +124,50 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   D.ascale = reinterpret_cast<float*>(ws + o_ascale);
   D.Ap = ws + o_ap;
   D.partials = reinterpret_cast<float*>(ws + o_part);
-  D.grid = (int)grid;
-  D.ks = ks;
-  D.stages = stages;
-  D.wait_ns = 0;  // the default limit
-  D.withhold = 0;
+  D.grid = sh.grid;
+  D.ks = sh.ks;
+  D.stages = sh.stages;
+  D.wait_ns = hooks.wait_limit_us > 0 ? (uint64_t)hooks.wait_limit_us * 1000ull : 0;
+  D.withhold = hooks.withhold_weights;
   D.layout = (uint32_t)W->layout;
+  D.resident = sh.resident;
   int launches = 0;
   e = launch_decode(D, (cudaStream_t)s, &launches);
-  if (e != cudaSuccess) return err(VT_ERR_CUDA, cudaGetErrorString(e));
+  if (e != cudaSuccess) return cuda_err(e);
   W->info.path = 1;
   W->info.grid = D.grid;
   W->info.warps_per_cta = 18;
   W->info.m_tile = mt;
-  W->info.items = items;
+  W->info.items = W->RT * W->KT;
   W->info.launches = launches;
   W->info.calls += 1;
+  return VT_OK;
+}
+
+extern "C" vt_status vt_fp4_noalloc_status(vt_stream_t s, int* status) {
+  if (!status) return err(VT_ERR_INVALID_ARG, "status must be set");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  void* base = nullptr;
+  if (e == cudaSuccess) e = scratch_address(dev, &base);
+  int v = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&v, base, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_err(e);
+  *status = v;
+  if (v) {
+    const int zero = 0;
+    e = cudaMemcpyAsync(base, &zero, sizeof(int), cudaMemcpyHostToDevice, (cudaStream_t)s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)s);
+    if (e != cudaSuccess) return cuda_err(e);
+  }
+  return VT_OK;
+}
+
+extern "C" vt_status vt_fp4_noalloc_test_hooks(int wait_limit_us, int withhold_weights) {
+  if (wait_limit_us < 0) return err(VT_ERR_INVALID_ARG, "wait_limit_us must be >= 0");
+  g_hook_wait_us.store(wait_limit_us);
+  g_hook_withhold.store(withhold_weights ? 1 : 0);
   return VT_OK;
 }

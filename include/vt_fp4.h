@@ -21,11 +21,19 @@
  *   - Pointers marked (device) are CUDA device pointers owned by the caller; (host) are
  *     host pointers.  The library never allocates device memory and keeps no global
  *     cache keyed by address: all state of a prepacked weight lives in its handle and in
- *     the caller's packed buffer.
+ *     the caller's packed buffer.  Source: "keep the ModelOpt NVFP4 lm_head packed"
+ *     (PR #263), "Round-2 findings resolved", item 1 (residency is a property of the
+ *     weight, not of the GEMM) and "Merge with origin/main" (#237 / #276: the weights own
+ *     their resident device state, not a static address map, which reused stale pointers
+ *     after teardown).
  *   - Work is enqueued on the caller's stream `s` and is asynchronous; no entry point
- *     synchronises the device except vt_fp4_workspace_status.
- *   - Every entry returns a vt_status and never aborts.  On failure nothing is enqueued
- *     and vt_fp4_last_error() returns a message for the calling thread.
+ *     synchronises the device except vt_fp4_workspace_status and vt_fp4_noalloc_status.
+ *   - Every entry returns a vt_status and never aborts, and no entry falls back to another
+ *     path when its own cannot run: a case it does not serve is an error.  On failure
+ *     nothing is enqueued and vt_fp4_last_error() returns a message for the calling thread.
+ *     Source: same page, "Round-2 findings resolved", the backend-asymmetric hard abort
+ *     (an abort is recorded as a defect) and why it was preferred to a silent fall-through
+ *     (a head that quietly lost its packed form costs throughput with no other symptom).
  *   - Built for sm_103a only; on another device the launches fail with VT_ERR_CUDA.
  */
 #ifndef VT_FP4_H
@@ -88,7 +96,11 @@ typedef struct {
 
 /* Exact size in bytes of the prepacked buffer for an N x K weight of format `fmt`:
  * a 256-byte header plus ceil(N/128)*ceil(K/64) tiles of 4608 (NVFP4) or 4352 (MXFP4)
- * bytes.  Requires N > 0, K > 0, K % 16 == 0 (NVFP4) or K % 32 == 0 (MXFP4). */
+ * bytes (the packed codes and scales plus padding of at most one tile in each direction).
+ * Requires N > 0, K > 0, K % 16 == 0 (NVFP4) or K % 32 == 0 (MXFP4).  Source: "keep the
+ * ModelOpt NVFP4 lm_head packed" (PR #263), "Round-2 findings resolved", item 5: the packed
+ * head's operands had been built 4 bytes per element and are now exactly sized; the caller
+ * allocates exactly this many bytes. */
 vt_status vt_fp4_prepack_bytes(vt_fp4_format fmt, int64_t N, int64_t K, size_t* packed_bytes);
 
 /* ------------------------------------------------------------------- prepack */
@@ -133,7 +145,10 @@ vt_status vt_fp4_prepack_gate_up_paired(const uint8_t* gate_codes, const uint8_t
                                         vt_fp4_format fmt, int64_t I, int64_t K, void* packed_dst,
                                         size_t dst_bytes, vt_stream_t s, vt_fp4_handle* out);
 
-/* Frees the host-side handle (never device memory). NULL is a no-op. */
+/* Frees the host-side handle (never device memory); the caller frees the packed buffer
+ * afterwards.  NULL is a no-op.  Source: "keep the ModelOpt NVFP4 lm_head packed" (PR #263),
+ * "Merge with origin/main" (#237 / #276): a weight's resident state is owned by the weight and
+ * released with it, never kept in a cache keyed by address. */
 vt_status vt_fp4_destroy(vt_fp4_handle W);
 
 /* Shape and format of a handle. */
@@ -238,17 +253,34 @@ vt_status vt_fp4_w4a16_gemm_greedy(const void* A, int64_t M, int64_t lda, vt_fp4
  * that reserves memory up front, a plugin whose host forbids foreign allocations) or a
  * call path that must not depend on a runtime allocation.  The pages have no counterpart
  * of this entry point; it exists for such callers only.
- *   A, M, lda, W, C, ldc, s  as for vt_fp4_w4a16_gemm (M <= 16; M == 0 is a no-op).
+ *   A, M, lda, W, C, ldc, s  as for vt_fp4_w4a16_gemm (M <= 16; M == 0 is a no-op); the
+ *   launch shape is the one vt_fp4_w4a16_gemm chooses.  A grouped weight is rejected with
+ *   VT_ERR_INVALID_ARG, K > 110000 with VT_ERR_UNSUPPORTED.
  * It uses one scratch area of 4 MiB inside the library's device image instead of a
  * workspace; every GPU that loads the library holds that area until the process exits.
  * A weight and M whose scratch needs exceed it are rejected with VT_ERR_UNSUPPORTED.
  * It allocates nothing: no cudaMalloc, no cudaFree.  The first call on a device looks up
  * the scratch area's device address (with that device current), so make that first call
- * before any stream capture.  Every call shares the same area and clears its counters on
- * the stream first: calls that may overlap on the GPU (other streams, other threads) race
- * and must not be issued. */
+ * before any stream capture.  Every call shares the same area and clears its split-K
+ * counters on the stream first: calls that may overlap on the GPU (other streams, other
+ * threads) race and must not be issued.  A bounded device-side wait that gives up records
+ * VT_ERR_TIMEOUT in the area's status word, which stays set until vt_fp4_noalloc_status
+ * reads it. */
 vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t lda, vt_fp4_handle W,
                                     void* C, int64_t ldc, vt_stream_t s);
+
+/* The status word of the no-alloc scratch area on the current device (synchronises `s`):
+ * *status = VT_OK, or VT_ERR_TIMEOUT if a bounded wait of an earlier
+ * vt_fp4_w4a16_gemm_noalloc call gave up (that call's output is then undefined); the word
+ * is then cleared.  No counterpart on the pages (see vt_fp4_w4a16_gemm_noalloc). */
+vt_status vt_fp4_noalloc_status(vt_stream_t s, int* status);
+
+/* Test hook of vt_fp4_w4a16_gemm_noalloc, whose signature has no options: for the calls
+ * made after it, every bounded device-side wait gives up after wait_limit_us microseconds
+ * (0 = the 2 s default), and a nonzero withhold_weights stops the weight producer from
+ * issuing copies, as vt_fp4_gemm_opts does for the workspace entry points.  Process-wide;
+ * (0, 0) restores the defaults.  No counterpart on the pages. */
+vt_status vt_fp4_noalloc_test_hooks(int wait_limit_us, int withhold_weights);
 
 /* Reads the workspace status word (synchronises `s`): *status = VT_OK, VT_ERR_TIMEOUT if
  * a bounded device-side wait gave up during an earlier call, or 6 if a grouped call
@@ -300,7 +332,12 @@ vt_status vt_fp4_quantize_act(const void* A, int64_t M, int64_t lda, int64_t K,
 /* ------------------------------------------------------------ debug / tests */
 
 /* out (device) fp32 [N][K]: the dequantised weight as the kernels see it,
- * NVFP4 fl32(e2m1*e4m3*global) (e2m1*e4m3 is exact), MXFP4 e2m1*2^(e-127) (exact). */
+ * NVFP4 fl32(e2m1*e4m3*global) (e2m1*e4m3 is exact), MXFP4 fl32(e2m1*2^(e-127)) (exact for
+ * every scale byte 0x00..0xFE, inf where 6 * 2^127 exceeds fp32; 0xFF gives NaN).  A weight
+ * whose finite MXFP4 scale bytes span at most 30 exponents keeps them in the tiles as f16
+ * powers of two relative to the largest; a wider span keeps the raw bytes and the kernels
+ * apply each group's scale in fp32 (the decode kernel) or as exact bf16 tiles (the
+ * tensor-core path); both hold every weight exactly. */
 vt_status vt_fp4_dequant(vt_fp4_handle W, float* out, vt_stream_t s);
 
 /* Inverse of the prepack: codes (device) u8 [N][K/2] and scales (device) u8 [N][K/g] in
