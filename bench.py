@@ -228,7 +228,7 @@ class ClockSampler:
 
 
 # -------------------------------------------------------------------- GPU leg
-def _build_weights(w: Workload, copies: int, dev):
+def _build_weights(w: Workload, copies: int, dev, first_copy: int = 0):
     """GPU-side synthetic weights: bf16 N(0, 0.02) from a seeded torch generator, quantised
     by the library's quantiser, prepacked.  Returns list over copies/layers of lists of
     PackedWeight (one per projection)."""
@@ -252,7 +252,7 @@ def _build_weights(w: Workload, copies: int, dev):
             del codes, scales
         torch.cuda.synchronize()
         return sets
-    for c in range(copies):
+    for c in range(first_copy, first_copy + copies):
         layer_sets = []
         for layer in range(w.layers):
             ws = []
@@ -386,13 +386,21 @@ def job_rate(w: Workload, units_per_rank: float, world: int, seconds: float) -> 
     return _rate(w, units_per_rank * world, seconds)
 
 
-def run_gpu(args, rank: int, world: int):
+def _extra_copies(w: Workload, pi: int, n: int, dev):
+    """n more prepacked copies of projection pi (other seeds than the step's copies), for
+    per-call chains that must not find their weights in the L2."""
+    sub = Workload(w.name, w.wid, w.fmt, w.Ms, [w.projs[pi]], layers=1, kind=w.kind,
+                   extra=w.extra, note=w.note)
+    return [cs[0][0] for cs in _build_weights(sub, n, dev, first_copy=1000)]
+
+
+def run_gpu(args, rank: int, world: int, wname: str | None = None):
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
     from fp4_weight_only_nvfp4_gb300 import build as vtbuild
     vtbuild.build()
 
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[wname or args.workload]
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -534,72 +542,136 @@ def run_gpu(args, rank: int, world: int):
     sampler = ClockSampler(local)
     sampler.start()
     load_for(0.6)
+    # `repeats` timed regions of exactly K steps each, every one bracketed by a barrier and a
+    # synchronize; the step time is the median region's (max over ranks), min and max reported
+    region_ms = []
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    with torch.cuda.stream(stream):  # replay() launches on the current stream
-        t0.record(stream)
-        for _ in range(args.steps):
-            replay_step()
-        t1.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+    for _ in range(max(1, args.repeats)):
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            t0.record(stream)
+            for _ in range(args.steps):
+                replay_step()
+            t1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        region_ms.append(max_over_ranks(t0.elapsed_time(t1), dist, dev))
     load_for(0.6)
     clocks = sampler.stop()
-    ms_total = t0.elapsed_time(t1)
-    ms_total = max_over_ranks(ms_total, dist, dev)
+    ms_total = statistics.median(region_ms)
     ms_step = ms_total / args.steps
+    timing = {"repeats": len(region_ms), "steps_per_repeat": args.steps,
+              "ms_per_step_median": round(ms_step, 5),
+              "ms_per_step_min": round(min(region_ms) / args.steps, 5),
+              "ms_per_step_max": round(max(region_ms) / args.steps, 5),
+              "spread": round((max(region_ms) - min(region_ms)) / ms_total, 4)}
     value = job_rate(w, step_bytes, world, ms_step * 1e-3)
     # the outputs of the timed graph, checked before anything else runs on them
     check = self_check(w, sets, steps_calls[turn["last"]], A, C, w.extra.get("w4a4"))
 
-    # per-call durations: a second graph with an event record node around every call (the
-    # event nodes break the overlap between calls, so these durations are slightly larger
-    # than the calls' share of the timed step)
-    # (over every rotated step, so that the calls read cold weights here too)
-    all_calls = [x for sc in steps_calls for x in sc]
-    try:
-        ev = [[(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_calls)]
-              for _ in range(rot)]
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g2, stream=stream):
-                for j in range(rot):
-                    issue(ev[j], j=j)
-            for _ in range(3):
-                g2.replay()
-        stream.synchronize()
-        durs = [e[0].elapsed_time(e[1]) for evj in ev for e in evj]
-    except (TypeError, RuntimeError):
-        torch.cuda.synchronize()
-        durs = []
-        for c, layer, pi, M in all_calls:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            one_call(c, layer, pi, M)
-            e1.record(stream)
-            stream.synchronize()
-            durs.append(e0.elapsed_time(e1))
+    # per-call durations: for every (projection, M), one CUDA graph of the same call repeated
+    # back to back (no event nodes between calls, so consecutive calls overlap as in the
+    # step) on distinct weight copies whose bytes exceed twice the L2; us/call = graph time /
+    # calls.  Extra copies are built where the step's own copies are too few.
     per_call = []
-    agg = {}
-    for i, (c, layer, pi, M) in enumerate(all_calls):
-        p = w.projs[pi]
-        key = (p.name, M)
-        b = moe_bytes[(c, M)] if moe else _work(w, p.N, p.K, M)
-        a = agg.setdefault(key, [0.0, 0, 0])
-        a[0] += durs[i]
-        a[1] += 1
-        a[2] += b
-    for (name, M), (ms, n, b) in agg.items():
-        us = ms * 1e3 / n
-        per_call.append({"proj": name, "M": M, "us_per_call": round(us, 3),
-                         w.unit.replace("/", "p"): round(_rate(w, b / n, us * 1e-6), 1)})
-    kernel_ms = sum(durs) / rot
+    kernel_ms = 0.0
+    if not moe:
+        pcs = sorted({(pi, M) for _, _, pi, M in calls}, key=lambda x: (w.Ms.index(x[1]), x[0]))
+        extra_w = {}
+        for pi in sorted({pi for pi, _ in pcs}):
+            p = w.projs[pi]
+            have = [sets[c][layer][pi] for c in range(copies) for layer in range(w.layers)]
+            b1 = _algo_bytes(w.fmt, p.N, p.K, 0)
+            need = int(np.ceil(2 * L2_BYTES / b1))
+            if w.kind != "prefill" and len(have) < need:
+                have = have + _extra_copies(w, pi, min(need - len(have), 256), dev)
+            extra_w[pi] = have
+        for pi, M in pcs:
+            p = w.projs[pi]
+            Ws = extra_w[pi]
+            reps = max(1, int(np.ceil(20 / len(Ws))))
+            seq = [Ws[i % len(Ws)] for i in range(len(Ws) * reps)]
+
+            def chain():
+                for Wt in seq:
+                    if greedy:
+                        vt.w4a16_gemm_greedy(A[(M, p.K)], Wt, workspace=ws, stream=stream)
+                    elif silu and p.fused:
+                        vt.w4a16_gemm_silu_mul(A[(M, p.K)], Wt, out=act[M], workspace=ws,
+                                               stream=stream)
+                    elif silu:
+                        vt.w4a16_gemm(act[M], Wt, out=C[(M, p.N)], workspace=ws, stream=stream)
+                    elif a4 is not None:
+                        vt.w4a4_gemm(A[(M, p.K)], Wt, a4, out=C[(M, p.N)], workspace=ws,
+                                     stream=stream)
+                    else:
+                        vt.w4a16_gemm(A[(M, p.K)], Wt, out=C[(M, p.N)], workspace=ws,
+                                      stream=stream)
+            with torch.cuda.stream(stream):
+                chain()
+            stream.synchronize()
+            gc_ = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(gc_, stream=stream):
+                    chain()
+                for _ in range(2):
+                    gc_.replay()
+            stream.synchronize()
+            tims = []
+            for _ in range(5):
+                with torch.cuda.stream(stream):
+                    t0.record(stream)
+                    gc_.replay()
+                    t1.record(stream)
+                stream.synchronize()
+                tims.append(t0.elapsed_time(t1))
+            us = statistics.median(tims) * 1e3 / len(seq)
+            b = _work(w, p.N, p.K, M)
+            kernel_ms += us * 1e-3
+            per_call.append({"proj": p.name, "M": M, "us_per_call": round(us, 3),
+                             w.unit.replace("/", "p"): round(_rate(w, b, us * 1e-6), 1),
+                             "chained_calls": len(seq), "distinct_weights": len(Ws)})
+            del gc_
+        del extra_w
+    else:
+        # the grouped call per M, chained over the copies (each copy: its own experts)
+        for M in w.Ms:
+            seq = [c for c in range(copies)] * max(1, int(np.ceil(20 / copies)))
+
+            def chain_moe():
+                for c in seq:
+                    vt.w4a16_gemm_moe(A[(M, w.projs[0].K)], sets[c][0][0], route[(c, M)],
+                                      out=Cm[M], workspace=ws, stream=stream)
+            with torch.cuda.stream(stream):
+                chain_moe()
+            stream.synchronize()
+            gm = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(gm, stream=stream):
+                    chain_moe()
+                for _ in range(2):
+                    gm.replay()
+            stream.synchronize()
+            tims = []
+            for _ in range(5):
+                with torch.cuda.stream(stream):
+                    t0.record(stream)
+                    gm.replay()
+                    t1.record(stream)
+                stream.synchronize()
+                tims.append(t0.elapsed_time(t1))
+            us = statistics.median(tims) * 1e3 / len(seq)
+            b = statistics.mean(moe_bytes[(c, M)] for c in range(copies))
+            kernel_ms += us * 1e-3
+            per_call.append({"proj": w.projs[0].name, "M": M, "us_per_call": round(us, 3),
+                             "GBps": round(_rate(w, b, us * 1e-6), 1),
+                             "chained_calls": len(seq), "distinct_weights": copies})
+            del gm
     unfused = None
     if greedy or silu:
         # the same step with the logits written and a separate argmax per call
@@ -637,7 +709,7 @@ def run_gpu(args, rank: int, world: int):
         "achieved": achieved, "kernel_ms": kernel_ms, "per_call": per_call, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "copies": copies,
         "calls_per_step": n_calls, "rotation": rot, "ws_status": ws_status, "unfused": unfused,
-        "self_check": check,
+        "self_check": check, "timing": timing,
     }
 
 
@@ -941,16 +1013,17 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="vtfp4", choices=["vtfp4", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=10,
+                    help="timed regions of K steps each; the median one is reported")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the chosen workload only (no per_config entries)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = WORKLOADS[args.workload]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    config = {"workload": w.name, "description": w.note,
-              "format": "nvfp4" if w.fmt == NVFP4 else "mxfp4", "Ms": w.Ms,
-              "shapes": [{"proj": p.name, "N": p.N, "K": p.K} for p in w.projs],
-              "layers": w.layers}
+    config = _config(w)
 
     if args.impl == "reference":
         if rank != 0:
@@ -981,6 +1054,33 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     r = run_gpu(args, rank, world)
+    line = _line(w, r, args, world, config) if rank == 0 else None
+    # Every other configuration of the workload definition, measured the same way in the
+    # same run (rank 0 prints them inside the one JSON line, under per_config).
+    per_config = []
+    if not args.no_per_config and args.workload == DEFAULT_WORKLOAD:
+        import torch
+        for wname in PER_CONFIG:
+            torch.cuda.empty_cache()
+            rc = run_gpu(args, rank, world, wname)
+            if rank == 0:
+                wc = WORKLOADS[wname]
+                entry = _line(wc, rc, args, world, _config(wc))
+                entry = {k: entry[k] for k in ("metric", "value", "unit", "ms_per_step", "timing",
+                                               "config", "roofline", "per_call", "e2e",
+                                               "gpu_launches", "clocks", "workspace_status",
+                                               "self_check") if k in entry}
+                if wc.wid == 1:
+                    entry["latency_bound"] = (
+                        "one 1.2 MB call per step: its time is set by the launch and the "
+                        "dependent-launch hop, not by HBM bandwidth; graded on parity and us/call")
+                if not args.no_cpu_baseline:
+                    g_, d_, t_, desc_ = run_oracle_sample(wc, target_s=3.0)
+                    entry["cpu_baseline"] = {"value": round(g_, 4), "unit": wc.unit, "cores": t_,
+                                             "kind": "oracle", "sample": desc_,
+                                             "seconds": round(d_, 2)}
+                per_config.append(entry)
+            del rc
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -988,6 +1088,42 @@ def main():
         if world > 1:
             dist.destroy_process_group()
         return
+    if per_config:
+        line["per_config"] = per_config
+    if not args.no_cpu_baseline:
+        gbps, dt, threads, desc = run_oracle_sample(w)
+        line["cpu_baseline"] = {"value": round(gbps, 4), "unit": w.unit, "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+        if w.wid in (1, 2) and w.extra.get("w4a4") is None:
+            # the oracle on one core too, for the single GEMM and the MLP decode
+            g1, d1, _, desc1 = run_oracle_sample(w, target_s=4.0, nthreads=1)
+            line["cpu_baseline"]["single_thread"] = {"value": round(g1, 4), "cores": 1,
+                                                     "sample": desc1, "seconds": round(d1, 2)}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    bad = [line] + per_config
+    if any(not x["self_check"].get("ok", True) or x["workspace_status"] for x in bad):
+        sys.stderr.write("bench: the timed outputs failed the self-check or the workspace "
+                         "reported an error; the numbers above are not valid\n")
+        sys.exit(3)
+
+
+# the configurations measured beside the headline (config 1, config 3 at both K, config 4,
+# config 5), each with its own value, roofline, e2e and self-check
+PER_CONFIG = ["nvfp4_gemm_2048x1024", "nvfp4_lm_head_248320x2560", "nvfp4_lm_head_248320x5120",
+              "nvfp4_layer_sweep_5120", "nvfp4_prefill_gate_up_34816x5120"]
+
+
+def _config(w: Workload) -> dict:
+    return {"workload": w.name, "description": w.note,
+            "format": "nvfp4" if w.fmt == NVFP4 else "mxfp4", "Ms": w.Ms,
+            "shapes": [{"proj": p.name, "N": p.N, "K": p.K} for p in w.projs],
+            "layers": w.layers}
+
+
+def _line(w: Workload, r: dict, args, world: int, config: dict) -> dict:
+    """The JSON line of one measured workload (everything but the CPU baseline)."""
     peak, peak_kind = _peak(w)
     traffic = _profiled_traffic(w, r["step_bytes"], r["calls_per_step"])
     prefill = w.kind == "prefill"
@@ -995,6 +1131,7 @@ def main():
         "metric": PREFILL_METRIC if prefill else METRIC, "value": round(r["value"], 2),
         "unit": w.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
+        "timing": r["timing"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16-mma-f32-acc", "data": "synthetic",
         "config": dict(config, parallelism=f"replicas{world}",
@@ -1016,6 +1153,9 @@ def main():
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
                      "traffic_detail": traffic},
         "per_call": r["per_call"],
+        "per_call_timing": ("each (projection, M): one CUDA graph of that call repeated back "
+                            "to back on distinct weight copies (over twice the L2), median of "
+                            "5 replays / calls"),
         "e2e": r["e2e"],
         "gpu_launches": r["gpu_launches"],
         "clocks": r["clocks"],
@@ -1024,22 +1164,7 @@ def main():
     }
     if r.get("unfused"):
         line["unfused"] = r["unfused"]
-    if not args.no_cpu_baseline:
-        gbps, dt, threads, desc = run_oracle_sample(w)
-        line["cpu_baseline"] = {"value": round(gbps, 4), "unit": w.unit, "cores": threads,
-                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
-        if w.wid in (1, 2) and w.extra.get("w4a4") is None:
-            # the oracle on one core too, for the single GEMM and the MLP decode
-            g1, d1, _, desc1 = run_oracle_sample(w, target_s=4.0, nthreads=1)
-            line["cpu_baseline"]["single_thread"] = {"value": round(g1, 4), "cores": 1,
-                                                     "sample": desc1, "seconds": round(d1, 2)}
-    print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
-    if not r["self_check"].get("ok", True) or r["ws_status"]:
-        sys.stderr.write("bench: the timed outputs failed the self-check or the workspace "
-                         "reported an error; the numbers above are not valid\n")
-        sys.exit(3)
+    return line
 
 
 if __name__ == "__main__":
