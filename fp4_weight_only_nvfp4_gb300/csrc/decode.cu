@@ -257,27 +257,20 @@ __device__ __forceinline__ void publish_release(unsigned int* ctr) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
-// Acquire-release add of n at GPU scope; returns the previous value (see arrive_acq_rel).
-__device__ __forceinline__ unsigned int arrive_acq_rel_n(unsigned int* ctr, unsigned int n) {
-  unsigned int prev;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(prev) : "l"(ctr), "r"(n) : "memory");
-  return prev;
-}
-
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* ctr) {
   unsigned int v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
   return v;
 }
 
-// Bounded wait until the low 16 bits of *ctr equal target (acquire).
-__device__ __forceinline__ bool wait_low16(const unsigned int* ctr, unsigned int target,
+// Bounded wait until *ctr == target (acquire); false once `limit_ns` of wall time passed.
+__device__ __forceinline__ bool wait_count(const unsigned int* ctr, unsigned int target,
                                            uint64_t limit_ns) {
-  if ((ld_acquire_gpu(ctr) & 0xFFFFu) == target) return true;
+  if (ld_acquire_gpu(ctr) == target) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     __nanosleep(100);
-    if ((ld_acquire_gpu(ctr) & 0xFFFFu) == target) return true;
+    if (ld_acquire_gpu(ctr) == target) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -392,7 +385,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   constexpr int SLOT = MT * kSlotPad;  // floats per warp reduction slot (32 rows + pad)
   constexpr int WBYTES = KS * TB;      // weight bytes of a full stage
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_flag, s_ncon, s_n1;
+  __shared__ int s_flag, s_ncon;
   __shared__ unsigned long long s_gkey[16];  // greedy head: this CTA's best key per token
   __shared__ int64_t s_clo;
   // The next kernel in the stream may launch now: it only waits (griddepcontrol.wait)
@@ -467,10 +460,9 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
 
   if (warp == CW + 1) {
     // ------------------------------------------------------------- publisher
-    // A CTA whose range starts inside a row tile and continues past it shares that tile
-    // with the CTA before it: publish this CTA's partial of it once the consumers have
-    // written it (a range that ends inside the tile arrives from the consumers instead).
-    if (lane == 0 && i0 < i1 && i0 % KT != 0 && i1 > (i0 / KT) * KT + KT) {
+    // A CTA whose range starts inside a row tile shares that tile with the CTA before it:
+    // publish this CTA's partial of it once the consumers have written it.
+    if (lane == 0 && i0 < i1 && i0 % KT != 0) {
       if (mbar_wait_bounded(pub_u, 0, p.wait_ns))
         publish_release(reinterpret_cast<unsigned int*>(&p.counters[i0 / KT]));
       else
@@ -815,7 +807,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
               acc[b][u][3] = fmaf(t1[3] * a2[1], fg81, acc[b][u][3]);
             }
           }
-        } else {
+          return;
+        }
         uint32_t bfr[NJ][4][2];
         float as[NJ][2];
 #pragma unroll
@@ -865,7 +858,6 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
             acc[b][u][3] = fmaf(tmp[u][3], as[u][1], acc[b][u][3]);
           }
         }
-        }
       };
       if (FMT == FMT_MX && (WIDE || ((GRP || MT == 16) && wide))) {
 #pragma unroll 1
@@ -889,23 +881,16 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     if (pos != i1 && kt != 0) continue;
 
     // ---- end of a row-tile segment: warp partials -> slots -> fixed-order sums.  The tile
-    // is complete when it lies inside this CTA's item range.  A shared tile's contributors
-    // are CTAs c_lo .. c_hi.  A segment that ends this CTA's range (c_lo's last segment, or
-    // the whole range of a CTA inside the tile) stores its partial and arrives with an
-    // acquire-release add of 2^16 on the tile's counter; the last of those arrivals sums every
-    // contributor's partial in contributor order, so whoever sums, the bits are the same.  A
-    // segment that does not end the range (the first segment of a CTA that continues into
-    // the next tile) stores its partial and its publisher warp adds 1 without waiting.
+    // is complete when it lies inside this CTA's item range; otherwise one thread finds the
+    // CTAs that share it (64-bit divisions, so once per CTA, not per thread).
     const bool complete = (rt * KT >= i0) && (rt * KT + KT <= i1);
-    const bool lead = !complete && rt * KT >= i0;      // tile starts in range: last segment
-    const bool ends = !complete && rt * KT + KT >= i1;  // this segment ends the CTA's range
-    const bool first_only = !complete && !ends;         // published by the publisher warp
-    if (ends && threadIdx.x == 0) {
-      const int64_t c_lo = owner_of(rt * KT, I, G), c_hi = owner_of(rt * KT + KT - 1, I, G);
-      s_clo = c_lo;
-      s_ncon = (int)(c_hi - c_lo + 1);
-      // the range of c_hi runs past the tile: it is the one contributor publishing early
-      s_n1 = ((c_hi + 1) * I / G > rt * KT + KT) ? 1 : 0;
+    // shared tile: this CTA reduces it when the tile starts inside its range (then it is
+    // this CTA's last segment), else it contributes its first segment's partial
+    const bool reducer = !complete && rt * KT >= i0;
+    if (reducer && threadIdx.x == 0) {
+      const int64_t c_hi = owner_of(rt * KT + KT - 1, I, G);
+      s_clo = c;
+      s_ncon = (int)(c_hi - c + 1);
     }
     float* my = slots + warp * SLOT;
 #pragma unroll
@@ -937,10 +922,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         if (i < p.seg_split)
           p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
       }
-    } else {
-      // partial slot of a contributor: [c][1] for c_lo's segment, [c][0] otherwise (a CTA
-      // holds at most one of each)
-      const size_t pslot = ((size_t)c * 2 + (lead ? 1 : 0)) * MT;
+    } else if (!reducer) {  // a reducer adds its slots when the other partials are in
       for (int idx = threadIdx.x; idx < nout; idx += CT) {
         const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
         float sum = 0.0f;
@@ -961,57 +943,46 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
             const float f = n < p.seg_split ? f0 : f1;
             p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
-        } else {
-          p.partials[(pslot + m) * 128 + row] = sum;
+        } else if (!reducer) {
+          p.partials[((size_t)c * 2 * MT + m) * 128 + row] = sum;
         }
       }
     }
-    if (first_only) {
-      // the partial of this CTA's first segment: the publisher warp announces it
+    if (!complete && !reducer) {
+      // this CTA's partial of a tile reduced by an earlier CTA: hand it to the publisher
       __syncwarp();
       if (lane == 0) mbar_arrive(pub_u);
     }
-    if (ends) {
-      consumer_sync(CT);  // every consumer's partial store precedes the arrival below
+    if (reducer) {
       if (threadIdx.x == 0) {
         unsigned int* ctr = reinterpret_cast<unsigned int*>(&p.counters[rt]);
-        const int n2 = s_ncon - s_n1;
-        const unsigned int prev = arrive_acq_rel_n(ctr, 1u << 16);
-        bool mine = (int)(prev >> 16) == n2 - 1;  // the last of the range-ending segments
-        if (mine) {
-          // the early publication (if any) has almost always arrived by now
-          const bool got = wait_low16(ctr, (unsigned int)s_n1, p.wait_ns);
-          if (got) *ctr = 0;  // every contributor has arrived: reset for the next call
-          else atomicExch(p.status, 5);
-          mine = got;
-        }
-        s_flag = mine;
+        const bool got = wait_count(ctr, (unsigned int)(s_ncon - 1), p.wait_ns);
+        if (got) *ctr = 0;  // every contributor has arrived: reset for the next call
+        else atomicExch(p.status, 5);
+        s_flag = got;
       }
       consumer_sync(CT);
       if (s_flag) {
-        // every contributor's partial in contributor order (this CTA's own from its slots,
-        // bit-identical to the copy it stored), loaded in batches of 8
+        // this CTA's own partial (its slots, in fixed order) first, then the later
+        // contributors' partials in contributor order, loaded in batches of 8
         const int64_t c_lo = s_clo;
         const int ncon = s_ncon;
         auto tile_sum = [&](int m, int row) -> float {
           const int pr = row >> 5, rr = row & 31;
-          float own = 0.0f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) own += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
-          const size_t off = (size_t)m * 128 + row;
           float sum = 0.0f;
-          for (int b0 = 0; b0 < ncon; b0 += 8) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
+          const size_t off = (size_t)m * 128 + row;
+          for (int b0 = 1; b0 < ncon; b0 += 8) {
             float v[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const int64_t cc = c_lo + b0 + q;
-              v[q] = (b0 + q < ncon && cc != c)
-                         ? __ldcg(&p.partials[((size_t)cc * 2 + (cc == c_lo ? 1 : 0)) * MT * 128 + off])
-                         : own;
+              v[q] = (b0 + q < ncon) ? __ldcg(&p.partials[(size_t)cc * 2 * MT * 128 + off]) : 0.0f;
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              if (b0 + q < ncon) sum = (b0 + q == 0) ? v[q] : sum + v[q];
+              if (b0 + q < ncon) sum += v[q];
           }
           return sum;
         };
