@@ -38,19 +38,25 @@ namespace {
 constexpr uint64_t kPfWaitNs = 2000000000ull;  // drains of copies and MMAs in flight
 constexpr int kBM = 128;          // tokens per tile (MMA M)
 constexpr int kBN = 256;          // weight rows per tile (MMA N): two packed row tiles
-constexpr int kAStages = 6;
-constexpr int kPStages = 4;
+// A tile is 256 weight rows x 2 token tiles of 128: one dequantised B tile serves two MMAs
+// per k step (the B-tile work and shared-memory traffic per flop are halved); the two
+// accumulators then fill the 512 TMEM columns, so the epilogue of a tile does not overlap
+// the next tile's MMAs.
+constexpr int kPair = 2;
+constexpr int kAStages = 4;       // activation stages, each the pair of 128 x 64 tiles
+constexpr int kPStages = 3;
 constexpr int kBStages = 2;
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kPfThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
 constexpr int kABytes = kBM * kTileK * 2;                     // 16 KB
+constexpr int kAStageBytes = kPair * kABytes;                 // 32 KB
 constexpr int kBBytes = kBN * kTileK * 2;                     // 32 KB
 constexpr uint32_t kTmemCols = 512;                           // 2 x 256 fp32 columns
 
 // Shared-memory map (from a 1024-byte aligned base).
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kAStages * kABytes;
+constexpr int kOffB = kOffA + kAStages * kAStageBytes;
 constexpr int kOffP = kOffB + kBStages * kBBytes;
 __host__ __device__ constexpr int off_bar(int fmt) { return kOffP + kPStages * 2 * tile_bytes(fmt); }
 constexpr int kNumBars = 2 * kAStages + 2 * kPStages + 2 * kBStages + 4 + 1;
@@ -162,7 +168,7 @@ struct PrefillParams {
   const uint8_t* tiles;
   const PackedHeader* hdr;
   int64_t N, RT, KT, M, ldc, seg_split;
-  int64_t mtiles, tiles_total;
+  int64_t mtiles, mptiles, tiles_total;  // token tiles, token-tile pairs, (pair, 256 rows) tiles
   const float* rowscale;
   __nv_bfloat16* C;
   int* status;
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int64_t KT = p.KT, RT = p.RT, mtiles = p.mtiles, T = p.tiles_total;
+  const int64_t KT = p.KT, RT = p.RT, mtiles = p.mtiles, mptiles = p.mptiles, T = p.tiles_total;
   const int64_t G = gridDim.x;
 
   if (warp == 0) {
@@ -237,14 +243,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int a_issued = 0, p_issued = 0;  // copies issued (for the drain after a timeout)
       bool ok = true;
       for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
-        const int64_t nt = tile / mtiles, mt = tile % mtiles;
+        const int64_t nt = tile / mptiles, mt0 = 2 * (tile % mptiles);
+        const bool two = mt0 + 1 < mtiles;
         const int64_t rt0 = 2 * nt;
         const int nrt = (RT - rt0) >= 2 ? 2 : 1;
         for (int64_t kt = 0; kt < KT; ++kt) {
           if (!(ok = pf_wait(a_empty + 8 * ia, pa ^ 1u, abort, p.wait_ns))) break;
-          mbar_expect_tx(a_full + 8 * ia, kABytes);
-          tma_load_2d(sA + ia * kABytes, &tmA, (int)(kt * kTileK), (int)(mt * kBM), a_full + 8 * ia,
-                      pol_a);
+          mbar_expect_tx(a_full + 8 * ia, two ? 2 * kABytes : kABytes);
+          tma_load_2d(sA + ia * kAStageBytes, &tmA, (int)(kt * kTileK), (int)(mt0 * kBM),
+                      a_full + 8 * ia, pol_a);
+          if (two)
+            tma_load_2d(sA + ia * kAStageBytes + kABytes, &tmA, (int)(kt * kTileK),
+                        (int)((mt0 + 1) * kBM), a_full + 8 * ia, pol_a);
           ++a_issued;
           if (++ia == kAStages) { ia = 0; pa ^= 1u; }
           if (!(ok = pf_wait(p_empty + 8 * ip, pp ^ 1u, abort, p.wait_ns))) break;
@@ -278,29 +288,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = (FMT == FMT_MX && p.hdr->wide) ? kIdescBF16 : kIdesc;
-      uint32_t ia = 0, pa = 0, ib = 0, pb = 0, ab = 0, pab = 0;
+      uint32_t ia = 0, pa = 0, ib = 0, pb = 0, pab = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
-        if (!(ok = pf_wait(acc_empty + 8 * ab, pab ^ 1u, abort, p.wait_ns))) break;
+        const bool two = 2 * (tile % mptiles) + 1 < mtiles;
+        // both accumulators are free once the epilogue has read the previous tile's
+        if (!(ok = pf_wait(acc_empty, pab ^ 1u, abort, p.wait_ns))) break;
         tc_fence_after();
-        const uint32_t d = tmem + ab * kBN;
         for (int64_t kt = 0; kt < KT; ++kt) {
           if (!(ok = pf_wait(a_full + 8 * ia, pa, abort, p.wait_ns))) break;
           if (!(ok = pf_wait(b_full + 8 * ib, pb, abort, p.wait_ns))) break;
           tc_fence_after();
-          const uint64_t ad = desc_sw128(sA + ia * kABytes);
+          const uint64_t ad0 = desc_sw128(sA + ia * kAStageBytes);
+          const uint64_t ad1 = desc_sw128(sA + ia * kAStageBytes + kABytes);
           const uint64_t bd = desc_sw128(sB + ib * kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk)  // +32 bytes per 16-element k step
-            mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTileK / 16; ++kk) {  // +32 bytes per 16-element k step
+            const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+            mma_f16(tmem, ad0 + 2 * kk, bd + 2 * kk, idesc, acc);
+            if (two) mma_f16(tmem + kBN, ad1 + 2 * kk, bd + 2 * kk, idesc, acc);
+          }
           mma_commit(a_empty + 8 * ia);
           mma_commit(b_empty + 8 * ib);
           if (++ia == kAStages) { ia = 0; pa ^= 1u; }
           if (++ib == kBStages) { ib = 0; pb ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(acc_full + 8 * ab);
-        if (++ab == 2) { ab = 0; pab ^= 1u; }
+        mma_commit(acc_full);
+        pab ^= 1u;
       }
       if (!ok) atomicExch(p.status, 5);
       // every MMA issued has completed once this commit arrives
@@ -319,7 +334,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint32_t ip = 0, pp = 0, ib = 0, pb = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
-      const int64_t nt = tile / mtiles;
+      const int64_t nt = tile / mptiles;
       const int nrt = (RT - 2 * nt) >= 2 ? 2 : 1;
       for (int64_t kt = 0; kt < KT; ++kt) {
         if (!(ok = pf_wait(p_full + 8 * ip, pp, abort, p.wait_ns))) break;
@@ -417,12 +432,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3;  // TMEM lane quarter this warp may access
     const float f0 = p.hdr->factor[0], f1 = p.hdr->factor[1];
-    uint32_t ab = 0, pab = 0;
+    uint32_t pab = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; ok && tile < T; tile += G) {
-      const int64_t nt = tile / mtiles, mt = tile % mtiles;
-      if (!(ok = pf_wait(acc_full + 8 * ab, pab, abort, p.wait_ns))) break;
+      const int64_t nt = tile / mptiles, mp = tile % mptiles;
+      if (!(ok = pf_wait(acc_full, pab, abort, p.wait_ns))) break;
       tc_fence_after();
+      for (int h = 0; h < kPair; ++h) {  // the tile's two token tiles, accumulator h
+      const int64_t mt = 2 * mp + h;
+      if (mt >= mtiles) break;  // warp-uniform
+      const uint32_t ab = (uint32_t)h;
       const int64_t m = mt * kBM + qd * 32 + lane;
       const bool live = m < p.M;
       const float rs = live ? p.rowscale[m] : 0.0f;
@@ -511,10 +530,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + 8 * ab);
-      if (++ab == 2) { ab = 0; pab ^= 1u; }
+      if (lane == 0) mbar_arrive(acc_empty);
+      pab ^= 1u;
     }
     if (!ok && lane == 0) atomicExch(p.status, 5);
   }
@@ -731,8 +751,9 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   pp.ldc = L.ldc;
   pp.seg_split = L.seg_split;
   pp.mtiles = (L.M + kBM - 1) / kBM;
+  pp.mptiles = (pp.mtiles + kPair - 1) / kPair;
   const int64_t ntiles = (L.RT + 1) / 2;
-  pp.tiles_total = pp.mtiles * ntiles;
+  pp.tiles_total = pp.mptiles * ntiles;
   pp.rowscale = L.rowscale;
   pp.C = reinterpret_cast<__nv_bfloat16*>(L.C);
   pp.status = L.status;
