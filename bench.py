@@ -431,6 +431,13 @@ def run_gpu(args, rank: int, world: int, wname: str | None = None):
         for c, layer, pi, M in calls:
             ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(M)])
             route[(c, M)] = torch.from_numpy(ids.astype(np.int32)).to(dev)
+        # the per-call chains run every M on every copy: routes for the pairs the step does
+        # not use, drawn after the step's own
+        for c in range(copies):
+            for M in w.Ms:
+                if (c, M) not in route:
+                    ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(M)])
+                    route[(c, M)] = torch.from_numpy(ids.astype(np.int32)).to(dev)
         ebytes = _algo_bytes(w.fmt, w.projs[0].N, w.projs[0].K, 0)
         moe_bytes = {k: len(np.unique(v.cpu().numpy())) * ebytes + 2 * k[1] * w.projs[0].K
                      for k, v in route.items()}
