@@ -506,8 +506,14 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   // token tile of the decode kernel: 8 rows when M <= 8 (an expert then has at most M pairs
   // unless a token names it twice; such extra pairs are left out), else 16
   const int mrows = decode_mt((int)M);
-  int stages = 6;  // the grouped kernel also holds ~3 KB of static shared memory (the grouping)
-  while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages) > 223 * 1024) --stages;
+  // up to 8 tokens whose converted activations fit kGroupedResidentMaxBytes: the decode
+  // kernel groups the routing and converts the activations itself (one kernel, no pre-pass)
+  const bool resident = mrows == 8 && decode_resident_bytes(mrows, W->KT) <= kGroupedResidentMaxBytes;
+  const int64_t rkt = resident ? W->KT : 0;
+  int stages = 6;  // the grouped kernel also holds ~3.5 KB of static shared memory (the grouping)
+  while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages, rkt) > 222 * 1024) --stages;
+  if (decode_smem_bytes(W->fmt, mrows, ks, stages, rkt) > 222 * 1024)
+    return fail(VT_ERR_UNSUPPORTED, "K too large for the grouped kernel's shared memory");
   const int64_t pmax = npairs < W->E ? npairs : W->E;
   const int64_t items = pmax * W->RT * W->KT;  // an upper bound: the pre-pass finds P
   int64_t grid = sm_count();
@@ -539,6 +545,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   D.withhold = 0;
   D.gtab = reinterpret_cast<const int*>(ws + L.table);
   D.expert_bytes = W->expert_bytes ? W->expert_bytes : (int64_t)W->packed_bytes;
+  D.resident = resident ? 1 : 0;
   int launches = 0;
   cudaError_t e = launch_decode_grouped(D, topk_ids, npairs, (int)topk, (int)W->E,
                                         (cudaStream_t)s, &launches);

@@ -53,6 +53,10 @@ constexpr int kResidentPrefetch = VT_RESIDENT_PREFETCH;  // resident mode: stage
 #define VT_GROUPED_PREFETCH 2
 #endif
 constexpr int kGroupedPrefetch = VT_GROUPED_PREFETCH;  // grouped mode: stages before the pre-pass ends
+#ifndef VT_GROUPED_RESIDENT_PREFETCH
+#define VT_GROUPED_RESIDENT_PREFETCH 2
+#endif
+constexpr int kGroupedResidentPrefetch = VT_GROUPED_RESIDENT_PREFETCH;  // grouped resident mode
 
 int decode_mt(int M) { return M <= 8 ? 8 : 16; }
 
@@ -198,6 +202,7 @@ struct DecodeParams {
   int64_t expert_bytes, RT;    // bytes per expert; 128-row tiles per expert
   const int32_t* topk_ids;     // grouped mode: the routing, grouped again by the kernel itself
   int npairs, E;
+  int Mtok, topk;              // grouped resident mode: tokens of A, slots per token
 };
 
 // SiLU(x) = x / (1 + e^-x) in fp32 (e^-x overflowing to infinity gives -0 for large -x).
@@ -400,17 +405,27 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   __shared__ int s_rwarp[4], s_rP;
   __shared__ int s_rexp[GRP ? kGtMaxProblems : 1], s_rcnt[GRP ? kGtMaxProblems : 1];
   __shared__ int s_rrsum[GRP ? kGtMaxProblems : 1];
+  __shared__ int s_rfirst[GRP ? kGtMaxProblems : 1];  // a problem's first sorted position
   if constexpr (GRP) {
     if (threadIdx.x < kGroupThreads) {
+      // Without a pre-pass (grouped resident mode) nothing has waited for the kernel that
+      // may have written topk_ids: wait here, before reading them.
+      if constexpr (RA) pdl_wait();
       const int tid = threadIdx.x;
       const uint32_t key = tid < p.npairs ? pair_key(__ldcg(p.topk_ids + tid), tid, p.E) : 0xFFFFFFFFu;
       const PairPlace q = group_pairs<2>(key, MT, s_rin, s_rkey, s_rwarp);
       if (q.kept && q.head) {
         s_rexp[q.prob] = q.e;
         s_rrsum[q.prob] = q.rsum;
+        s_rfirst[q.prob] = tid;
       }
       if (q.last) s_rcnt[q.prob] = q.slot + 1;
       if (tid == kGroupThreads - 1) s_rP = q.prob + 1;
+      // the pre-pass's report, made here when there is none: an id outside [0, E), or a pair
+      // beyond its expert's token tile, was skipped (status 6)
+      if (RA && blockIdx.x == 0 &&
+          ((tid < p.npairs && key == 0xFFFFFFFFu) || (q.valid && !q.kept)))
+        atomicExch(p.status, 6);
     }
     __syncthreads();
   }
@@ -471,7 +486,51 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     return;
   }
 
-  if constexpr (GRP) {
+  if constexpr (GRP && RA) {
+    if (warp == CW) {
+      // ------------------------------------------------ producer (grouped, resident)
+      // weights only (the consumers convert the activations themselves): the first stages
+      // at once, the rest once the activations are in shared memory
+      if (lane == 0 && !p.withhold) {
+        const uint64_t pol = l2_evict_first_policy();
+        int64_t pos = i0, rtl = 0;
+        int kt = kt_first, issued = 0, slot = 0;
+        int prob = (int)((i0 / KT) / p.RT), e = 0;
+        rtl = i0 / KT - (int64_t)prob * p.RT;
+        if (pos < i1) e = s_rexp[prob];
+        while (pos < i1) {
+          if (issued == kGroupedResidentPrefetch && !mbar_wait_bounded(aready_u, 0, p.wait_ns)) {
+            atomicExch(p.status, 5);
+            break;
+          }
+          if (issued >= S &&
+              !mbar_wait_bounded(empty_u + 8 * slot, (uint32_t)((issued / S - 1) & 1), p.wait_ns)) {
+            atomicExch(p.status, 5);
+            break;
+          }
+          const int n = stage_len(pos, kt);
+          mbar_expect_tx(full_u + 8 * slot, (uint32_t)(n * TB));
+          bulk_g2s(ring_u + slot * STAGE,
+                   p.gbase + e * p.expert_bytes + kHeaderBytes + (rtl * KT + kt) * TB,
+                   (uint32_t)(n * TB), full_u + 8 * slot, pol);
+          pos += n;
+          kt += n;
+          if (kt == KTi) {
+            kt = 0;
+            if (++rtl == p.RT && pos < i1) {
+              rtl = 0;
+              e = s_rexp[++prob];
+            }
+          }
+          ++issued;
+          if (++slot == S) slot = 0;
+        }
+      }
+      return;
+    }
+  }
+
+  if constexpr (GRP && !RA) {
     if (warp == CW) {
       // --------------------------------------------------------- producer (grouped)
       // virtual row tile rt = problem * RT + rt_l; the weights of expert e = expert[problem].
@@ -658,18 +717,22 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     // k tile kt) from the tile's largest magnitude, scales[kt][m] = 2^p; 16-byte granules
     // XOR-swizzled by (m & 7).  Eight consecutive threads hold one (m, kt) tile row; the
     // loop runs the same number of times in every warp (the shuffles need all lanes).
-    const int64_t total = (int64_t)M * KT * 8;
+    // Grouped: only the call's tokens are converted; a slot reads its token's row, so the
+    // tile's rows past the tokens are never read.
+    const int Mrows = GRP ? p.Mtok : M;
+    const int64_t total = (int64_t)Mrows * KT * 8;
     const __nv_bfloat16* A = p.A;
     for (int64_t base = 0; base < total; base += CT) {
       const int64_t idx = base + threadIdx.x;
       const bool valid = idx < total;
       const int gi = (int)(idx & 7);
       const int64_t r = idx >> 3;
-      const int64_t ktr = r / M;
-      const int m = (int)(r - ktr * M);
+      const int64_t ktr = r / Mrows;
+      const int m = (int)(r - ktr * Mrows);
       const int64_t k0 = ktr * 64 + gi * 8;
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (valid && k0 < p.K) v = __ldg(reinterpret_cast<const uint4*>(A + m * p.lda + k0));
+      if (valid && k0 < p.K)
+        v = __ldg(reinterpret_cast<const uint4*>(A + m * p.lda + k0));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       int mx = act_maxmag8(w);
 #pragma unroll
@@ -695,6 +758,14 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   // grouped mode: the current problem's token count, output rows and expert factor
   int Mc = M, gprob = -1;
   const int* grow = nullptr;
+  // grouped resident mode: the problem's first sorted position; this lane's token rows
+  int gfirst = 0, tok_g = 0, tok_a0 = 0, tok_a1 = 0;
+  // the output row of slot m: the token itself, or (grouped) its (token, slot) pair
+  auto out_row = [&](int m) -> int64_t {
+    if constexpr (!GRP) return m;
+    else if constexpr (RA) return (int64_t)(s_rkey[gfirst + m] & 0xFFu);
+    else return (int64_t)grow[m];
+  };
   const int soff = scale_offset(FMT, 2 * jp, g, t);
   float acc[2][NJ][4];
 #pragma unroll
@@ -723,7 +794,16 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       if (pr != gprob) {
         gprob = pr;
         Mc = s_rcnt[pr];
-        grow = p.gtab + kGtPair + pr * 16;  // written by the pre-pass (complete: waited above)
+        if constexpr (RA) {
+          // slot m of the problem is sorted position gfirst + m; its token is pair / topk
+          gfirst = s_rfirst[pr];
+          auto tok = [&](int m) { return m < Mc ? (int)((s_rkey[gfirst + m] & 0xFFu) / p.topk) : 0; };
+          tok_g = tok(g);
+          tok_a0 = tok(2 * t);
+          tok_a1 = tok(2 * t + 1);
+        } else {
+          grow = p.gtab + kGtPair + pr * 16;  // written by the pre-pass (complete: waited above)
+        }
         const PackedHeader* he = reinterpret_cast<const PackedHeader*>(
             p.gbase + (int64_t)s_rexp[pr] * p.expert_bytes);
         f0 = f1 = he->factor[0];
@@ -745,9 +825,10 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         auto load_b = [&](int u, uint32_t (&bf)[4][2]) {
           const int m = g + 8 * u;
           if (m < Mc) {
-            const uint32_t rowa = ab + m * 128;
-            const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (m & 7)) << 4));
-            const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (m & 7)) << 4));
+            const int r = (GRP && RA) ? tok_g : m;  // grouped resident: the slot's token row
+            const uint32_t rowa = ab + r * 128;
+            const int4 v0 = ld_shared_v4(rowa + (((2 * t) ^ (r & 7)) << 4));
+            const int4 v1 = ld_shared_v4(rowa + (((2 * t + 1) ^ (r & 7)) << 4));
             bf[0][0] = v0.x; bf[0][1] = v0.y;
             bf[1][0] = v0.z; bf[1][1] = v0.w;
             bf[2][0] = v1.x; bf[2][1] = v1.y;
@@ -759,10 +840,16 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         };
         // activation scales of this k tile for the tokens of this lane's accumulators
         auto load_as = [&](int u, float (&a)[2]) {
-          const uint32_t sa =
-              RA ? rscale_u + (uint32_t)(((kt + kh) * kResScaleStride + 2 * t + 8 * u) * 4)
-                 : sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
-          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[0]), "=f"(a[1]) : "r"(sa));
+          if constexpr (GRP && RA) {  // the tokens of slots 2t and 2t + 1 (8-token tile)
+            const uint32_t sr = rscale_u + (uint32_t)((kt + kh) * kResScaleStride * 4);
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a[0]) : "r"(sr + tok_a0 * 4));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a[1]) : "r"(sr + tok_a1 * 4));
+          } else {
+            const uint32_t sa =
+                RA ? rscale_u + (uint32_t)(((kt + kh) * kResScaleStride + 2 * t + 8 * u) * 4)
+                   : sbase + SCALES_OFF + kh * kAScaleStride * 4 + (2 * t + 8 * u) * 4;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[0]), "=f"(a[1]) : "r"(sa));
+          }
         };
         if constexpr (W) {
           // Exact MXFP4 over the whole E8M0 range: lane t's k lie in group t >> 1 of the
@@ -934,7 +1021,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
                                    : rt * kTileRows + row;
           const int64_t n = packed_to_row(p.layout, prow, p.N, p.seg_split);
-          const int64_t crow = GRP ? (int64_t)grow[m] : (int64_t)m;
+          const int64_t crow = out_row(m);
           if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
             unsigned long long key = 0;
             if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
@@ -1001,7 +1088,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
                                    : rt * kTileRows + row;
           const int64_t n = packed_to_row(p.layout, prow, p.N, p.seg_split);
-          const int64_t crow = GRP ? (int64_t)grow[m] : (int64_t)m;
+          const int64_t crow = out_row(m);
           if (p.g_idx) {
             unsigned long long key = 0;
             if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
@@ -1099,6 +1186,8 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   p.topk_ids = L.topk_ids;
   p.npairs = L.npairs;
   p.E = L.E;
+  p.Mtok = L.Mtok;
+  p.topk = L.topk;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)L.grid);
@@ -1206,7 +1295,18 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L0, const int32_t* topk_id
   L.topk_ids = topk_ids;
   L.npairs = npairs;
   L.E = E;
+  L.topk = topk;
+  L.Mtok = npairs / topk;
   cudaError_t e = cudaSuccess;
+  if (L.resident) {  // one kernel: it groups the routing and converts the activations itself
+    if (decode_mt(L.M) != 8) return cudaErrorInvalidValue;
+    e = (L.ks == 4) ? ((L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 4, true, true>(L, s)
+                                         : launch_t<FMT_MX, 8, 4, true, true>(L, s))
+                    : ((L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 8, true, true>(L, s)
+                                         : launch_t<FMT_MX, 8, 8, true, true>(L, s));
+    if (launches) *launches = 1;
+    return e;
+  }
   {
     const int pmax = npairs < E ? npairs : E;
     cudaLaunchConfig_t cfg = {};

@@ -52,7 +52,9 @@ struct DecodeLaunch {
   // NVFP4 activation global)
   int w4a4 = 0;
   float alpha = 1.0f;
-  int resident = 0;  // resident-activation mode (decode_resident_ok; not with w4a4 / grouped)
+  int resident = 0;  // resident-activation mode (decode_resident_ok; not with w4a4); grouped:
+                    // the decode kernel groups the routing and converts A itself, no pre-pass
+  int Mtok = 0, topk = 0;  // grouped resident mode: tokens of A, slots per token
 };
 int decode_mt(int M);  // 8 or 16
 // Resident-activation decode (small M * K): the decode kernel converts A into shared memory
@@ -72,6 +74,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches);
 cudaError_t launch_decode_grouped(const DecodeLaunch& L, const int32_t* topk_ids, int npairs,
                                   int topk, int E, cudaStream_t s, int* launches);
 constexpr int kGroupTableInts = 1 + 3 * 128 + 128 * 16;  // see the decode kernel
+// Grouped resident mode (M <= 8 tokens): the largest converted activation matrix a CTA keeps.
+constexpr size_t kGroupedResidentMaxBytes = 64 * 1024;
 size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt = 0);
 
 // Prefill tile GEMM (tensor cores), any M.

@@ -127,3 +127,27 @@ def test_moe_pairs_beyond_an_experts_token_tile_are_skipped():
     assert np.all(got[8:] == 5.0)
     ref = _oracle(fmt, Ab, srcs, ids, N)
     check_rows(got[:8], ref[:8], what="pairs within the token tile")
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+def test_moe_both_grouped_modes_match_oracle(fmt):
+    """Up to 8 tokens with K = 2048 (a 33 KB converted activation tile): the decode kernel
+    groups the routing and converts the activations itself, one launch.  K = 8192 (129 KB)
+    takes the pre-pass, two launches.  Token counts 1, 3 and 8, a token naming one expert
+    twice, and every row against the oracle."""
+    E, N = 6, 384
+    for K, launches in ((2048, 1), (8192, 2)):
+        srcs, W = _experts(fmt, E, N, K, 20 + fmt + K // 1024)
+        ws = W.moe_workspace(8, 4)
+        for M, topk in ((1, 4), (3, 2), (8, 4)):
+            ids = _routing(M, topk, E, seed=M * 7 + K, distinct=(M != 3))
+            if M == 3:
+                ids[1] = [5, 5]
+            Ab = make_acts(synth.tensor_id(89, 20 + fmt, K, M), M, K)
+            y = vt.w4a16_gemm_moe(bf16_dev(Ab), W, to_dev(ids), workspace=ws)
+            torch.cuda.synchronize()
+            st = W.stats()
+            assert st["m_tile"] == 8 and st["launches"] == launches, (K, M, st)
+            check_rows(y.float().cpu().numpy(), _oracle(fmt, Ab, srcs, ids, N),
+                       what=f"moe fmt={fmt} K={K} M={M}")
+        assert vt.workspace_status(ws) == 0
