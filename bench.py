@@ -1151,7 +1151,7 @@ def _line(w: Workload, r: dict, args, world: int, config: dict) -> dict:
                        calls_per_step=r["calls_per_step"]),
         "roofline": {"bound": "tensor" if prefill else "hbm",
                      "kernel": ("k_prefill (+ k_prep_rows, one GEMM call)" if prefill else
-                                "k_decode, grouped (+ k_group_prep; one MoE call)"
+                                "k_decode, grouped (one MoE call; + k_group_prep above 8 tokens)"
                                 if w.kind == "moe" else
                                 "k_decode (+ k_prep_a where a pre-pass converts the "
                                 "activations; one GEMM call)"),
