@@ -744,9 +744,12 @@ class _Slots:
         if self.nbytes:
             self.dev[:self.nbytes].copy_(self.host[:self.nbytes], non_blocking=True)
 
-    def to_host(self):
-        if self.nbytes:
-            self.host[:self.nbytes].copy_(self.dev[:self.nbytes], non_blocking=True)
+    def to_host(self, lo=0, hi=None):
+        """Slots lo .. hi - 1 (default: all) back to the host, one copy."""
+        a = self.off[lo] if lo < len(self.off) else self.nbytes
+        b = self.nbytes if hi is None or hi >= len(self.off) else self.off[hi]
+        if b > a:
+            self.host[a:b].copy_(self.dev[a:b], non_blocking=True)
 
 
 def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h, copies=2):
@@ -805,11 +808,13 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
     # overlapped).
     # A decode step without rotation keeps two sets of input slots: while a step computes on
     # one, its input copy for the next step fills the other, the way a serving loop stages the
-    # next batch (still one host-to-device copy per timed step).
+    # next batch (still one host-to-device copy per timed step).  A decode step's results go
+    # back in two copies on a side stream: the outputs of all calls but the last while the
+    # last call runs, then the last call's output.
     piped = w.kind == "prefill"
     double = not piped and len(steps_calls) == 1
     side_in = torch.cuda.Stream(device=dev) if (piped or double) else None
-    side_out = torch.cuda.Stream(device=dev) if piped else None
+    side_out = torch.cuda.Stream(device=dev)
 
     def make_step(calls):
         # MLP chain: the host input feeds gate_up, down's output goes back; act stays on device
@@ -869,15 +874,23 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
                     with torch.cuda.stream(side_out):
                         OUT.view(i, (M, p.N), torch.bfloat16, host=True).copy_(
                             OUT.view(i, (M, p.N), torch.bfloat16), non_blocking=True)
+                elif not piped and i == len(calls) - 2:
+                    side_out.wait_stream(stream)
+                    with torch.cuda.stream(side_out):
+                        OUT.to_host(0, i + 1)
             if piped:
                 stream.wait_stream(side_in)
                 stream.wait_stream(side_out)
             else:
-                OUT.to_host()
+                side_out.wait_stream(stream)
+                with torch.cuda.stream(side_out):
+                    OUT.to_host(len(calls) - 1)
+                stream.wait_stream(side_out)
                 if double:
                     stream.wait_stream(side_in)
         issues = [issue] if not double else [lambda: issue(0), lambda: issue(1)]
-        return issues, INS[0].nbytes, OUT.nbytes, (sum(host_in) + sum(host_out)) if piped else 2
+        copies = (sum(host_in) + sum(host_out)) if piped else (3 if len(calls) > 1 else 2)
+        return issues, INS[0].nbytes, OUT.nbytes, copies
 
     steps = [make_step(sc) for sc in steps_calls]
     return _time_e2e(args, w, [f for st in steps for f in st[0]], stream, dev, step_bytes, world,
