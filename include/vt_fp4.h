@@ -218,10 +218,12 @@ vt_status vt_fp4_moe_workspace_bytes(vt_fp4_handle W, int64_t M_max, int64_t top
 
 /* Mixture-of-experts decode GEMM (M <= 16): for every token m and slot j,
  *   C[m * topk + j][n] = sum_k A[m][k] * W_e[n][k],  e = topk_ids[m * topk + j],
- * in one call.  A pre-pass on the stream groups the (m, j) pairs by expert (each expert in
- * use is streamed once, however many tokens chose it), in increasing expert order with
- * pairs in increasing order, so results do not depend on the routing's order; then one
- * decode kernel runs every expert's problem.
+ * in one call.  The (m, j) pairs are grouped by expert on the device (each expert in use is
+ * streamed once, however many tokens chose it), in increasing expert order with pairs in
+ * increasing order, so results do not depend on the routing's order; one decode kernel runs
+ * every expert's problem.  Up to 8 tokens whose converted activations fit 64 KB (8 rows x K
+ * f16 plus their scales: K <= 3968) take one launch, the decode kernel grouping the pairs
+ * and converting A itself; otherwise a pre-pass on the stream does both first.
  *   topk_ids (device) int32 [M][topk], 1 <= topk <= 8; C (device) bf16 [M*topk][ldc].
  * A pair whose expert id is outside [0, E) is skipped (its C row is not written) and the
  * workspace status word reads 6.  Each token's ids should be distinct: an expert serves at
