@@ -331,15 +331,17 @@ struct PairPlace {
   bool valid, kept, head, last;
 };
 
+// Threads at positions >= n hold the invalid key: only the first n keys need comparing (an
+// invalid key at position j >= n sorts after every key before it and before the others).
 template <int BAR>
-__device__ __forceinline__ PairPlace group_pairs(uint32_t key, int cap, uint32_t* s_in,
+__device__ __forceinline__ PairPlace group_pairs(uint32_t key, int n, int cap, uint32_t* s_in,
                                                  uint32_t* s_key, int* s_warp) {
   const int tid = threadIdx.x;
   s_in[tid] = key;
   group_sync<BAR>();
-  int rank = 0;  // smaller keys, ties (the invalid ones) broken by position
-#pragma unroll 8
-  for (int j = 0; j < kGroupThreads; ++j) {
+  int rank = tid < n ? 0 : tid - n;  // smaller keys, ties (the invalid ones) broken by position
+#pragma unroll 4
+  for (int j = 0; j < n; ++j) {
     const uint32_t x = s_in[j];
     rank += (x < key) | ((x == key) & (j < tid));
   }
@@ -354,8 +356,10 @@ __device__ __forceinline__ PairPlace group_pairs(uint32_t key, int cap, uint32_t
   const int first = group_scan<BAR, true>(q.head ? tid : 0, s_warp);
   q.slot = tid - first;
   q.kept = q.valid && q.slot < cap;
-  q.prob = group_scan<BAR, false>(q.head ? 1 : 0, s_warp) - 1;
-  q.rsum = group_scan<BAR, false>(q.kept ? 1 : 0, s_warp) - 1;  // kept pairs before this one
+  // problems so far (low half) and kept pairs so far (high half) in one scan
+  const int cnt = group_scan<BAR, false>((q.head ? 1 : 0) | (q.kept ? 1 << 16 : 0), s_warp);
+  q.prob = (cnt & 0xFFFF) - 1;
+  q.rsum = (cnt >> 16) - 1;  // kept pairs before this one
   q.last = q.kept && (tid + 1 == kGroupThreads || !(s_key[tid + 1] != 0xFFFFFFFFu &&
                                                    (s_key[tid + 1] >> 8) == key >> 8 &&
                                                    q.slot + 1 < cap));
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       if constexpr (RA) pdl_wait();
       const int tid = threadIdx.x;
       const uint32_t key = tid < p.npairs ? pair_key(__ldcg(p.topk_ids + tid), tid, p.E) : 0xFFFFFFFFu;
-      const PairPlace q = group_pairs<2>(key, MT, s_rin, s_rkey, s_rwarp);
+      const PairPlace q = group_pairs<2>(key, p.npairs, MT, s_rin, s_rkey, s_rwarp);
       if (q.kept && q.head) {
         s_rexp[q.prob] = q.e;
         s_rrsum[q.prob] = q.rsum;
@@ -710,7 +714,11 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   }
 
   // ---------------------------------------------------------------- consumers
-  pdl_wait();
+  // Grouped resident mode: the grouping threads have waited already, and the block barrier
+  // after the grouping orders every thread after that wait (griddepcontrol.wait makes the
+  // earlier grids' memory visible to the whole grid); a second wait would only add its
+  // release latency.
+  if constexpr (!(GRP && RA)) pdl_wait();
   if constexpr (RA) {
     // The activation conversion of the pre-pass, done here into shared memory: A[m][k]
     // (bf16) -> A'[kt][m][64] (f16) = A * 2^-p with one power of two p per (token m, 64-wide
@@ -1244,7 +1252,7 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
   if (tid < npairs) id = __ldcg(topk_ids + tid);
   const uint32_t key0 = tid < npairs ? pair_key(id, tid, E) : 0xFFFFFFFFu;
   if (tid < npairs && key0 == 0xFFFFFFFFu && lead) atomicExch(status, 6);
-  const PairPlace q = group_pairs<0>(key0, cap, s_in, s_key, s_warp);
+  const PairPlace q = group_pairs<0>(key0, npairs, cap, s_in, s_key, s_warp);
   if (q.valid && !q.kept && lead) atomicExch(status, 6);
   const int prob = q.prob, slot = q.slot, pair = q.pair;
   const bool kept = q.kept, head = q.head, last = q.last;
