@@ -67,7 +67,7 @@ size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt
   const size_t mt = (size_t)decode_mt(M);
   const size_t stage = resident_kt ? (size_t)ks * tile_bytes(fmt)
                                    : (size_t)ks * (tile_bytes(fmt) + (size_t)M * 128 + kAScaleStride * 4);
-  return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 +
+  return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 + mt * 128 * 4 +
          decode_resident_bytes(M, resident_kt) + (size_t)stages * 16 + 64;
 }
 
@@ -377,7 +377,10 @@ __device__ __forceinline__ PairPlace group_pairs(uint32_t key, int n, int cap, u
 // as its first segment, writes its partial sums, and the publisher warp announces them with
 // a release add on the tile's counter, so that no consumer waits on a global round trip in
 // the middle of a call.  c_lo waits (bounded) for the count, adds the partials in
-// contributor order to its own and resets the counter for the next call.
+// contributor order to its own and resets the counter for the next call.  When exactly one
+// later CTA shares the tile, c_lo's publisher warp does that wait while c_lo's consumers
+// still stream and copies the partial into shared memory, so the reduction at the end of
+// the call makes no global round trip.
 //
 // Resident mode (RA, small M * K): the kernel converts the whole activation matrix into
 // shared memory itself after griddepcontrol.wait (no pre-pass kernel), the stages carry
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   constexpr int SLOT = MT * kSlotPad;  // floats per warp reduction slot (32 rows + pad)
   constexpr int WBYTES = KS * TB;      // weight bytes of a full stage
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_flag, s_ncon;
+  __shared__ int s_flag, s_ncon, s_pre;
   __shared__ unsigned long long s_gkey[16];  // greedy head: this CTA's best key per token
   __shared__ int64_t s_clo;
   // The next kernel in the stream may launch now: it only waits (griddepcontrol.wait)
@@ -445,8 +448,10 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   const int64_t i0 = c * I / G, i1 = (c + 1) * I / G;
 
   float* slots = reinterpret_cast<float*>(smem + (size_t)S * STAGE);
+  // the reducer's copy [MT][128] of the partial of its last tile's one later contributor
+  float* pre = slots + (size_t)CW * SLOT;
   // resident mode: activations [KT][M][64] f16 (the pre-pass layout) and scales [KT][8]
-  uint8_t* res = smem + (size_t)S * STAGE + (size_t)CW * SLOT * 4;
+  uint8_t* res = smem + (size_t)S * STAGE + (size_t)CW * SLOT * 4 + (size_t)MT * 128 * 4;
   const size_t res_bytes = RA ? decode_resident_bytes(M, KT) : 0;
   const uint32_t res_u = smem_u32(res), rscale_u = res_u + (uint32_t)(M * KT * 128);
   uint64_t* full = reinterpret_cast<uint64_t*>(res + res_bytes);
@@ -454,6 +459,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   const uint32_t ring_u = smem_u32(smem), full_u = smem_u32(full), empty_u = smem_u32(empty);
   const uint32_t pub_u = smem_u32(empty + S);  // consumers -> publisher: partial written
   const uint32_t aready_u = smem_u32(empty + S + 1);  // resident mode: activations converted
+  const uint32_t pre_u = smem_u32(empty + S + 2);  // publisher -> reducer: later partials in
 
   // Stages walk the CTA's items in order; all loop state advances incrementally.
   const int kt_first = (int)(i0 % KT);
@@ -473,6 +479,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     }
     mbar_init(pub_u, CW);
     mbar_init(aready_u, 1);
+    mbar_init(pre_u, 1);
   }
   fence_mbar_init();
   __syncthreads();
@@ -486,6 +493,36 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         publish_release(reinterpret_cast<unsigned int*>(&p.counters[i0 / KT]));
       else
         atomicExch(p.status, 5);
+    }
+    // A CTA whose last segment starts a row tile that exactly one later CTA shares reduces
+    // that tile, and that CTA's partial is its first segment, published early: wait for it
+    // here, while the consumers still stream, copy it into shared memory and reset the
+    // counter.  s_pre: 2 the partial is in `pre`, 0 the wait ran out.  (Tiles shared by more
+    // CTAs end in middle CTAs that finish with this one; their reducer's consumers wait for
+    // them themselves.)  The counters are the previous call's until that grid has finished:
+    // wait for it first.
+    const int64_t rl = i0 < i1 ? (i1 - 1) / KT : 0;
+    if (i0 < i1 && rl * KT >= i0 && rl * KT + KT > i1 && owner_of(rl * KT + KT - 1, I, G) == c + 1) {
+      pdl_wait();
+      unsigned int* ctr = reinterpret_cast<unsigned int*>(&p.counters[rl]);
+      bool got = false;
+      if (lane == 0) got = wait_count(ctr, 1u, p.wait_ns);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (got) {
+        (void)ld_acquire_gpu(ctr);  // every lane acquires the contributor's writes
+        const int mrows = GRP ? s_rcnt[(int)(rl / p.RT)] : M;
+        const float* src = p.partials + (size_t)(c + 1) * 2 * MT * 128;
+        for (int i = lane; i < mrows * 128; i += 32) pre[i] = __ldcg(src + i);
+        __syncwarp();
+        if (lane == 0) *ctr = 0;  // the contributor has arrived: reset for the next call
+      } else if (lane == 0) {
+        atomicExch(p.status, 5);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        s_pre = got ? 2 : 0;
+        mbar_arrive(pre_u);
+      }
     }
     return;
   }
@@ -1050,24 +1087,35 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     }
     if (reducer) {
       if (threadIdx.x == 0) {
-        unsigned int* ctr = reinterpret_cast<unsigned int*>(&p.counters[rt]);
-        const bool got = wait_count(ctr, (unsigned int)(s_ncon - 1), p.wait_ns);
-        if (got) *ctr = 0;  // every contributor has arrived: reset for the next call
-        else atomicExch(p.status, 5);
-        s_flag = got;
+        int f = 0;
+        if (s_ncon == 2) {
+          // the publisher warp has the later contributor's partial (and reset the counter)
+          if (mbar_wait_bounded(pre_u, 0, p.wait_ns)) f = s_pre;
+        } else {
+          unsigned int* ctr = reinterpret_cast<unsigned int*>(&p.counters[rt]);
+          if (wait_count(ctr, (unsigned int)(s_ncon - 1), p.wait_ns)) {
+            *ctr = 0;  // every contributor has arrived: reset for the next call
+            f = 1;
+          }
+        }
+        if (!f) atomicExch(p.status, 5);
+        s_flag = f;
       }
       consumer_sync(CT);
       if (s_flag) {
         // this CTA's own partial (its slots, in fixed order) first, then the later
-        // contributors' partials in contributor order, loaded in batches of 8
+        // contributors' partials in contributor order (one: from shared memory; more:
+        // loaded in batches of 8)
         const int64_t c_lo = s_clo;
         const int ncon = s_ncon;
+        const bool in_smem = s_flag == 2;
         auto tile_sum = [&](int m, int row) -> float {
           const int pr = row >> 5, rr = row & 31;
           float sum = 0.0f;
 #pragma unroll
           for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + pr) * SLOT + m * kSlotPad + rr];
           const size_t off = (size_t)m * 128 + row;
+          if (in_smem) return sum + pre[off];
           for (int b0 = 1; b0 < ncon; b0 += 8) {
             float v[8];
 #pragma unroll
