@@ -40,6 +40,7 @@ constexpr int kGtCount = kGtExpert + kGtMaxProblems;
 constexpr int kGtRowsum = kGtCount + kGtMaxProblems;
 constexpr int kGtPair = kGtRowsum + kGtMaxProblems;
 constexpr int kGtInts = kGtPair + kGtMaxProblems * 16;
+static_assert(kGtInts == kGroupTableInts, "group table size differs from the workspace layout's");
 constexpr int kSlotPad = 36;        // floats per token row of a warp's reduction slot
 #ifndef VT_DECODE_PREFETCH
 #define VT_DECODE_PREFETCH 2
@@ -939,55 +940,55 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
               acc[b][u][3] = fmaf(t1[3] * a2[1], fg81, acc[b][u][3]);
             }
           }
-          return;
-        }
-        uint32_t bfr[NJ][4][2];
-        float as[NJ][2];
-#pragma unroll
-        for (int u = 0; u < NJ; ++u) {
-          load_b(u, bfr[u]);
-          load_as(u, as[u]);
-        }
-        uint32_t sc4;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc4) : "r"(tb + soff));
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int j = 2 * jp + b;
-          const int4 wv = ld_shared_v4(tb + j * 512 + lane * 16);
-          const uint32_t two = b ? (sc4 >> 16) : (sc4 & 0xFFFFu);
-          const uint32_t sc = (FMT == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
-          const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc);
-          const __half2 sg = __low2half2(sc2), sg8 = __high2half2(sc2);
-          const uint32_t words[4] = {(uint32_t)wv.x, (uint32_t)wv.y, (uint32_t)wv.z,
-                                     (uint32_t)wv.w};
-          float tmp[NJ][4];
-#pragma unroll
-          for (int u = 0; u < NJ; ++u)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) tmp[u][r] = 0.0f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t r0, r1, r2, r3;
-            e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
-            __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&r0), sg);
-            __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&r1), sg8);
-            __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&r2), sg);
-            __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&r3), sg8);
-            const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0);
-            const uint32_t a1 = *reinterpret_cast<uint32_t*>(&h1);
-            const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2);
-            const uint32_t a3 = *reinterpret_cast<uint32_t*>(&h3);
-#pragma unroll
-            for (int u = 0; u < NJ; ++u)
-              mma_f16_16816(tmp[u], a0, a1, a2, a3, bfr[u][q][0], bfr[u][q][1]);
-          }
-          // this k tile's sums back to the activations' true scale
+        } else {
+          uint32_t bfr[NJ][4][2];
+          float as[NJ][2];
 #pragma unroll
           for (int u = 0; u < NJ; ++u) {
-            acc[b][u][0] = fmaf(tmp[u][0], as[u][0], acc[b][u][0]);
-            acc[b][u][1] = fmaf(tmp[u][1], as[u][1], acc[b][u][1]);
-            acc[b][u][2] = fmaf(tmp[u][2], as[u][0], acc[b][u][2]);
-            acc[b][u][3] = fmaf(tmp[u][3], as[u][1], acc[b][u][3]);
+            load_b(u, bfr[u]);
+            load_as(u, as[u]);
+          }
+          uint32_t sc4;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc4) : "r"(tb + soff));
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int j = 2 * jp + b;
+            const int4 wv = ld_shared_v4(tb + j * 512 + lane * 16);
+            const uint32_t two = b ? (sc4 >> 16) : (sc4 & 0xFFFFu);
+            const uint32_t sc = (FMT == FMT_NV) ? e4m3x2_to_f16x2(two) : mxenc2_to_f16x2(two);
+            const __half2 sc2 = *reinterpret_cast<const __half2*>(&sc);
+            const __half2 sg = __low2half2(sc2), sg8 = __high2half2(sc2);
+            const uint32_t words[4] = {(uint32_t)wv.x, (uint32_t)wv.y, (uint32_t)wv.z,
+                                       (uint32_t)wv.w};
+            float tmp[NJ][4];
+#pragma unroll
+            for (int u = 0; u < NJ; ++u)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) tmp[u][r] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t r0, r1, r2, r3;
+              e2m1x8_to_f16x8(words[q], r0, r1, r2, r3);
+              __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&r0), sg);
+              __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&r1), sg8);
+              __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&r2), sg);
+              __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&r3), sg8);
+              const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0);
+              const uint32_t a1 = *reinterpret_cast<uint32_t*>(&h1);
+              const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2);
+              const uint32_t a3 = *reinterpret_cast<uint32_t*>(&h3);
+#pragma unroll
+              for (int u = 0; u < NJ; ++u)
+                mma_f16_16816(tmp[u], a0, a1, a2, a3, bfr[u][q][0], bfr[u][q][1]);
+            }
+            // this k tile's sums back to the activations' true scale
+#pragma unroll
+            for (int u = 0; u < NJ; ++u) {
+              acc[b][u][0] = fmaf(tmp[u][0], as[u][0], acc[b][u][0]);
+              acc[b][u][1] = fmaf(tmp[u][1], as[u][1], acc[b][u][1]);
+              acc[b][u][2] = fmaf(tmp[u][2], as[u][0], acc[b][u][2]);
+              acc[b][u][3] = fmaf(tmp[u][3], as[u][1], acc[b][u][3]);
+            }
           }
         }
       };
