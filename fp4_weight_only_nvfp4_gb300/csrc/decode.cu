@@ -768,17 +768,10 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     const int Mrows = GRP ? p.Mtok : M;
     const int64_t total = (int64_t)Mrows * KT * 8;
     const __nv_bfloat16* A = p.A;
-    for (int64_t base = 0; base < total; base += CT) {
-      const int64_t idx = base + threadIdx.x;
+    // granule idx (loaded as v) converted and stored; a whole warp calls it (shuffles)
+    auto put = [&](int64_t idx, uint4 v, int64_t ktr, int m) {
       const bool valid = idx < total;
       const int gi = (int)(idx & 7);
-      const int64_t r = idx >> 3;
-      const int64_t ktr = r / Mrows;
-      const int m = (int)(r - ktr * Mrows);
-      const int64_t k0 = ktr * 64 + gi * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (valid && k0 < p.K)
-        v = __ldg(reinterpret_cast<const uint4*>(A + m * p.lda + k0));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       int mx = act_maxmag8(w);
 #pragma unroll
@@ -789,6 +782,41 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         st_shared_v4(res_u + (uint32_t)(((ktr * M + m) * 64 + ((gi ^ (m & 7)) * 8)) * 2),
                      o.x, o.y, o.z, o.w);
         if (gi == 0) st_shared_f32(rscale_u + (uint32_t)((ktr * kResScaleStride + m) * 4), ldexpf(1.0f, pe));
+      }
+    };
+    if constexpr (GRP) {
+      // up to 8 tokens of up to 62 k tiles: a thread's granules are loaded together first,
+      // so that their loads are in flight at once
+      constexpr int CU = 4;
+      for (int64_t base = 0; base < total; base += CU * CT) {
+        uint4 v[CU];
+        int64_t kr[CU];
+        int mm[CU];
+#pragma unroll
+        for (int j = 0; j < CU; ++j) {
+          const int64_t idx = base + j * CT + threadIdx.x;
+          const int64_t r = idx >> 3;
+          kr[j] = r / Mrows;
+          mm[j] = (int)(r - kr[j] * Mrows);
+          const int64_t k0 = kr[j] * 64 + (idx & 7) * 8;
+          v[j] = make_uint4(0, 0, 0, 0);
+          if (idx < total && k0 < p.K)
+            v[j] = __ldg(reinterpret_cast<const uint4*>(A + mm[j] * p.lda + k0));
+        }
+#pragma unroll
+        for (int j = 0; j < CU; ++j) put(base + j * CT + threadIdx.x, v[j], kr[j], mm[j]);
+      }
+    } else {
+      for (int64_t base = 0; base < total; base += CT) {
+        const int64_t idx = base + threadIdx.x;
+        const int64_t r = idx >> 3;
+        const int64_t ktr = r / Mrows;
+        const int m = (int)(r - ktr * Mrows);
+        const int64_t k0 = ktr * 64 + (int)(idx & 7) * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (idx < total && k0 < p.K)
+          v = __ldg(reinterpret_cast<const uint4*>(A + m * p.lda + k0));
+        put(idx, v, ktr, m);
       }
     }
     // scales of the token columns past M (read by the fragments of absent tokens)
