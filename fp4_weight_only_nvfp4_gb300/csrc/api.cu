@@ -222,6 +222,9 @@ vt_status vt::decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_op
   out->stages = stages;
   out->grid = (int)grid;
   out->resident = resident ? 1 : 0;
+  // up to 2 tokens and at least three row tiles per CTA (the long lm_head-like calls): the
+  // per-group epilogue, so that most warps do not stop at every tile's end
+  out->epi = (ks == 8 && M <= 2 && items >= 3 * W->KT * grid) ? 1 : 0;
   return VT_OK;
 }
 
@@ -407,6 +410,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     D.w4a4 = w4a4 ? 1 : 0;
     D.alpha = alpha;
     D.resident = sh.resident;
+    D.epi = sh.epi;
     if (g_idx) {
       D.g_idx = g_idx;
       D.g_val = g_val;

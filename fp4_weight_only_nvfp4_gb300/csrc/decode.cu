@@ -69,7 +69,7 @@ size_t decode_smem_bytes(int fmt, int M, int ks, int stages, int64_t resident_kt
   const size_t stage = resident_kt ? (size_t)ks * tile_bytes(fmt)
                                    : (size_t)ks * (tile_bytes(fmt) + (size_t)M * 128 + kAScaleStride * 4);
   return (size_t)stages * stage + kConsumerWarps * mt * kSlotPad * 4 + mt * 128 * 4 +
-         decode_resident_bytes(M, resident_kt) + (size_t)stages * 16 + 64;
+         decode_resident_bytes(M, resident_kt) + (size_t)stages * 16 + 128;
 }
 
 bool decode_resident_ok(int M, int64_t KT, int64_t RT) {
@@ -389,7 +389,7 @@ __device__ __forceinline__ PairPlace group_pairs(uint32_t key, int n, int cap, u
 // can queue behind the weights.  The split-K counters then rely on being left at zero by
 // the previous call (each reducer resets its counter; the workspace keeps the counters in a
 // fixed region that no other data of any weight overlaps).
-template <int FMT, int MT, int KS, bool GRP, bool RA>
+template <int FMT, int MT, int KS, bool GRP, bool RA, bool EPI>
 __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const DecodeParams p) {
   constexpr int TB = tile_bytes(FMT);
   constexpr int NJ = MT / 8;           // n8 MMA column blocks
@@ -461,6 +461,10 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   const uint32_t pub_u = smem_u32(empty + S);  // consumers -> publisher: partial written
   const uint32_t aready_u = smem_u32(empty + S + 1);  // resident mode: activations converted
   const uint32_t pre_u = smem_u32(empty + S + 2);  // publisher -> reducer: later partials in
+  // EPI, per row-block group jp: the group's other three warps have written their slots
+  // (gfull), the group's reducing warp has read them (gfree)
+  [[maybe_unused]] const uint32_t gfull_u = smem_u32(empty + S + 3);
+  [[maybe_unused]] const uint32_t gfree_u = smem_u32(empty + S + 7);
 
   // Stages walk the CTA's items in order; all loop state advances incrementally.
   const int kt_first = (int)(i0 % KT);
@@ -481,6 +485,12 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
     mbar_init(pub_u, CW);
     mbar_init(aready_u, 1);
     mbar_init(pre_u, 1);
+    if constexpr (EPI) {
+      for (int j = 0; j < 4; ++j) {
+        mbar_init(gfull_u + 8 * j, 3);
+        mbar_init(gfree_u + 8 * j, 1);
+      }
+    }
   }
   fence_mbar_init();
   __syncthreads();
@@ -861,6 +871,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   uint32_t par = 0;
   const int64_t rt_first = i0 / KT;
   int64_t rt = rt_first;  // row tile of the current segment
+  [[maybe_unused]] uint32_t nfast = 0;  // EPI: group epilogues so far (every warp meets the same tiles)
   while (pos < i1) {
     const int n = stage_len(pos, kt);
     if constexpr (GRP) {
@@ -1053,6 +1064,10 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
       s_clo = c;
       s_ncon = (int)(c_hi - c + 1);
     }
+    if constexpr (EPI) {
+      // the group's last reduction must have read the slots before they are rewritten
+      if (nfast > 0 && ok) ok = mbar_wait_bounded(gfree_u + 8 * jp, (nfast - 1) & 1u, p.wait_ns);
+    }
     float* my = slots + warp * SLOT;
 #pragma unroll
     for (int b = 0; b < 2; ++b)
@@ -1067,6 +1082,39 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[b][u][r] = 0.0f;
       }
+    if constexpr (EPI) {
+      if (complete && !p.silu && Mc <= 2) {
+        // Rows 32 jp .. 32 jp + 31 of a complete tile need only the slots of the four warps
+        // of row-block group jp: one of them (in turn) sums those rows once the other three
+        // have written their slots, and the rest go straight on to the next tile.  The sums
+        // and their order are those of the CTA-wide epilogue below.
+        __syncwarp();
+        if (kq != (int)(nfast & 3u)) {
+          if (lane == 0) mbar_arrive(gfull_u + 8 * jp);
+        } else {
+          if (ok) ok = mbar_wait_bounded(gfull_u + 8 * jp, nfast & 1u, p.wait_ns);
+          for (int m = 0; m < Mc; ++m) {  // one token per pass: warp-uniform m
+            float sum = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sum += slots[(q * 4 + jp) * SLOT + m * kSlotPad + lane];
+            const int64_t n = packed_to_row(p.layout, rt * kTileRows + 32 * jp + lane, p.N, p.seg_split);
+            if (p.g_idx) {
+              unsigned long long key = 0;
+              if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
+              greedy_fold(key, s_gkey, m);
+            } else if (n >= 0) {
+              const float f = n < p.seg_split ? f0 : f1;
+              p.C[(int64_t)m * p.ldc + n] = __float2bfloat16_rn(sum * f);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(gfree_u + 8 * jp);
+        }
+        ++nfast;
+        ++rt;
+        continue;
+      }
+    }
     consumer_sync(CT);
     const int nout = Mc * 128;
     if (complete && p.silu) {
@@ -1231,11 +1279,11 @@ static cudaError_t allow_smem(Kern* k, int bytes, int* done_per_device) {
   return e;
 }
 
-template <int FMT, int MT, int KS, bool GRP = false, bool RA = false>
+template <int FMT, int MT, int KS, bool GRP = false, bool RA = false, bool EPI = false>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   static int done[64] = {0};
   const size_t smem = decode_smem_bytes(FMT, GRP ? MT : L.M, KS, L.stages, RA ? L.KT : 0);
-  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP, RA>, (int)smem, done);
+  cudaError_t e = allow_smem(k_decode<FMT, MT, KS, GRP, RA, EPI>, (int)smem, done);
   if (e != cudaSuccess) return e;
   DecodeParams p;
   p.tiles = reinterpret_cast<const uint8_t*>(L.packed) + kHeaderBytes;
@@ -1284,7 +1332,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP, RA>, p);
+  return cudaLaunchKernelEx(&cfg, k_decode<FMT, MT, KS, GRP, RA, EPI>, p);
 }
 
 // ------------------------------------------------------------- grouped pre-pass
@@ -1431,6 +1479,9 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) 
     if (L.ks == 4)
       e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 4, false, true>(L, s)
                             : launch_t<FMT_MX, 8, 4, false, true>(L, s);
+    else if (L.epi)
+      e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 8, false, true, true>(L, s)
+                            : launch_t<FMT_MX, 8, 8, false, true, true>(L, s);
     else
       e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 8, false, true>(L, s)
                             : launch_t<FMT_MX, 8, 8, false, true>(L, s);
@@ -1466,7 +1517,10 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) 
     if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 4>(L, s) : launch_t<FMT_NV, 16, 4>(L, s);
     else e = (mt == 8) ? launch_t<FMT_MX, 8, 4>(L, s) : launch_t<FMT_MX, 16, 4>(L, s);
   } else {
-    if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 8>(L, s) : launch_t<FMT_NV, 16, 8>(L, s);
+    if (mt == 8 && L.epi)
+      e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 8, false, false, true>(L, s)
+                            : launch_t<FMT_MX, 8, 8, false, false, true>(L, s);
+    else if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 8>(L, s) : launch_t<FMT_NV, 16, 8>(L, s);
     else e = (mt == 8) ? launch_t<FMT_MX, 8, 8>(L, s) : launch_t<FMT_MX, 16, 8>(L, s);
   }
   if (launches) *launches = 2;

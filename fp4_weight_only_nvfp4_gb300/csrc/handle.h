@@ -29,7 +29,7 @@ int sm_count();
 // (library choice); w4a4 calls always take the activation pre-pass.  Shared by every decode
 // entry point so that they launch the same shapes.
 struct DecodeShape {
-  int ks, stages, grid, resident;
+  int ks, stages, grid, resident, epi;
 };
 vt_status decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_opts* opts, bool w4a4,
                        DecodeShape* out);

@@ -131,6 +131,7 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   D.withhold = hooks.withhold_weights;
   D.layout = (uint32_t)W->layout;
   D.resident = sh.resident;
+  D.epi = sh.epi;
   int launches = 0;
   e = launch_decode(D, (cudaStream_t)s, &launches);
   if (e != cudaSuccess) return cuda_err(e);
