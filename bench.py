@@ -752,9 +752,11 @@ class _Slots:
             self.host[a:b].copy_(self.dev[a:b], non_blocking=True)
 
 
-def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h, copies=2):
+def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h, copies=2,
+              flush=None):
     """Warm-up, one CUDA graph per rotated step (copy in, every call, copy out), timed
-    replays in turn."""
+    replays in turn.  flush(index of the last graph replayed), if given, finishes the last
+    timed step's copies inside the timed region."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -779,6 +781,8 @@ def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h, c
         t0.record(stream)
         for st in range(args.steps):
             graphs[st % len(graphs)].replay()
+        if flush is not None:
+            flush((args.steps - 1) % len(graphs))
         t1.record(stream)
     stream.synchronize()
     ms_step = max_over_ranks(t0.elapsed_time(t1), dist, dev) / args.steps
@@ -790,8 +794,8 @@ def _time_e2e(args, w, issues, stream, dev, step_bytes, world, dist, h2d, d2h, c
 def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist):
     """The step end to end through the public API: every call's activations from pinned host
     memory (one host-to-device copy of the step's inputs), the calls, and every call's
-    result back to pinned host memory (one device-to-host copy), all inside the timed
-    region.  steps_calls: the rotated steps (one, unless a step alone fits the L2)."""
+    result back to pinned host memory, all inside the timed region.  steps_calls: the
+    rotated steps (one, unless a step alone fits the L2)."""
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
     greedy = w.kind == "greedy"
@@ -810,7 +814,8 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
     # one, its input copy for the next step fills the other, the way a serving loop stages the
     # next batch (still one host-to-device copy per timed step).  A decode step's results go
     # back in two copies on a side stream: the outputs of all calls but the last while the
-    # last call runs, then the last call's output.
+    # last call runs, then (without rotation: two sets of output slots) the last call's output
+    # while the next step computes; after the timed steps the last one's goes back too.
     piped = w.kind == "prefill"
     double = not piped and len(steps_calls) == 1
     side_in = torch.cuda.Stream(device=dev) if (piped or double) else None
@@ -822,17 +827,26 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
         host_out = [not (silu and w.projs[pi].fused) for _, _, pi, _ in calls]
         INS = [_Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
                        for i, (_, _, pi, M) in enumerate(calls)], dev) for _ in range(2 if double else 1)]
-        OUT = _Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
-                      for i, (_, _, pi, M) in enumerate(calls)], dev)
+        # a decode step without rotation also keeps two sets of output slots: the last call's
+        # output of a step goes back to the host while the next step computes
+        OUTS = [_Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
+                        for i, (_, _, pi, M) in enumerate(calls)], dev)
+                for _ in range(2 if double else 1)]
         for IN in INS:
             for i, (_, _, pi, M) in enumerate(calls):
                 if host_in[i]:
                     IN.view(i, (M, w.projs[pi].K), torch.bfloat16, host=True).copy_(
                         torch.randn((M, w.projs[pi].K)).to(torch.bfloat16))
 
+        last = len(calls) - 1
+
         def issue(par=0):
-            IN = INS[par]
+            IN, OUT = INS[par], OUTS[par]
             ready = []
+            if double:  # the previous step's last output, back while this step computes
+                side_out.wait_stream(stream)
+                with torch.cuda.stream(side_out):
+                    OUTS[1 - par].to_host(last)
             if piped:
                 side_in.wait_stream(stream)
                 with torch.cuda.stream(side_in):
@@ -881,20 +895,23 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
             if piped:
                 stream.wait_stream(side_in)
                 stream.wait_stream(side_out)
+            elif double:
+                stream.wait_stream(side_out)
+                stream.wait_stream(side_in)
             else:
                 side_out.wait_stream(stream)
                 with torch.cuda.stream(side_out):
-                    OUT.to_host(len(calls) - 1)
+                    OUT.to_host(last)
                 stream.wait_stream(side_out)
-                if double:
-                    stream.wait_stream(side_in)
         issues = [issue] if not double else [lambda: issue(0), lambda: issue(1)]
         copies = (sum(host_in) + sum(host_out)) if piped else (3 if len(calls) > 1 else 2)
-        return issues, INS[0].nbytes, OUT.nbytes, copies
+        # after the timed steps: the last step's last output (its own device-to-host copy)
+        flush = (lambda par: OUTS[par].to_host(last)) if double else None
+        return issues, INS[0].nbytes, OUTS[0].nbytes, copies, flush
 
     steps = [make_step(sc) for sc in steps_calls]
     return _time_e2e(args, w, [f for st in steps for f in st[0]], stream, dev, step_bytes, world,
-                     dist, steps[0][1], steps[0][2], copies=steps[0][3])
+                     dist, steps[0][1], steps[0][2], copies=steps[0][3], flush=steps[0][4])
 
 
 def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
