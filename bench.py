@@ -916,30 +916,54 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
 
 def run_e2e_moe(args, w, sets, calls, ws, stream, dev, step_bytes, world, dist, route):
     """The MoE step end to end: every call's activations and routing from pinned host memory
-    (one copy in), the calls, every call's expert outputs back to the host (one copy out)."""
+    (one copy in), the calls, every call's expert outputs back to the host.  As for the
+    dense decode steps: two sets of input slots (a step's inputs come in while the previous
+    step computes), the outputs of all calls but the last go back while the last call runs,
+    and the last call's output (two sets of output slots) while the next step computes; after
+    the timed steps the last one's goes back inside the timed region."""
     import torch
     import fp4_weight_only_nvfp4_gb300 as vt
     p, topk = w.projs[0], w.extra["topk"]
     sizes = []
     for _, _, _, M in calls:
         sizes += [M * p.K * 2, M * topk * 4]
-    IN = _Slots(sizes, dev)
-    OUT = _Slots([M * topk * p.N * 2 for _, _, _, M in calls], dev)
-    for i, (c, _, _, M) in enumerate(calls):
-        IN.view(2 * i, (M, p.K), torch.bfloat16, host=True).copy_(
-            torch.randn((M, p.K)).to(torch.bfloat16))
-        IN.view(2 * i + 1, (M, topk), torch.int32, host=True).copy_(route[(c, M)].cpu())
+    INS = [_Slots(sizes, dev) for _ in range(2)]
+    OUTS = [_Slots([M * topk * p.N * 2 for _, _, _, M in calls], dev) for _ in range(2)]
+    for IN in INS:
+        for i, (c, _, _, M) in enumerate(calls):
+            IN.view(2 * i, (M, p.K), torch.bfloat16, host=True).copy_(
+                torch.randn((M, p.K)).to(torch.bfloat16))
+            IN.view(2 * i + 1, (M, topk), torch.int32, host=True).copy_(route[(c, M)].cpu())
+    side_in, side_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    last = len(calls) - 1
 
-    def issue():
-        IN.to_dev()
+    def issue(par):
+        IN, OUT = INS[par], OUTS[par]
+        side_out.wait_stream(stream)
+        with torch.cuda.stream(side_out):  # the previous step's last output
+            OUTS[1 - par].to_host(last)
+        side_in.wait_stream(stream)
+        with torch.cuda.stream(side_in):  # the next step's inputs
+            INS[1 - par].to_dev()
         for i, (c, layer, pi, M) in enumerate(calls):
             vt.w4a16_gemm_moe(IN.view(2 * i, (M, p.K), torch.bfloat16), sets[c][layer][pi],
                               IN.view(2 * i + 1, (M, topk), torch.int32),
                               out=OUT.view(i, (M * topk, p.N), torch.bfloat16), workspace=ws,
                               stream=stream)
-        OUT.to_host()
+            if i == last - 1:
+                side_out.wait_stream(stream)
+                with torch.cuda.stream(side_out):
+                    OUT.to_host(0, i + 1)
+        stream.wait_stream(side_out)
+        stream.wait_stream(side_in)
 
-    return _time_e2e(args, w, [issue], stream, dev, step_bytes, world, dist, IN.nbytes, OUT.nbytes)
+    # the first step's inputs are in place before the timing starts (later ones come in
+    # during the step before)
+    with torch.cuda.stream(stream):
+        INS[0].to_dev()
+    return _time_e2e(args, w, [lambda: issue(0), lambda: issue(1)], stream, dev, step_bytes,
+                     world, dist, INS[0].nbytes, OUTS[0].nbytes, copies=3,
+                     flush=lambda par: OUTS[par].to_host(last))
 
 
 # ---------------------------------------------------------------- CPU (oracle) leg
