@@ -21,7 +21,8 @@ _ST = ctypes.c_int
 class LaunchInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("warps_per_cta", ctypes.c_int),
                 ("m_tile", ctypes.c_int), ("items", ctypes.c_int64),
-                ("launches", ctypes.c_int64), ("calls", ctypes.c_int64)]
+                ("launches", ctypes.c_int64), ("calls", ctypes.c_int64),
+                ("tile_epilogue", ctypes.c_int)]
 
 
 class GemmOpts(ctypes.Structure):

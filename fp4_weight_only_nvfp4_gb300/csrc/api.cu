@@ -421,6 +421,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     cudaError_t e = launch_decode(D, (cudaStream_t)s, &launches);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     W->info.path = 1;
+    W->info.tile_epilogue = sh.epi;
     W->info.grid = D.grid;
     W->info.warps_per_cta = 18;  // 16 consumer warps, the TMA producer, the publisher
     W->info.m_tile = mt;
@@ -459,6 +460,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     return fail(VT_ERR_UNSUPPORTED, "the prefill tile path is not available in this build");
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   W->info.path = 2;
+  W->info.tile_epilogue = 0;
   W->info.grid = grid;
   W->info.warps_per_cta = 14;  // TMA, MMA, 8 dequantiser and 4 epilogue warps
   W->info.m_tile = 128;
@@ -555,6 +557,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
                                         (cudaStream_t)s, &launches);
   if (e != cudaSuccess) return cuda_fail(e, "grouped decode launch");
   W->info.path = 3;
+  W->info.tile_epilogue = 0;
   W->info.grid = D.grid;
   W->info.warps_per_cta = 18;
   W->info.m_tile = mrows;

@@ -73,6 +73,8 @@ typedef struct {
                          them (the routing is read on the device); prefill: output tiles */
   int64_t launches;   /* kernels enqueued by that call */
   int64_t calls;      /* GEMM calls made on this handle so far */
+  int tile_epilogue;  /* decode: 1 when complete row tiles were summed per row-block group
+                         (up to 2 tokens, at least three row tiles per CTA), else 0 */
 } vt_fp4_launch_info;
 
 /* Optional overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
