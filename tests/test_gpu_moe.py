@@ -151,3 +151,19 @@ def test_moe_both_grouped_modes_match_oracle(fmt):
             check_rows(y.float().cpu().numpy(), _oracle(fmt, Ab, srcs, ids, N),
                        what=f"moe fmt={fmt} K={K} M={M}")
         assert vt.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+def test_moe_one_kernel_mode_ragged_k(fmt):
+    """K = 544 (8.5 k tiles of 64): the in-kernel conversion of the one-launch mode zero-fills
+    the last k tile past K, as the prepack zero-fills the weights there."""
+    E, N, K = 5, 260, 544
+    srcs, W = _experts(fmt, E, N, K, 30 + fmt)
+    for M, topk in ((1, 3), (6, 2)):
+        ids = _routing(M, topk, E, seed=M + 40)
+        Ab = make_acts(synth.tensor_id(89, 30 + fmt, M), M, K)
+        y = vt.w4a16_gemm_moe(bf16_dev(Ab), W, to_dev(ids))
+        torch.cuda.synchronize()
+        assert W.stats()["launches"] == 1
+        check_rows(y.float().cpu().numpy(), _oracle(fmt, Ab, srcs, ids, N),
+                   what=f"moe ragged K fmt={fmt} M={M}")
