@@ -51,6 +51,45 @@ def test_quantize_act_bit_exact(fmt):
             assert np.array_equal(codes.cpu().numpy(), rc), (alpha, M, K)
 
 
+MIDPOINTS = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+EVEN_CODE = [0, 2, 2, 4, 4, 6, 6]  # E2M1 codes 0..7 = 0, .5, 1, 1.5, 2, 3, 4, 6: ties go to the even one
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+def test_quantize_act_e2m1_midpoints(fmt):
+    # every group holds 6 * 2^k (its largest magnitude), so the group step is exactly 2^k
+    # (NVFP4 with alpha = 1: s = E4M3(2^k); MXFP4: e = k) and x / step lands exactly on each
+    # midpoint of the E2M1 grid, on both signs, on its bf16 neighbours, on small magnitudes
+    # that round to +0 from below zero, and on the saturation point
+    g = 16 if fmt == vt.NVFP4 else 32
+    vals = MIDPOINTS + [-v for v in MIDPOINTS]
+    vals += [0.25 + 2 ** -9, 0.75 - 2 ** -8, 1.25 + 2 ** -7, 3.5 - 2 ** -6, -0.1, -0.2421875,
+             0.0, 6.0, -6.0, 5.0 + 2 ** -5, -(2.5 - 2 ** -6)]
+    per = g - 1
+    groups = [vals[i:i + per] for i in range(0, len(vals), per)]
+    rows = []
+    for k in (0, -5, -8, 7):
+        row = []
+        for grp in groups:
+            grp = grp + [0.0] * (per - len(grp))
+            row += [6.0 * 2.0 ** k] + [v * 2.0 ** k for v in grp]
+        rows.append(row)
+    A = _bits(np.array(rows))
+    M, K = A.shape
+    codes, scales = vt.quantize_act(bf16_dev(A), fmt, 1.0)
+    torch.cuda.synchronize()
+    c, s = codes.cpu().numpy(), scales.cpu().numpy()
+    rc, rs, _ = oracle.quantize_act(fmt, A, 1.0)
+    assert np.array_equal(s, rs) and np.array_equal(c, rc)
+    nib = np.stack([c & 15, c >> 4], axis=-1).reshape(M, K)
+    for m in range(M):
+        for j, v in enumerate(MIDPOINTS):  # the first group holds the midpoints, then their negatives
+            assert nib[m, 1 + j] == EVEN_CODE[j], (m, v)
+            neg = nib[m, 1 + len(MIDPOINTS) + j] if 1 + len(MIDPOINTS) + j < g else None
+            if neg is not None:
+                assert neg == (0 if EVEN_CODE[j] == 0 else 8 | EVEN_CODE[j]), (m, -v)
+
+
 def test_quantize_act_strided_and_nonfinite():
     fmt, M, K = vt.NVFP4, 6, 256
     A = make_acts(synth.tensor_id(91, 0, 1), M, K)
