@@ -1013,8 +1013,13 @@ def run_oracle_sample(w: Workload, target_s: float = 12.0, nthreads: int | None 
 
     frac = 1.0 / 1024
     nbytes, dt = run(frac)
-    frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))
-    nbytes, dt = run(frac)
+    # grow the sample towards the target: a small sample's time is mostly fixed per-call cost
+    # (the 8-column minimum, the W4A4 activation quantiser), so one extrapolation falls short
+    for _ in range(4):
+        if frac >= 1.0 or dt >= 0.5 * target_s:
+            break
+        frac = min(1.0, frac * max(1.0, target_s / max(dt, 1e-3)))
+        nbytes, dt = run(frac)
     reps = 1
     if frac >= 1.0 and dt < 0.5 * target_s:
         # the whole step is quicker than the target: run it repeatedly
