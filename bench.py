@@ -814,10 +814,11 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
     # one, its input copy for the next step fills the other, the way a serving loop stages the
     # next batch (still one host-to-device copy per timed step).  A decode step's results go
     # back in two copies on a side stream: the outputs of all calls but the last while the
-    # last call runs, then (without rotation: two sets of output slots) the last call's output
-    # while the next step computes; after the timed steps the last one's goes back too.
+    # last call runs, then the last call's output.  A step without rotation (decode or
+    # prefill) keeps two sets of output slots, and its last call's output goes back while the
+    # next step computes; after the timed steps the last one's goes back too.
     piped = w.kind == "prefill"
-    double = not piped and len(steps_calls) == 1
+    double = len(steps_calls) == 1
     side_in = torch.cuda.Stream(device=dev) if (piped or double) else None
     side_out = torch.cuda.Stream(device=dev)
 
@@ -826,9 +827,10 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
         host_in = [not (silu and not w.projs[pi].fused) for _, _, pi, _ in calls]
         host_out = [not (silu and w.projs[pi].fused) for _, _, pi, _ in calls]
         INS = [_Slots([M * w.projs[pi].K * 2 if host_in[i] else 0
-                       for i, (_, _, pi, M) in enumerate(calls)], dev) for _ in range(2 if double else 1)]
-        # a decode step without rotation also keeps two sets of output slots: the last call's
-        # output of a step goes back to the host while the next step computes
+                       for i, (_, _, pi, M) in enumerate(calls)], dev)
+               for _ in range(2 if double and not piped else 1)]
+        # a step without rotation also keeps two sets of output slots: the last call's output
+        # of a step goes back to the host while the next step computes
         OUTS = [_Slots([(M * 4 if greedy else M * w.projs[pi].N * 2) if host_out[i] else 0
                         for i, (_, _, pi, M) in enumerate(calls)], dev)
                 for _ in range(2 if double else 1)]
@@ -841,7 +843,7 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
         last = len(calls) - 1
 
         def issue(par=0):
-            IN, OUT = INS[par], OUTS[par]
+            IN, OUT = INS[par % len(INS)], OUTS[par]
             ready = []
             if double:  # the previous step's last output, back while this step computes
                 side_out.wait_stream(stream)
@@ -858,7 +860,7 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
                         ev = torch.cuda.Event()
                         ev.record(side_in)
                         ready.append(ev)
-            elif double:  # this step's inputs came in during the previous step
+            elif double:  # this decode step's inputs came in during the previous step
                 side_in.wait_stream(stream)
                 with torch.cuda.stream(side_in):
                     INS[1 - par].to_dev()
@@ -883,7 +885,7 @@ def run_e2e(args, w, sets, steps_calls, ws, stream, dev, step_bytes, world, dist
                 else:
                     vt.w4a16_gemm(A, W, out=OUT.view(i, (M, p.N), torch.bfloat16),
                                   workspace=ws, stream=stream)
-                if piped and host_out[i]:
+                if piped and host_out[i] and not (double and i == last):
                     side_out.wait_stream(stream)
                     with torch.cuda.stream(side_out):
                         OUT.view(i, (M, p.N), torch.bfloat16, host=True).copy_(
