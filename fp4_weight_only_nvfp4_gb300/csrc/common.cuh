@@ -279,9 +279,12 @@ __device__ __forceinline__ int act_pow2(int mx) {
   return p < -120 ? -120 : (p > 113 ? 113 : p);
 }
 
-// One granule times 2^-p, rounded to f16, as four f16x2 words.
+// 2^k in fp32 for k in [-126, 127] (a normal power of two), from its exponent field.
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// One granule times 2^-p, rounded to f16, as four f16x2 words (p in [-120, 113]).
 __device__ __forceinline__ uint4 act_granule_f16(const uint32_t w[4], int p) {
-  const float down = ldexpf(1.0f, -p);
+  const float down = pow2f(-p);
   uint32_t o[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

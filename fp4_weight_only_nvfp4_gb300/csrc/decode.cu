@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep_a(const __nv_bfloat16* __
   const int p = act_pow2(mx);
   *reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8))) =
       act_granule_f16(w, p);
-  if (gi == 0) ascale[kt * kAScaleStride + m] = ldexpf(1.0f, p);
+  if (gi == 0) ascale[kt * kAScaleStride + m] = pow2f(p);
 }
 
 // W4A4: the same pre-pass with the activations quantised to the weight's block format
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep_a4(const __nv_bfloat16* _
     const int et = aq_mx_exp(__uint_as_float((uint32_t)mt << 16));
     const int p = max(et - 12, -126);
     o = aq_mx_granule(w, aq_mx_exp(amax), p, bad, nullptr);
-    sc = ldexpf(1.0f, p);
+    sc = pow2f(p);
   }
   *reinterpret_cast<uint4*>(Ap + ((kt * rows + m) * 64 + ((gi ^ (m & 7)) * 8))) = o;
   if (gi == 0) ascale[kt * kAScaleStride + m] = sc;
@@ -234,13 +234,14 @@ __device__ __forceinline__ float greedy_value(unsigned long long key) {
 
 // Warp-wide max of the lanes' keys (all 32 lanes take part); lane 0 folds it into the
 // CTA's key of token m in shared memory (keys of one warp always belong to one token m).
+// The 64-bit max is taken as two 32-bit warp reductions: the largest high word, then the
+// largest low word among the lanes that hold it.
 __device__ __forceinline__ void greedy_fold(unsigned long long key, unsigned long long* keys,
                                             int m) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-    key = other > key ? other : key;
-  }
+  const uint32_t hi = (uint32_t)(key >> 32), lo = (uint32_t)key;
+  const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+  key = ((unsigned long long)mhi << 32) | mlo;
   if ((threadIdx.x & 31) == 0 && key) atomicMax(keys + m, key);  // shared-memory atomic
 }
 
@@ -791,7 +792,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         const uint4 o = act_granule_f16(w, pe);
         st_shared_v4(res_u + (uint32_t)(((ktr * M + m) * 64 + ((gi ^ (m & 7)) * 8)) * 2),
                      o.x, o.y, o.z, o.w);
-        if (gi == 0) st_shared_f32(rscale_u + (uint32_t)((ktr * kResScaleStride + m) * 4), ldexpf(1.0f, pe));
+        if (gi == 0) st_shared_f32(rscale_u + (uint32_t)((ktr * kResScaleStride + m) * 4), pow2f(pe));
       }
     };
     if constexpr (GRP) {
@@ -1417,7 +1418,7 @@ __global__ void __launch_bounds__(kGroupThreads) k_group_prep(
     const int pe = act_pow2(mx);
     *reinterpret_cast<uint4*>(Ap + ((rsum * KT + kt * cnt + sx) * 64 + ((gi ^ (sx & 7)) * 8))) =
         act_granule_f16(w, pe);
-    if (gi == 0) ascale[((int64_t)b * KT + kt) * kAScaleStride + sx] = ldexpf(1.0f, pe);
+    if (gi == 0) ascale[((int64_t)b * KT + kt) * kAScaleStride + sx] = pow2f(pe);
   }
 }
 
