@@ -853,6 +853,18 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   };
   const int soff = scale_offset(FMT, 2 * jp, g, t);
   float acc[2][NJ][4];
+  // Greedy head, 8-token tile: the CTA-wide epilogues give thread x the outputs x + j CT
+  // (j < 2, token (x + j CT) / 128) of every tile, so each thread keeps the best key of its
+  // two outputs in registers across tiles and folds them into the CTA's keys once, after its
+  // last tile.  (The 16-token tile folds every tile's keys at once.)
+  constexpr int kEpiIters = (MT * 128 + CT - 1) / CT;
+  [[maybe_unused]] unsigned long long gk_run[kEpiIters];
+#pragma unroll
+  for (int j = 0; j < kEpiIters; ++j) gk_run[j] = 0ull;
+  auto greedy_note = [&](unsigned long long key, int j, int m) {
+    if constexpr (MT == 8) gk_run[j] = key > gk_run[j] ? key : gk_run[j];
+    else greedy_fold(key, s_gkey, m);
+  };
 #pragma unroll
   for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -1133,7 +1145,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
       }
     } else if (!reducer) {  // a reducer adds its slots when the other partials are in
-      for (int idx = threadIdx.x; idx < nout; idx += CT) {
+      // output idx (token idx / 128, tile row idx % 128), the thread's j-th of the tile
+      auto cta_out = [&](int idx, int j) {
         const int m = idx >> 7, row = idx & 127, pr = row >> 5, rr = row & 31;
         float sum = 0.0f;
 #pragma unroll
@@ -1148,7 +1161,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           if (p.g_idx) {  // warp-uniform: a warp's 32 outputs belong to one token
             unsigned long long key = 0;
             if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
-            greedy_fold(key, s_gkey, m);
+            greedy_note(key, j, m);
           } else if (n >= 0) {
             const float f = n < p.seg_split ? f0 : f1;
             p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
@@ -1156,6 +1169,16 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
         } else if (!reducer) {
           p.partials[((size_t)c * 2 * MT + m) * 128 + row] = sum;
         }
+      };
+      if constexpr (MT == 8) {
+#pragma unroll
+        for (int j = 0; j < kEpiIters; ++j) {
+          const int idx = threadIdx.x + j * CT;
+          if (idx >= nout) break;
+          cta_out(idx, j);
+        }
+      } else {
+        for (int idx = threadIdx.x; idx < nout; idx += CT) cta_out(idx, 0);
       }
     }
     if (!complete && !reducer) {
@@ -1216,7 +1239,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
               p.C[(int64_t)m * p.ldc + i] = __float2bfloat16_rn(silu_f(gs * f0) * (us * f1));
           }
         }
-        for (int idx = threadIdx.x; idx < (p.silu ? 0 : nout); idx += CT) {
+        auto red_out = [&](int idx, int j) {
           const int m = idx >> 7, row = idx & 127;
           const float sum = tile_sum(m, row);
           const int64_t prow = GRP ? (rt - (int64_t)gprob * p.RT) * kTileRows + row
@@ -1226,11 +1249,22 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
           if (p.g_idx) {
             unsigned long long key = 0;
             if (n >= 0) key = greedy_key(__float2bfloat16_rn(sum * (n < p.seg_split ? f0 : f1)), n);
-            greedy_fold(key, s_gkey, m);
+            greedy_note(key, j, m);
           } else if (n >= 0) {
             const float f = n < p.seg_split ? f0 : f1;
             p.C[crow * p.ldc + n] = __float2bfloat16_rn(sum * f);
           }
+        };
+        const int nred = p.silu ? 0 : nout;
+        if constexpr (MT == 8) {
+#pragma unroll
+          for (int j = 0; j < kEpiIters; ++j) {
+            const int idx = threadIdx.x + j * CT;
+            if (idx >= nred) break;
+            red_out(idx, j);
+          }
+        } else {
+          for (int idx = threadIdx.x; idx < nred; idx += CT) red_out(idx, 0);
         }
       }
     }
@@ -1248,6 +1282,14 @@ __global__ void __launch_bounds__(kConsumerWarps * 32 + 64, 1) k_decode(const De
   }
   if (!ok && lane == 0) atomicExch(p.status, 5);
   if (p.g_idx) {
+    if constexpr (MT == 8) {
+      // the running keys of the CTA-wide epilogues (warp-uniform token per j)
+#pragma unroll
+      for (int j = 0; j < kEpiIters; ++j) {
+        const int idx = threadIdx.x + j * CT;
+        if (idx < M * 128) greedy_fold(gk_run[j], s_gkey, idx >> 7);
+      }
+    }
     // One global atomic per token per CTA; the last CTA to finish turns the keys into
     // indices and values and clears them (and the counter) for the next call.
     consumer_sync(CT);
