@@ -98,3 +98,28 @@ def test_greedy_keys_reset_between_calls():
         assert np.array_equal(tok.cpu().numpy(), own), rep
     head = ws[:256].cpu().numpy()
     assert not head[64:64 + 16 * 8 + 4].any()  # keys and counter are back to zero
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+def test_greedy_many_tiles_per_cta_three_to_sixteen_tokens(fmt):
+    # 469 row tiles of 4 k tiles: the default launch gives each CTA about four tiles, some
+    # shared with a neighbour, so the 8-token tile carries each thread's best keys across
+    # tiles (complete and reduced) before folding them; 16 tokens fold per tile
+    N, K = 60000, 256
+    codes, scales, G = make_weight(fmt, synth.tensor_id(88, fmt, 1), N, K)
+    W = vt.PackedWeight.from_codes(to_dev(codes), to_dev(scales), G, fmt, N, K)
+    ws = W.new_workspace(16)
+    for M in (3, 5, 8, 16):
+        Ab = make_acts(synth.tensor_id(88, fmt, 2, M), M, K)
+        A = bf16_dev(Ab)
+        y = vt.w4a16_gemm(A, W, workspace=ws)
+        tok, val = vt.w4a16_gemm_greedy(A, W, workspace=ws)
+        torch.cuda.synchronize()
+        st = W.stats()
+        assert st["tile_epilogue"] == 0 and st["items"] >= 3 * 4 * st["grid"], st  # >= 3 tiles per CTA
+        own, f = _first_argmax(bf16_host_bits(y))
+        tok = tok.cpu().numpy()
+        assert np.array_equal(tok, own), (M, tok, own)
+        assert np.array_equal(val.cpu().numpy(), f[np.arange(M), own])
+        check_against_oracle(tok, Ab, codes, scales, G, fmt, N, what=f"many tiles fmt={fmt} M={M}")
+    assert vt.workspace_status(ws) == 0
