@@ -109,6 +109,40 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// The same load, only issued: the registers are valid after tmem_ld_wait on them.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for every TMEM load this thread issued; v (the last one's registers) is read
+// and written by the wait, so no use of v moves above it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+        "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+        "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]),
+        "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]),
+        "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+      :
+      : "memory");
+}
+// 32 bytes to global memory in one store (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(ptr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 // 2-D tiled TMA load (tensor map in kernel parameter space), completion on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar, uint64_t policy) {
@@ -173,6 +207,7 @@ struct PrefillParams {
   __nv_bfloat16* C;
   int* status;
   int vec_store;     // C 16-byte aligned and ldc % 8 == 0
+  int vec32_store;   // C 32-byte aligned and ldc % 16 == 0
   int pair_store;    // C 4-byte aligned and ldc even: two outputs per 32-bit store
   uint64_t wait_ns;  // limit of every bounded wait
   int withhold;      // test hook: issue no copies (the waits then run out)
@@ -485,6 +520,68 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
+      if (!p.silu && p.layout != kLayoutPaired && p.vec_store) {
+        // Plain layout with vector stores: chunk c + 1's TMEM load is in flight while chunk
+        // c is scaled, rounded and stored (32 columns of this lane's token row per chunk).
+        const int64_t ncol = p.N - nt * kBN;  // valid columns of the tile, > 0
+        const int nch = ncol >= kBN ? kBN / 32 : (int)((ncol + 31) / 32);
+        const uint32_t tb = tmem + ab * kBN + ((uint32_t)(qd * 32) << 16);
+        auto chunk = [&](const uint32_t (&v)[32], int c) {
+          if (!live) return;
+          const int64_t n0 = nt * kBN + c * 32;
+          uint32_t o[16];
+          if (n0 + 32 <= p.seg_split || n0 >= p.seg_split) {  // one global for the chunk
+            const float f = n0 < p.seg_split ? f0 : f1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * rs * f,
+                                                       __uint_as_float(v[2 * i + 1]) * rs * f);
+              o[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t n = n0 + 2 * i;
+              const float fa = n < p.seg_split ? f0 : f1, fb = (n + 1) < p.seg_split ? f0 : f1;
+              __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * rs * fa,
+                                                       __uint_as_float(v[2 * i + 1]) * rs * fb);
+              o[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+          }
+          if (n0 + 32 <= p.N) {
+            if (p.vec32_store) {
+              st_global_v8(crow + n0, o);
+              st_global_v8(crow + n0 + 16, o + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(crow + n0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t n = n0 + 2 * i;
+              if (n + 1 < p.N) {
+                *reinterpret_cast<uint32_t*>(crow + n) = o[i];
+              } else if (n < p.N) {
+                *reinterpret_cast<uint16_t*>(crow + n) = (uint16_t)(o[i] & 0xFFFFu);
+              }
+            }
+          }
+        };
+        uint32_t va[32], vb[32];
+        tmem_ld32_issue(tb, va);
+        for (int c = 0; c < nch; c += 2) {
+          tmem_ld_wait(va);
+          if (c + 1 < nch) tmem_ld32_issue(tb + (uint32_t)(c + 1) * 32, vb);
+          chunk(va, c);
+          if (c + 1 < nch) {
+            tmem_ld_wait(vb);
+            if (c + 2 < nch) tmem_ld32_issue(tb + (uint32_t)(c + 2) * 32, va);
+            chunk(vb, c + 1);
+          }
+        }
+      } else
       for (int c = 0; c < (p.silu ? 0 : kBN / 32); ++c) {
         const int64_t n0 = nt * kBN + c * 32;
         // warp-uniform; paired tiles map columns past N onto valid up rows, so they check
@@ -758,6 +855,7 @@ cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s, int* launches
   pp.C = reinterpret_cast<__nv_bfloat16*>(L.C);
   pp.status = L.status;
   pp.vec_store = ((uintptr_t)L.C % 16 == 0) && (L.ldc % 8 == 0);
+  pp.vec32_store = ((uintptr_t)L.C % 32 == 0) && (L.ldc % 16 == 0);
   pp.pair_store = ((uintptr_t)L.C % 4 == 0) && (L.ldc % 2 == 0);
   pp.wait_ns = L.wait_ns ? L.wait_ns : 2000000000ull;
   pp.withhold = L.withhold;
