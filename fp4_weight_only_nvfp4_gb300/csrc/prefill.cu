@@ -569,17 +569,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
           }
         };
+        // Straight-line over the 8 chunks, every load issued (the columns past N are TMEM
+        // of this accumulator and are not stored): an issued load's registers are written
+        // asynchronously, so no branch merge or loop edge may carry them to their wait.
         uint32_t va[32], vb[32];
         tmem_ld32_issue(tb, va);
-        for (int c = 0; c < nch; c += 2) {
+#pragma unroll
+        for (int c = 0; c < kBN / 32; c += 2) {
           tmem_ld_wait(va);
-          if (c + 1 < nch) tmem_ld32_issue(tb + (uint32_t)(c + 1) * 32, vb);
-          chunk(va, c);
-          if (c + 1 < nch) {
-            tmem_ld_wait(vb);
-            if (c + 2 < nch) tmem_ld32_issue(tb + (uint32_t)(c + 2) * 32, va);
-            chunk(vb, c + 1);
-          }
+          tmem_ld32_issue(tb + (uint32_t)(c + 1) * 32, vb);
+          if (c < nch) chunk(va, c);
+          tmem_ld_wait(vb);
+          if (c + 2 < kBN / 32) tmem_ld32_issue(tb + (uint32_t)(c + 2) * 32, va);
+          if (c + 1 < nch) chunk(vb, c + 1);
         }
       } else
       for (int c = 0; c < (p.silu ? 0 : kBN / 32); ++c) {
