@@ -22,7 +22,7 @@ class LaunchInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("warps_per_cta", ctypes.c_int),
                 ("m_tile", ctypes.c_int), ("items", ctypes.c_int64),
                 ("launches", ctypes.c_int64), ("calls", ctypes.c_int64),
-                ("tile_epilogue", ctypes.c_int)]
+                ("tile_epilogue", ctypes.c_int), ("stage_k_tiles", ctypes.c_int)]
 
 
 class GemmOpts(ctypes.Structure):

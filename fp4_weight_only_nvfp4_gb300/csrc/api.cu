@@ -196,7 +196,7 @@ vt_status vt::decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_op
                            bool w4a4, DecodeShape* out) {
   const int64_t items = W->RT * W->KT;
   // k tiles per pipeline stage (8: up to 37 KB of weights per TMA copy) and ring depth
-  const int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
+  int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
   if (ks != 4 && ks != 8) return fail(VT_ERR_INVALID_ARG, "stage width must be 4 or 8 k tiles");
   // small M * K: the decode kernel converts the activations itself (no pre-pass)
   const bool resident = !w4a4 && !(opts && opts->force_path == 3) &&
@@ -218,6 +218,17 @@ vt_status vt::decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_op
   if (grid > items) grid = items;
   if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
   if (grid < 1) grid = 1;
+  // 3 to 8 tokens on a long call (at least three row tiles per CTA, the activations from the
+  // pre-pass): stages of 16 k tiles, half the per-stage work per weight of the consumers,
+  // which bound such calls (lm_head M = 8 -4 %); the shorter calls keep 8 (two 16-tile stages
+  // hold fewer bytes in flight than six of 8, and lose ~2 %)
+  if (!(opts && opts->warps) && W->E <= 1 && !resident && M > 2 && M <= 8 &&
+      items >= 3 * W->KT * grid &&
+      decode_smem_bytes(W->fmt, M, 16, 2, 0) <= 226 * 1024) {
+    ks = 16;
+    stages = 6;
+    while (stages > 2 && decode_smem_bytes(W->fmt, M, ks, stages, 0) > 226 * 1024) --stages;
+  }
   out->ks = ks;
   out->stages = stages;
   out->grid = (int)grid;
@@ -422,6 +433,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     W->info.path = 1;
     W->info.tile_epilogue = sh.epi;
+    W->info.stage_k_tiles = sh.ks;
     W->info.grid = D.grid;
     W->info.warps_per_cta = 18;  // 16 consumer warps, the TMA producer, the publisher
     W->info.m_tile = mt;
@@ -461,6 +473,7 @@ vt_status gemm_impl(const void* A, int64_t M, int64_t lda, vt_fp4_handle W, void
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   W->info.path = 2;
   W->info.tile_epilogue = 0;
+  W->info.stage_k_tiles = 1;
   W->info.grid = grid;
   W->info.warps_per_cta = 14;  // TMA, MMA, 8 dequantiser and 4 epilogue warps
   W->info.m_tile = 128;
@@ -558,6 +571,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   if (e != cudaSuccess) return cuda_fail(e, "grouped decode launch");
   W->info.path = 3;
   W->info.tile_epilogue = 0;
+  W->info.stage_k_tiles = D.ks;
   W->info.grid = D.grid;
   W->info.warps_per_cta = 18;
   W->info.m_tile = mrows;

@@ -1555,8 +1555,11 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t s, int* launches) 
                              L.alpha, 6.0f * L.alpha, L.counters, L.RT);
     if (e != cudaSuccess) return e;
   }
-  // stage width in k tiles (KS): 4 or 8
-  if (L.ks == 4) {
+  // stage width in k tiles (KS): 4, 8, or 16 (8-token tile only)
+  if (L.ks == 16) {
+    if (mt != 8) return cudaErrorInvalidValue;
+    e = (L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 16>(L, s) : launch_t<FMT_MX, 8, 16>(L, s);
+  } else if (L.ks == 4) {
     if (L.fmt == FMT_NV) e = (mt == 8) ? launch_t<FMT_NV, 8, 4>(L, s) : launch_t<FMT_NV, 16, 4>(L, s);
     else e = (mt == 8) ? launch_t<FMT_MX, 8, 4>(L, s) : launch_t<FMT_MX, 16, 4>(L, s);
   } else {

@@ -137,6 +137,7 @@ extern "C" vt_status vt_fp4_w4a16_gemm_noalloc(const void* A, int64_t M, int64_t
   if (e != cudaSuccess) return cuda_err(e);
   W->info.path = 1;
   W->info.tile_epilogue = sh.epi;
+  W->info.stage_k_tiles = sh.ks;
   W->info.grid = D.grid;
   W->info.warps_per_cta = 18;
   W->info.m_tile = mt;

@@ -64,7 +64,7 @@ def test_greedy_head_on_a_weight_of_many_row_tiles(fmt):
         Ab = make_acts(synth.tensor_id(87, fmt, 6, M), M, K)
         A = bf16_dev(Ab)
         y = vt.w4a16_gemm(A, W, workspace=ws)
-        assert W.stats()["tile_epilogue"] == 1
+        assert W.stats()["tile_epilogue"] == 1 and W.stats()["stage_k_tiles"] == 8
         tok, val = vt.w4a16_gemm_greedy(A, W, workspace=ws)
         torch.cuda.synchronize()
         assert W.stats()["tile_epilogue"] == 1
