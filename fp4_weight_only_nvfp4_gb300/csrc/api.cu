@@ -198,8 +198,19 @@ vt_status vt::decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_op
   // k tiles per pipeline stage (8: up to 37 KB of weights per TMA copy) and ring depth
   int ks = (opts && opts->warps) ? opts->warps : 8;  // opts->warps selects the stage width
   if (ks != 4 && ks != 8) return fail(VT_ERR_INVALID_ARG, "stage width must be 4 or 8 k tiles");
+  // A long call (at least three row tiles per CTA of the default grid; bound by the
+  // consumers) of up to 8 tokens and more than 4096 activation elements streams stages of
+  // 16 k tiles, with the activations from the pre-pass: half the per-stage work per weight
+  // (lm_head K = 5120: M = 1 -4 %, M = 2 -6 %, M = 8 -4 %).  Smaller activations keep the
+  // in-kernel conversion and 8-tile stages (K = 2560, M = 1: +1.3 % with 16), and so do the
+  // shorter calls (two 16-tile stages hold fewer bytes in flight than six of 8: ~2 % slower).
+  const int64_t g8 = sm_count() < cdiv(items, 16) ? sm_count() : cdiv(items, 16);
+  const bool long16 = !(opts && (opts->warps || opts->grid || opts->stages)) && W->E <= 1 &&
+                      M <= 8 && (int64_t)M * W->K > 4096 && items >= 3 * W->KT * g8 &&
+                      decode_smem_bytes(W->fmt, M, 16, 2, 0) <= 226 * 1024;
+  if (long16) ks = 16;
   // small M * K: the decode kernel converts the activations itself (no pre-pass)
-  const bool resident = !w4a4 && !(opts && opts->force_path == 3) &&
+  const bool resident = !w4a4 && !(opts && opts->force_path == 3) && !long16 &&
                         decode_resident_ok(M, W->KT, W->RT);
   const int64_t rkt = resident ? W->KT : 0;
   int stages = (opts && opts->stages) ? opts->stages : 0;
@@ -218,17 +229,6 @@ vt_status vt::decode_shape(const vt_fp4_weight_s* W, int M, const vt_fp4_gemm_op
   if (grid > items) grid = items;
   if (grid > kMaxDecodeGrid) grid = kMaxDecodeGrid;
   if (grid < 1) grid = 1;
-  // 3 to 8 tokens on a long call (at least three row tiles per CTA, the activations from the
-  // pre-pass): stages of 16 k tiles, half the per-stage work per weight of the consumers,
-  // which bound such calls (lm_head M = 8 -4 %); the shorter calls keep 8 (two 16-tile stages
-  // hold fewer bytes in flight than six of 8, and lose ~2 %)
-  if (!(opts && opts->warps) && W->E <= 1 && !resident && M > 2 && M <= 8 &&
-      items >= 3 * W->KT * grid &&
-      decode_smem_bytes(W->fmt, M, 16, 2, 0) <= 226 * 1024) {
-    ks = 16;
-    stages = 6;
-    while (stages > 2 && decode_smem_bytes(W->fmt, M, ks, stages, 0) > 226 * 1024) --stages;
-  }
   out->ks = ks;
   out->stages = stages;
   out->grid = (int)grid;

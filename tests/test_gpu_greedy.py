@@ -104,9 +104,9 @@ def test_greedy_keys_reset_between_calls():
 def test_greedy_many_tiles_per_cta_three_to_sixteen_tokens(fmt):
     # 469 row tiles of 32 k tiles: the default launch gives each CTA about three tiles, some
     # shared with a neighbour, so the 8-token tile carries each thread's best keys across
-    # tiles (complete and reduced) before folding them; 16 tokens fold per tile.  With the
-    # activation pre-pass (5 and 8 tokens here; 3 are converted in the kernel) such a call
-    # takes stages of 16 k tiles
+    # tiles (complete and reduced) before folding them; 16 tokens fold per tile.  Up to 8
+    # tokens such a call (more than 4096 activation elements) takes the activation pre-pass
+    # and stages of 16 k tiles
     N, K = 60000, 2048
     codes, scales, G = make_weight(fmt, synth.tensor_id(88, fmt, 1), N, K)
     W = vt.PackedWeight.from_codes(to_dev(codes), to_dev(scales), G, fmt, N, K)
@@ -117,12 +117,12 @@ def test_greedy_many_tiles_per_cta_three_to_sixteen_tokens(fmt):
         y = vt.w4a16_gemm(A, W, workspace=ws)
         torch.cuda.synchronize()
         st = W.stats()
-        assert st["stage_k_tiles"] == (16 if M in (5, 8) else 8) and st["launches"] == (1 if M == 3 else 2), (M, st)
+        assert st["stage_k_tiles"] == (16 if M <= 8 else 8) and st["launches"] == 2, (M, st)
         tok, val = vt.w4a16_gemm_greedy(A, W, workspace=ws)
         torch.cuda.synchronize()
         st = W.stats()
         assert st["tile_epilogue"] == 0 and st["items"] >= 3 * (K // 64) * st["grid"], st  # >= 3 tiles per CTA
-        assert st["stage_k_tiles"] == (16 if M in (5, 8) else 8), (M, st)
+        assert st["stage_k_tiles"] == (16 if M <= 8 else 8), (M, st)
         own, f = _first_argmax(bf16_host_bits(y))
         tok = tok.cpu().numpy()
         assert np.array_equal(tok, own), (M, tok, own)
