@@ -84,7 +84,9 @@ typedef struct {
 /* Optional overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
 typedef struct {
   int grid;      /* decode: number of CTAs (clamped to [1, 512]); prefill: CTAs (>= 1) */
-  int warps;     /* decode: k tiles (of 64) per pipeline stage, 4 or 8 */
+  int warps;     /* decode: k tiles (of 64) per pipeline stage, 4 or 8 (the library's own
+                    choice is 8, or 16 for the long calls that stage_k_tiles describes;
+                    setting grid, warps or stages keeps it from choosing 16) */
   int stages;    /* decode: depth of the CTA's TMA ring, 2..16 */
   int force_path;/* 1 decode (requires M <= 16), 2 prefill, 3 decode with the activations
                     always converted by the pre-pass kernel (small M * K otherwise converts
