@@ -521,7 +521,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   if (ws_bytes < L.total)
     return fail(VT_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, L.total);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  const int ks = 8;
+  int ks = 8;
   // token tile of the decode kernel: 8 rows when M <= 8 (an expert then has at most M pairs
   // unless a token names it twice; such extra pairs are left out), else 16
   const int mrows = decode_mt((int)M);
@@ -529,6 +529,13 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   // kernel groups the routing and converts the activations itself (one kernel, no pre-pass)
   const bool resident = mrows == 8 && decode_resident_bytes(mrows, W->KT) <= kGroupedResidentMaxBytes;
   const int64_t rkt = resident ? W->KT : 0;
+  {  // long calls (at least three row tiles per CTA for the routing's upper bound on experts
+     // named): 16-k-tile stages halve the consumers' per-stage waits and releases
+    const int64_t pm = M * topk < W->E ? M * topk : W->E;
+    if (resident && pm * W->RT * W->KT >= 3 * W->KT * sm_count() &&
+        decode_smem_bytes(W->fmt, mrows, 16, 2, rkt) <= 222 * 1024)
+      ks = 16;
+  }
   int stages = 6;  // the grouped kernel also holds ~3.5 KB of static shared memory (the grouping)
   while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages, rkt) > 222 * 1024) --stages;
   if (decode_smem_bytes(W->fmt, mrows, ks, stages, rkt) > 222 * 1024)

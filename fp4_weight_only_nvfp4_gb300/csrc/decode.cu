@@ -1476,10 +1476,13 @@ cudaError_t launch_decode_grouped(const DecodeLaunch& L0, const int32_t* topk_id
   cudaError_t e = cudaSuccess;
   if (L.resident) {  // one kernel: it groups the routing and converts the activations itself
     if (decode_mt(L.M) != 8) return cudaErrorInvalidValue;
-    e = (L.ks == 4) ? ((L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 4, true, true>(L, s)
-                                         : launch_t<FMT_MX, 8, 4, true, true>(L, s))
-                    : ((L.fmt == FMT_NV) ? launch_t<FMT_NV, 8, 8, true, true>(L, s)
-                                         : launch_t<FMT_MX, 8, 8, true, true>(L, s));
+    const bool nv = L.fmt == FMT_NV;
+    if (L.ks == 16)
+      e = nv ? launch_t<FMT_NV, 8, 16, true, true>(L, s) : launch_t<FMT_MX, 8, 16, true, true>(L, s);
+    else if (L.ks == 4)
+      e = nv ? launch_t<FMT_NV, 8, 4, true, true>(L, s) : launch_t<FMT_MX, 8, 4, true, true>(L, s);
+    else
+      e = nv ? launch_t<FMT_NV, 8, 8, true, true>(L, s) : launch_t<FMT_MX, 8, 8, true, true>(L, s);
     if (launches) *launches = 1;
     return e;
   }

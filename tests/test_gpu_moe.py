@@ -167,3 +167,23 @@ def test_moe_one_kernel_mode_ragged_k(fmt):
         assert W.stats()["launches"] == 1
         check_rows(y.float().cpu().numpy(), _oracle(fmt, Ab, srcs, ids, N),
                    what=f"moe ragged K fmt={fmt} M={M}")
+
+
+@pytest.mark.parametrize("fmt", [vt.NVFP4, vt.MXFP4])
+def test_moe_long_one_kernel_call_uses_16_k_tile_stages(fmt):
+    """16 experts of 3700 x 2048 (29 row tiles, the last ragged): 8 tokens that may name all 16
+    experts give at least three row tiles per CTA, so the one-launch mode stages 16 k tiles at
+    a time; one token naming 8 experts stays at 8.  Both against the oracle, row by row."""
+    E, N, K = 16, 3700, 2048
+    srcs, W = _experts(fmt, E, N, K, 50 + fmt)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for M, topk in ((8, 8), (8, 2), (1, 8)):
+        ids = _routing(M, topk, E, seed=M * 13 + topk)
+        Ab = make_acts(synth.tensor_id(89, 50 + fmt, M, topk), M, K)
+        y = vt.w4a16_gemm_moe(bf16_dev(Ab), W, to_dev(ids))
+        torch.cuda.synchronize()
+        st = W.stats()
+        long_call = min(M * topk, E) * 29 >= 3 * sms
+        assert st["launches"] == 1 and st["stage_k_tiles"] == (16 if long_call else 8), (M, st)
+        check_rows(y.float().cpu().numpy(), _oracle(fmt, Ab, srcs, ids, N),
+                   what=f"moe long call fmt={fmt} M={M} topk={topk}")
