@@ -77,8 +77,9 @@ typedef struct {
                          (up to 2 tokens, at least three row tiles per CTA), else 0 */
   int stage_k_tiles;  /* decode and grouped: 64-wide k tiles per pipeline stage (4, 8, or 16
                          for up to 8 tokens and more than 4096 activation elements on a call
-                         of at least three row tiles per CTA); prefill: 1 (one 64-wide k
-                         step per stage) */
+                         of at least three row tiles per CTA; grouped: 16 in the one-launch
+                         mode when min(M * topk, E) experts give at least three row tiles
+                         per CTA); prefill: 1 (one 64-wide k step per stage) */
 } vt_fp4_launch_info;
 
 /* Optional overrides for vt_fp4_w4a16_gemm_ex (0 = library choice). */
