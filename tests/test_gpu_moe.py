@@ -148,6 +148,9 @@ def test_moe_both_grouped_modes_match_oracle(fmt):
             torch.cuda.synchronize()
             st = W.stats()
             assert st["m_tile"] == 8 and st["launches"] == launches, (K, M, st)
+            tiles = min(M * topk, E) * 3  # 384 rows: three row tiles per expert
+            if launches == 1 and tiles <= torch.cuda.get_device_properties(0).multi_processor_count:
+                assert st["grid"] == tiles, (K, M, st)  # one whole row tile per CTA
             check_rows(y.float().cpu().numpy(), _oracle(fmt, Ab, srcs, ids, N),
                        what=f"moe fmt={fmt} K={K} M={M}")
         assert vt.workspace_status(ws) == 0
