@@ -581,7 +581,7 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
                                         (cudaStream_t)s, &launches);
   if (e != cudaSuccess) return cuda_fail(e, "grouped decode launch");
   W->info.path = 3;
-  W->info.tile_epilogue = 0;
+  W->info.tile_epilogue = resident ? 1 : 0;  // one-launch mode: the per-group epilogue
   W->info.stage_k_tiles = D.ks;
   W->info.grid = D.grid;
   W->info.warps_per_cta = 18;

@@ -74,7 +74,9 @@ typedef struct {
   int64_t launches;   /* kernels enqueued by that call */
   int64_t calls;      /* GEMM calls made on this handle so far */
   int tile_epilogue;  /* decode: 1 when complete row tiles were summed per row-block group
-                         (up to 2 tokens, at least three row tiles per CTA), else 0 */
+                         (up to 2 tokens, at least three row tiles per CTA), else 0; grouped:
+                         1 in the one-launch mode, whose complete tiles of problems of up to
+                         2 slots are summed that way */
   int stage_k_tiles;  /* decode and grouped: 64-wide k tiles per pipeline stage (4, 8, or 16
                          for up to 8 tokens and more than 4096 activation elements on a call
                          of at least three row tiles per CTA; grouped: 16 in the one-launch
