@@ -56,7 +56,8 @@ struct DecodeLaunch {
                     // the decode kernel groups the routing and converts A itself, no pre-pass
   int Mtok = 0, topk = 0;  // grouped resident mode: tokens of A, slots per token
   int epi = 0;  // 8 k tiles per stage, M <= 8: the per-group epilogue for complete tiles of
-                // up to 2 tokens (decode_shape chooses it)
+                // up to 2 tokens (decode_shape chooses it; the grouped one-launch mode takes
+                // it at 8 and 16 k tiles per stage, for problems of up to 2 slots)
 };
 int decode_mt(int M);  // 8 or 16
 // Resident-activation decode (small M * K): the decode kernel converts A into shared memory
