@@ -54,6 +54,26 @@ def test_header_compiles_as_plain_c(tmp_path):
                     "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
 
 
+@pytest.mark.parametrize("cname,pytype", [("vt_fp4_launch_info", "LaunchInfo"),
+                                           ("vt_fp4_gemm_opts", "GemmOpts")])
+def test_binding_structs_match_the_header_layout(tmp_path, cname, pytype):
+    """The ctypes structures of the binding have the header's field names, offsets and size
+    (a plain C program built against the header prints them)."""
+    st = getattr(_lib, pytype)
+    names = [f for f, _ in st._fields_]
+    body = "".join(f'printf("%zu ", offsetof({cname}, {f}));' for f in names)
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "vt_fp4.h"\n'
+                   f'int main(void){{{body}printf("%zu\\n", sizeof({cname}));return 0;}}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                    str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [getattr(st, f).offset for f in names] + [ctypes.sizeof(st)]
+    assert got == want, (cname, names, got, want)
+
+
 def test_prepack_bytes_exact(L):
     assert vt.prepack_bytes(vt.NVFP4, 2048, 1024) == 256 + 16 * 16 * 4608
     assert vt.prepack_bytes(vt.MXFP4, 24576, 4096) == 256 + 192 * 64 * 4352
