@@ -46,6 +46,42 @@ def test_library_exports_every_declared_symbol(L):
         assert getattr(L, n) is not None
 
 
+def _c_kind(t):
+    t = " ".join(t.split())
+    if "*" in t or re.match(r"^(const )?(vt_fp4_handle|vt_stream_t)$", t):
+        return "ptr"
+    base = re.sub(r"\bconst\b", "", t).split()[0]
+    return {"int64_t": "i64", "size_t": "size", "int": "int", "int32_t": "int",
+            "vt_fp4_format": "int", "vt_status": "int", "float": "f32", "double": "f64",
+            "void": "void"}.get(base, "unknown " + base)
+
+
+def _py_kind(c):
+    if c is None:
+        return "void"
+    if c in (ctypes.c_void_p, ctypes.c_char_p) or isinstance(getattr(c, "_type_", None), type):
+        return "ptr"
+    return {ctypes.c_int64: "i64", ctypes.c_size_t: "size", ctypes.c_int: "int",
+            ctypes.c_float: "f32", ctypes.c_double: "f64"}.get(c, "unknown " + repr(c))
+
+
+def test_binding_signatures_match_the_header_prototypes():
+    """Every prototype's return and parameter types (by class: pointer, 32- or 64-bit
+    integer, size, float) agree with the binding's ctypes signature table."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = re.findall(r"([\w \t\*]+?)\b(vt_fp4_\w+)\s*\(([^)]*)\)\s*;", src)
+    assert {n for _, n, _ in protos} == set(_lib.SIGNATURES)
+    for ret, name, params in protos:
+        ps = [x.strip() for x in params.split(",") if x.strip()]
+        if ps == ["void"]:
+            ps = []
+        # a parameter is "type name" with the pointer star on the type
+        want = [_c_kind(x.rsplit(None, 1)[0]) for x in ps]
+        res, args = _lib.SIGNATURES[name]
+        assert [_py_kind(a) for a in args] == want, name
+        assert _py_kind(res) == _c_kind(ret), name
+
+
 def test_header_compiles_as_plain_c(tmp_path):
     src = tmp_path / "t.c"
     src.write_text('#include "vt_fp4.h"\nint main(void){vt_fp4_format f = VT_FP4_MXFP4;'
