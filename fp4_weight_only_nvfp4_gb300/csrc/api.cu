@@ -529,19 +529,18 @@ vt_status vt_fp4_w4a16_gemm_moe(const void* A, int64_t M, int64_t lda, vt_fp4_ha
   // kernel groups the routing and converts the activations itself (one kernel, no pre-pass)
   const bool resident = mrows == 8 && decode_resident_bytes(mrows, W->KT) <= kGroupedResidentMaxBytes;
   const int64_t rkt = resident ? W->KT : 0;
-  {  // long calls (at least three row tiles per CTA for the routing's upper bound on experts
-     // named): 16-k-tile stages halve the consumers' per-stage waits and releases
-    const int64_t pm = M * topk < W->E ? M * topk : W->E;
-    if (resident && pm * W->RT * W->KT >= 3 * W->KT * sm_count() &&
-        decode_smem_bytes(W->fmt, mrows, 16, 2, rkt) <= 222 * 1024)
-      ks = 16;
-  }
+  // the routing names at most pmax experts (the grouping finds how many it does)
+  const int64_t pmax = npairs < W->E ? npairs : W->E;
+  // long calls (at least three row tiles per CTA for pmax experts): 16-k-tile stages halve
+  // the consumers' per-stage waits and releases
+  if (resident && pmax * W->RT >= 3 * (int64_t)sm_count() &&
+      decode_smem_bytes(W->fmt, mrows, 16, 2, rkt) <= 222 * 1024)
+    ks = 16;
   int stages = 6;  // the grouped kernel also holds ~3.5 KB of static shared memory (the grouping)
   while (stages > 2 && decode_smem_bytes(W->fmt, mrows, ks, stages, rkt) > 222 * 1024) --stages;
   if (decode_smem_bytes(W->fmt, mrows, ks, stages, rkt) > 222 * 1024)
     return fail(VT_ERR_UNSUPPORTED, "K too large for the grouped kernel's shared memory");
-  const int64_t pmax = npairs < W->E ? npairs : W->E;
-  const int64_t items = pmax * W->RT * W->KT;  // an upper bound: the pre-pass finds P
+  const int64_t items = pmax * W->RT * W->KT;  // an upper bound
   int64_t grid = sm_count();
   if (grid > cdiv(items, 2 * ks)) grid = cdiv(items, 2 * ks);
   // one-launch mode whose row tiles (by the routing's upper bound) fit the SMs: one whole row
